@@ -1,0 +1,167 @@
+/*
+ * nvfp4mla: NVFP4-compressed paged MLA cache write and sparse MLA decode on
+ * GB300 (sm_103a). C ABI; plain pointers and sizes only.
+ *
+ * The method (sources are named per call below):
+ *   "Prime Inference: fast, reliable serving for frontier open models"
+ *   (translated launch post), section "Decode: NVFP4 KV compression";
+ *   "Prime Inference: serving GLM-5.3 to agents is a KV-cache problem",
+ *   sections "Four bits per latent value: where 352 comes from" and "A kernel
+ *   that reads four bits directly"; the "TokenSpeed" engine walkthrough,
+ *   section 8 "MLA KV layout" and its MLA decode benchmark example.
+ *
+ * Common rules for every call:
+ *   - All pointers except dev_status may be NULL only where stated. Data
+ *     pointers are DEVICE pointers of the current CUDA device.
+ *   - The caller owns every buffer. The library never allocates, never frees
+ *     and never synchronises; all work is enqueued on `stream` (a
+ *     cudaStream_t; NULL = legacy default stream) and the call returns before
+ *     the work finishes.
+ *   - Problems the host can see (bad sizes, NULL pointers, misalignment, a
+ *     workspace that is too small) return a non-zero status before anything
+ *     is enqueued. A failed launch returns NVFP4MLA_ERR_CUDA.
+ *   - Problems in the data (bad indices, bad page-table entries, bad slots)
+ *     never fault: the entry is skipped and counted in dev_status.
+ *   - The library keeps no state between calls and may be called from
+ *     several host threads at once (on different streams or the same one).
+ */
+#ifndef NVFP4MLA_H_
+#define NVFP4MLA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes. */
+enum {
+  NVFP4MLA_OK = 0,
+  NVFP4MLA_ERR_INVALID_ARG = 1, /* NULL pointer, negative or unsupported size       */
+  NVFP4MLA_ERR_ALIGNMENT = 2,   /* a pointer or stride breaks the alignment rules   */
+  NVFP4MLA_ERR_UNSUPPORTED = 3, /* valid request this build does not handle         */
+  NVFP4MLA_ERR_WORKSPACE = 4,   /* workspace NULL or smaller than required          */
+  NVFP4MLA_ERR_CUDA = 5         /* a CUDA call or kernel launch failed              */
+};
+
+/* Row format constants (bytes / values). */
+#define NVFP4MLA_LATENT_DIM 512   /* latent values per row                        */
+#define NVFP4MLA_ROPE_DIM 64      /* rope values per row                          */
+#define NVFP4MLA_QK_DIM 576       /* 512 + 64: width of an absorbed query         */
+#define NVFP4MLA_ROW_BYTES 352    /* 256 nibble bytes + 32 scale bytes + 64 rope  */
+#define NVFP4MLA_PAGE_TOKENS 64   /* tokens per cache page                        */
+#define NVFP4MLA_MAX_TOPK 8192    /* largest index list per query                 */
+
+/* Words of the optional device status array (int32[NVFP4MLA_STATUS_WORDS]).
+ * The library only ever adds to them (atomically); the caller zeroes them. */
+#define NVFP4MLA_STAT_BAD_INDEX 0 /* index entries other than -1 left out: < -1,
+                                     >= seq_len, or past the causal position    */
+#define NVFP4MLA_STAT_BAD_PAGE 1  /* entries left out because idx/64 is not a
+                                     page-table column or the entry is not a
+                                     page of the cache                          */
+#define NVFP4MLA_STAT_TIMEOUT 2   /* bounded in-kernel waits that gave up; the
+                                     outputs of that call are then undefined    */
+#define NVFP4MLA_STAT_BAD_SLOT 3  /* pack slots other than -1 outside the cache */
+#define NVFP4MLA_STATUS_WORDS 4
+
+/*
+ * mla_kv_pack: write bf16 latent + rope rows into the paged NVFP4 cache.
+ *
+ * Source: "Prime Inference" (translated), "Making room for low-latency
+ * decode": the 512-value latent is stored as 4-bit values with one FP8 scale
+ * per 16 values and the 64-value rope part as FP8, 352 bytes per row; the
+ * byte split is the table of "Four bits per latent value: where 352 comes
+ * from". The call shape follows the cache-write call of the TokenSpeed
+ * walkthrough, section 8 (location list + latent + rope).
+ *
+ * Per row: for each block k of 16 latent values, s_k = E4M3(amax_k / 6)
+ * (nearest-even, saturating at 448); each value is coded as e2m1(x / s_k)
+ * (nearest-even, saturating at 6, sign kept; all magnitudes 0 when s_k = 0).
+ * Row bytes: [0,256) nibbles, element 2i in the low nibble of byte i;
+ * [256,288) the 32 scales; [288,352) E4M3(rope[d]).
+ *
+ *   latent            bf16 [num_tokens, 512], row stride latent_row_stride
+ *                     ELEMENTS; base 16-byte aligned, stride a multiple of 8
+ *   rope              bf16 [num_tokens, 64], row stride rope_row_stride
+ *                     elements; base 4-byte aligned, stride a multiple of 2
+ *   slot_mapping      int64 [num_tokens]; token t goes to page slot/64, row
+ *                     slot%64; -1 = skip the token; other out-of-range slots
+ *                     are skipped and counted (NVFP4MLA_STAT_BAD_SLOT)
+ *   num_tokens        >= 0 (0 enqueues nothing and returns OK)
+ *   kv_cache          uint8 [num_pages, 64, 352], 16-byte aligned; rows not
+ *                     named by a slot are left untouched
+ *   num_pages         >= 1
+ *   dev_status        optional int32[NVFP4MLA_STATUS_WORDS] (may be NULL)
+ *   stream            cudaStream_t
+ * Two tokens mapped to the same slot race; the caller must not do that.
+ */
+int mla_kv_pack(const void* latent, int64_t latent_row_stride, const void* rope, int64_t rope_row_stride,
+                const int64_t* slot_mapping, int64_t num_tokens, void* kv_cache, int64_t num_pages,
+                int32_t* dev_status, void* stream);
+
+/*
+ * sparse_mla_decode_workspace_size: bytes of device workspace that
+ * sparse_mla_decode needs for these sizes on a GPU with num_sms SMs
+ * (num_sms <= 0: ask the current device). Returns 0 for invalid sizes.
+ */
+size_t sparse_mla_decode_workspace_size(int B, int Q, int H, int topk, int num_sms);
+
+/*
+ * sparse_mla_decode: one MLA decode step over the paged NVFP4 cache, each
+ * query attending only to its indexer-selected positions.
+ *
+ * Source: "Prime Inference" (translated), "Native NVFP4 sparse MLA decode
+ * kernel": load the selected compressed rows, unpack them on chip, score,
+ * softmax and blend with 16-bit operands and FP32 accumulation; -1 entries are
+ * unused and are not read. "Serving GLM-5.3 ...", "Prefill topology": one
+ * 512 + 64 row per token shared by every head. TokenSpeed MLA decode
+ * example: page size 64, softmax scale 1/sqrt(192).
+ *
+ * For query (b, j) and head h, with C_t the dequantised row of position t
+ * (latent e2m1 * E4M3 scale, rope E4M3) and T the multiset of usable entries
+ * of topk_indices[b, j, :]:
+ *   z_t = softmax_scale * <q[b,j,h,:], C_t>           (576-wide)
+ *   out[b,j,h,:] = sum_t exp(z_t - m) C_t[0:512] / sum_t exp(z_t - m)
+ *   lse[b,j,h]   = m + ln(sum_t exp(z_t - m)),  m = max_t z_t
+ * An entry idx is usable iff 0 <= idx < seq_lens[b], idx <= seq_lens[b]-Q+j
+ * (causal within the Q new tokens), idx/64 < max_pages_per_seq and
+ * 0 <= page_table[b, idx/64] < num_pages. Entries are counted as often as
+ * listed. A query with no usable entry gets out = 0 and lse = -inf.
+ *
+ *   q                 bf16 [B, Q, H, 576] contiguous, 16-byte aligned
+ *   kv_cache          uint8 [num_pages, 64, 352], 16-byte aligned
+ *   page_table        int32 [B, max_pages_per_seq] contiguous
+ *   topk_indices      int32 [B, Q, topk] contiguous; logical positions, -1 =
+ *                     unused
+ *   seq_lens          int32 [B]; cached tokens of request b including its Q
+ *                     new tokens
+ *   B, Q, H, topk     B >= 1, 1 <= Q <= 16, H in {16, 32, 64, 128},
+ *                     1 <= topk <= NVFP4MLA_MAX_TOPK
+ *   softmax_scale     > 0 (typically 1/sqrt(192))
+ *   out               bf16 [B, Q, H, 512] contiguous, 16-byte aligned
+ *   lse               fp32 [B, Q, H] (natural log)
+ *   workspace         device scratch of at least
+ *                     sparse_mla_decode_workspace_size(B, Q, H, topk, 0)
+ *                     bytes, 256-byte aligned; contents need no
+ *                     initialisation and are clobbered
+ *   dev_status        optional int32[NVFP4MLA_STATUS_WORDS] (may be NULL)
+ *   flags             0, or NVFP4MLA_FLAG_MAX_CTAS(n) to cap the number of
+ *                     decode CTAs at n (testing aid; 0 = no cap)
+ *   stream            cudaStream_t
+ * Calls that share a workspace must be ordered on one stream.
+ */
+#define NVFP4MLA_FLAG_MAX_CTAS(n) ((uint32_t)(n) & 0xFFFFu)
+int sparse_mla_decode(const void* q, const void* kv_cache, int64_t num_pages, const int32_t* page_table,
+                      int64_t max_pages_per_seq, const int32_t* topk_indices, const int32_t* seq_lens, int B,
+                      int Q, int H, int topk, float softmax_scale, void* out, float* lse, void* workspace,
+                      size_t workspace_bytes, int32_t* dev_status, uint32_t flags, void* stream);
+
+/* Human-readable name of a return code (static string, never NULL). */
+const char* nvfp4mla_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4MLA_H_ */

@@ -1,0 +1,153 @@
+"""Python binding for libnvfp4mla (NVFP4-compressed paged MLA cache + sparse MLA decode).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of libnvfp4mla.so. PyTorch is used for device memory and streams. If
+the library cannot be loaded (or built with nvcc), importing the functions
+raises; there is no CPU fallback.
+
+C entry points (see include/nvfp4mla.h): mla_kv_pack,
+sparse_mla_decode_workspace_size, sparse_mla_decode, nvfp4mla_status_string.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+ROW_BYTES = 352
+PAGE_TOKENS = 64
+LATENT_DIM = 512
+ROPE_DIM = 64
+QK_DIM = 576
+STATUS_WORDS = 4
+STAT_BAD_INDEX, STAT_BAD_PAGE, STAT_TIMEOUT, STAT_BAD_SLOT = 0, 1, 2, 3
+
+_LIB = None
+_LOCK = threading.Lock()
+
+
+class NvFp4MlaError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        super().__init__(f"{where}: {status_string(code)} (status {code})")
+        self.code = code
+
+
+def lib_path() -> str:
+    from . import _build
+    return _build.LIB_PATH
+
+
+def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load (building first if needed) the CUDA library; raise if impossible."""
+    global _LIB
+    with _LOCK:
+        if _LIB is not None:
+            return _LIB
+        from . import _build
+        if build_if_missing and not _build.up_to_date():
+            _build.build()
+        if not os.path.exists(_build.LIB_PATH):
+            raise RuntimeError(f"libnvfp4mla.so not found at {_build.LIB_PATH}; build it with __graft_entry__.build()")
+        lib = ctypes.CDLL(_build.LIB_PATH)
+        vp, i64, i32, u32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint32, ctypes.c_size_t
+        lib.mla_kv_pack.argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, vp, vp]
+        lib.mla_kv_pack.restype = i32
+        lib.sparse_mla_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+        lib.sparse_mla_decode_workspace_size.restype = sz
+        lib.sparse_mla_decode.argtypes = [vp, vp, i64, vp, i64, vp, vp, i32, i32, i32, i32, ctypes.c_float,
+                                          vp, vp, vp, sz, vp, u32, vp]
+        lib.sparse_mla_decode.restype = i32
+        lib.nvfp4mla_status_string.argtypes = [i32]
+        lib.nvfp4mla_status_string.restype = ctypes.c_char_p
+        _LIB = lib
+        return lib
+
+
+def status_string(code: int) -> str:
+    return load_library().nvfp4mla_status_string(int(code)).decode()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_ptr(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(t, name, dtype, device=None, ndim=None, contiguous=True):
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name}: must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name}: on {t.device}, expected {device}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name}: expected {ndim} dims, got {t.dim()}")
+    if contiguous and not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+
+
+def mla_kv_pack(latent, rope, slot_mapping, kv_cache, dev_status=None, stream=None) -> None:
+    """Encode bf16 latent [N,512] + rope [N,64] rows into kv_cache uint8 [P,64,352] at slot_mapping (int64 [N])."""
+    import torch
+    _check(latent, "latent", torch.bfloat16, ndim=2, contiguous=False)
+    _check(rope, "rope", torch.bfloat16, latent.device, 2, contiguous=False)
+    _check(slot_mapping, "slot_mapping", torch.int64, latent.device, 1)
+    _check(kv_cache, "kv_cache", torch.uint8, latent.device, 3)
+    if latent.stride(1) != 1 or rope.stride(1) != 1:
+        raise ValueError("latent/rope rows must be contiguous along the feature axis")
+    n = latent.shape[0]
+    if latent.shape[1] != LATENT_DIM or rope.shape != (n, ROPE_DIM) or slot_mapping.shape[0] != n:
+        raise ValueError("shape mismatch")
+    if kv_cache.shape[1:] != (PAGE_TOKENS, ROW_BYTES):
+        raise ValueError("kv_cache must be [num_pages, 64, 352]")
+    if dev_status is not None:
+        _check(dev_status, "dev_status", torch.int32, latent.device, 1)
+    rc = load_library().mla_kv_pack(_ptr(latent), latent.stride(0), _ptr(rope), rope.stride(0), _ptr(slot_mapping),
+                                    n, _ptr(kv_cache), kv_cache.shape[0], _ptr(dev_status), _stream_ptr(stream))
+    if rc != 0:
+        raise NvFp4MlaError(rc, "mla_kv_pack")
+
+
+def sparse_mla_decode_workspace_size(B: int, Q: int, H: int, topk: int, num_sms: int = 0) -> int:
+    return int(load_library().sparse_mla_decode_workspace_size(B, Q, H, topk, num_sms))
+
+
+def sparse_mla_decode(q, kv_cache, page_table, topk_indices, seq_lens, softmax_scale, out=None, lse=None,
+                      workspace=None, dev_status=None, max_ctas: int = 0, stream=None):
+    """One sparse MLA decode step. q bf16 [B,Q,H,576], kv_cache uint8 [P,64,352],
+    page_table int32 [B,max_pages], topk_indices int32 [B,Q,K], seq_lens int32 [B].
+    Returns (out bf16 [B,Q,H,512], lse fp32 [B,Q,H])."""
+    import torch
+    _check(q, "q", torch.bfloat16, ndim=4)
+    dev = q.device
+    _check(kv_cache, "kv_cache", torch.uint8, dev, 3)
+    _check(page_table, "page_table", torch.int32, dev, 2)
+    _check(topk_indices, "topk_indices", torch.int32, dev, 3)
+    _check(seq_lens, "seq_lens", torch.int32, dev, 1)
+    B, Q, H, D = q.shape
+    K = topk_indices.shape[2]
+    if D != QK_DIM or topk_indices.shape[:2] != (B, Q) or seq_lens.shape[0] != B or page_table.shape[0] != B:
+        raise ValueError("shape mismatch")
+    if out is None:
+        out = torch.empty((B, Q, H, LATENT_DIM), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((B, Q, H), dtype=torch.float32, device=dev)
+    _check(out, "out", torch.bfloat16, dev, 4)
+    _check(lse, "lse", torch.float32, dev, 3)
+    if workspace is None:
+        nbytes = sparse_mla_decode_workspace_size(B, Q, H, K)
+        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
+    if dev_status is not None:
+        _check(dev_status, "dev_status", torch.int32, dev, 1)
+    rc = load_library().sparse_mla_decode(
+        _ptr(q), _ptr(kv_cache), kv_cache.shape[0], _ptr(page_table), page_table.shape[1], _ptr(topk_indices),
+        _ptr(seq_lens), B, Q, H, K, float(softmax_scale), _ptr(out), _ptr(lse), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(dev_status), int(max_ctas) & 0xFFFF, _stream_ptr(stream))
+    if rc != 0:
+        raise NvFp4MlaError(rc, "sparse_mla_decode")
+    return out, lse

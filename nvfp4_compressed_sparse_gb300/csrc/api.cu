@@ -1,0 +1,160 @@
+// Host side of the C ABI declared in include/nvfp4mla.h: argument checks,
+// work split, workspace carving and kernel launches. No allocation, no
+// synchronisation; everything is enqueued on the caller's stream.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/nvfp4mla.h"
+#include "internal.h"
+
+namespace nvfp4mla {
+
+int device_sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  static std::mutex mu;
+  static int cached[64] = {0};
+  if (dev < 0 || dev >= 64) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    return n;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess) cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+DecodeSchedule make_schedule(int B, int Q, int H, int topk, int num_sms, int max_ctas) {
+  DecodeSchedule s{};
+  const int nh = H < kHeadsPerCta ? H : kHeadsPerCta;
+  s.units = (int64_t)B * Q * (H / nh);
+  s.tiles_per_unit = (topk + kTileTokens - 1) / kTileTokens;
+  s.total_tiles = s.units * s.tiles_per_unit;
+  int64_t g = num_sms > 0 ? num_sms : 1;
+  if (max_ctas > 0 && max_ctas < g) g = max_ctas;
+  if (g > s.total_tiles) g = s.total_tiles;
+  s.ctas = (int)g;
+  s.partial_slots = s.ctas + s.units - 1;
+  return s;
+}
+
+static inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+size_t workspace_bytes_for(const DecodeSchedule& s, int H) {
+  const int nh = H < kHeadsPerCta ? H : kHeadsPerCta;
+  const size_t o = (size_t)s.partial_slots * nh * kLatent * sizeof(float);
+  const size_t ml = (size_t)s.partial_slots * nh * 2 * sizeof(float);
+  return align256(o) + align256(ml);
+}
+
+static bool sizes_ok(int B, int Q, int H, int topk) {
+  if (B < 1 || Q < 1 || Q > 16 || topk < 1 || topk > NVFP4MLA_MAX_TOPK) return false;
+  return H == 16 || H == 32 || H == 64 || H == 128;
+}
+
+static inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace nvfp4mla
+
+using namespace nvfp4mla;
+
+extern "C" {
+
+const char* nvfp4mla_status_string(int status) {
+  switch (status) {
+    case NVFP4MLA_OK: return "ok";
+    case NVFP4MLA_ERR_INVALID_ARG: return "invalid argument";
+    case NVFP4MLA_ERR_ALIGNMENT: return "misaligned pointer or stride";
+    case NVFP4MLA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case NVFP4MLA_ERR_WORKSPACE: return "workspace missing or too small";
+    case NVFP4MLA_ERR_CUDA: return "CUDA error";
+    default: return "unknown status";
+  }
+}
+
+int mla_kv_pack(const void* latent, int64_t latent_row_stride, const void* rope, int64_t rope_row_stride,
+                const int64_t* slot_mapping, int64_t num_tokens, void* kv_cache, int64_t num_pages,
+                int32_t* dev_status, void* stream) {
+  if (num_tokens < 0 || num_pages < 1) return NVFP4MLA_ERR_INVALID_ARG;
+  if (num_tokens == 0) return NVFP4MLA_OK;
+  if (latent == nullptr || rope == nullptr || slot_mapping == nullptr || kv_cache == nullptr)
+    return NVFP4MLA_ERR_INVALID_ARG;
+  if (latent_row_stride < kLatent || rope_row_stride < kRope) return NVFP4MLA_ERR_INVALID_ARG;
+  if (num_pages > (INT64_MAX / (kPageTokens * kRowBytes))) return NVFP4MLA_ERR_INVALID_ARG;
+  if (!aligned(latent, 16) || (latent_row_stride % 8) != 0) return NVFP4MLA_ERR_ALIGNMENT;
+  if (!aligned(rope, 4) || (rope_row_stride % 2) != 0) return NVFP4MLA_ERR_ALIGNMENT;
+  if (!aligned(kv_cache, 16) || !aligned(slot_mapping, 8)) return NVFP4MLA_ERR_ALIGNMENT;
+  if (dev_status != nullptr && !aligned(dev_status, 4)) return NVFP4MLA_ERR_ALIGNMENT;
+  const cudaError_t err = launch_pack(static_cast<const uint16_t*>(latent), latent_row_stride,
+                                      static_cast<const uint16_t*>(rope), rope_row_stride, slot_mapping,
+                                      num_tokens, static_cast<uint8_t*>(kv_cache), num_pages, dev_status,
+                                      static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? NVFP4MLA_OK : NVFP4MLA_ERR_CUDA;
+}
+
+size_t sparse_mla_decode_workspace_size(int B, int Q, int H, int topk, int num_sms) {
+  if (!sizes_ok(B, Q, H, topk)) return 0;
+  if (num_sms <= 0) num_sms = device_sm_count();
+  if (num_sms <= 0) return 0;
+  return workspace_bytes_for(make_schedule(B, Q, H, topk, num_sms, 0), H);
+}
+
+int sparse_mla_decode(const void* q, const void* kv_cache, int64_t num_pages, const int32_t* page_table,
+                      int64_t max_pages_per_seq, const int32_t* topk_indices, const int32_t* seq_lens, int B,
+                      int Q, int H, int topk, float softmax_scale, void* out, float* lse, void* workspace,
+                      size_t workspace_bytes, int32_t* dev_status, uint32_t flags, void* stream) {
+  if (!sizes_ok(B, Q, H, topk)) return NVFP4MLA_ERR_INVALID_ARG;
+  if (q == nullptr || kv_cache == nullptr || page_table == nullptr || topk_indices == nullptr ||
+      seq_lens == nullptr || out == nullptr || lse == nullptr)
+    return NVFP4MLA_ERR_INVALID_ARG;
+  if (num_pages < 1 || max_pages_per_seq < 1) return NVFP4MLA_ERR_INVALID_ARG;
+  if (num_pages > (INT64_MAX / (kPageTokens * kRowBytes)) || num_pages > INT32_MAX) return NVFP4MLA_ERR_INVALID_ARG;
+  if (!(softmax_scale > 0.f) || softmax_scale != softmax_scale) return NVFP4MLA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(out, 16)) return NVFP4MLA_ERR_ALIGNMENT;
+  if (!aligned(page_table, 4) || !aligned(topk_indices, 4) || !aligned(seq_lens, 4) || !aligned(lse, 4))
+    return NVFP4MLA_ERR_ALIGNMENT;
+  if (dev_status != nullptr && !aligned(dev_status, 4)) return NVFP4MLA_ERR_ALIGNMENT;
+  const int sms = device_sm_count();
+  if (sms <= 0) return NVFP4MLA_ERR_CUDA;
+  const DecodeSchedule s = make_schedule(B, Q, H, topk, sms, (int)(flags & 0xFFFFu));
+  const size_t need = workspace_bytes_for(s, H);
+  if (workspace == nullptr || workspace_bytes < need) return NVFP4MLA_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return NVFP4MLA_ERR_ALIGNMENT;
+
+  DecodeParams p{};
+  p.q = static_cast<const uint16_t*>(q);
+  p.cache = static_cast<const uint8_t*>(kv_cache);
+  p.num_pages = num_pages;
+  p.page_table = page_table;
+  p.max_pages = max_pages_per_seq;
+  p.idx = topk_indices;
+  p.seq_lens = seq_lens;
+  p.B = B;
+  p.Q = Q;
+  p.H = H;
+  p.topk = topk;
+  p.heads_per_cta = H < kHeadsPerCta ? H : kHeadsPerCta;
+  p.head_groups = H / p.heads_per_cta;
+  p.scale_log2 = softmax_scale * 1.4426950408889634f;
+  p.out = static_cast<uint16_t*>(out);
+  p.lse = lse;
+  const size_t o_bytes = (size_t)s.partial_slots * p.heads_per_cta * kLatent * sizeof(float);
+  p.part_o = static_cast<float*>(workspace);
+  p.part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + align256(o_bytes));
+  p.status = dev_status;
+  p.units = s.units;
+  p.total_tiles = s.total_tiles;
+  p.tiles_per_unit = s.tiles_per_unit;
+  p.ctas = s.ctas;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (launch_decode(p, st) != cudaSuccess) return NVFP4MLA_ERR_CUDA;
+  if (launch_merge(p, st) != cudaSuccess) return NVFP4MLA_ERR_CUDA;
+  return NVFP4MLA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,684 @@
+// sparse_mla_decode kernels: NVFP4 sparse MLA decode on sm_103a (tcgen05 + TMEM).
+//
+// What is computed ("Prime Inference", translated page, "Native NVFP4 sparse MLA
+// decode kernel"; "Serving GLM-5.3 ...", "A kernel that reads four bits
+// directly"): each query token reads only the cache rows its index list
+// selects, unpacks them on chip, and computes softmax attention with 16-bit
+// operands and FP32 accumulation. -1 entries are not loaded.
+//
+// GB300 design (see the design notes for the measurements behind it):
+//  * Tokens on the UMMA M axis (M = 128 rows per tile), heads on N (16 or 32):
+//    S^T[tok, h] = K[tok, :] . q[h, :] and O^T[dim, h] = sum_tok V[tok, dim] P[tok, h].
+//  * The dequantised tile is written once per row by the thread that owns the
+//    row: the 576-wide K row into TMEM (A operand of the QK UMMA, read from
+//    TMEM), the 512-wide latent into shared memory (the V operand of PV, read
+//    MN-major from the same bytes).
+//  * Two MMA issuer threads (a single issuing thread caps out near 46-49
+//    cycles per M=128 UMMA; two reach the operand-bandwidth bound).
+//  * Rows are gathered with cp.async.bulk (352 B each, one per selected entry)
+//    into a 4-stage ring; -1 and other unusable entries issue no load and are
+//    zero-filled in V and masked in the softmax.
+//  * Work is cut stream-K style: the tiles of all (query, head-group) units
+//    form one sequence split evenly across the CTAs; each CTA writes one
+//    unnormalised partial (O, running max, sum) per unit it touches, and the
+//    merge kernel combines them with the log-sum-exp rule.
+//  * Operands are FP16: the dequantised e2m1 x E4M3 products are exact in FP16,
+//    and q is scaled by a power of two per unit into FP16 range (exact for
+//    every element above 2^-24 of the scaled range); the power of two is
+//    folded back into the softmax scale.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace nvfp4mla {
+namespace {
+
+using namespace ptx;
+
+constexpr int kThreads = 512;
+constexpr int kRingStages = 4;            // one tile of 4 x 32 rows
+constexpr int kRingRowStride = 368;       // 352 padded to 23 x 16 B (bank-conflict-free row reads)
+constexpr int kRingStageBytes = 32 * kRingRowStride;
+constexpr int kVBytes = 8 * 128 * 128;    // 8 SW128 atoms x 128 rows x 128 B
+constexpr int kTmemCols = 512;
+constexpr int kTmemK = 0;                 // K tile: 288 columns (576 fp16 per lane)
+constexpr int kTmemS = 288;               // S_a, S_b: NH columns each
+// O^T accumulators: 4 M-blocks x NH columns after S_b
+
+struct alignas(16) Smem {
+  alignas(16) float m_used[32];      // running max per head (log2 units); read as float4
+  alignas(16) float alpha[32];       // rescale factor of this tile per head; read as float4
+  uint64_t ring_full[kRingStages];
+  uint64_t ring_empty[kRingStages];
+  uint64_t vfree[4];
+  uint64_t kv_ready;
+  uint64_t s_full;
+  uint64_t p_full;
+  uint64_t o_done;
+  uint64_t q_ready;
+  uint64_t drain;
+  uint32_t tmem_base;
+  volatile int abort;
+  uint32_t maskbuf[kRingStages];     // producer -> dequant: valid rows of each ring stage
+  uint32_t vmask[2][4];              // dequant -> softmax: valid rows of the tile, by tile parity
+  float red[4][32];                  // softmax group: per-warp partial reductions
+  int need_rescale;
+  float qmax[4];
+};
+
+struct TileInfo {
+  int64_t unit;     // virtual unit (query, head group)
+  int local;        // tile index within the unit
+  bool first, last; // first/last tile of this CTA's segment of the unit
+};
+
+__device__ __forceinline__ TileInfo tile_info(const DecodeParams& p, int64_t g, int64_t t_begin, int64_t t_end) {
+  TileInfo ti;
+  ti.unit = g / p.tiles_per_unit;
+  ti.local = (int)(g - ti.unit * p.tiles_per_unit);
+  ti.first = (g == t_begin) || (ti.local == 0);
+  ti.last = (g == t_end - 1) || (ti.local == p.tiles_per_unit - 1);
+  return ti;
+}
+
+__device__ __forceinline__ void fail(Smem* sm, int32_t* status) {
+  if (!sm->abort) {
+    sm->abort = 1;
+    if (status != nullptr) atomicAdd(status + 2, 1);
+  }
+}
+
+__device__ __forceinline__ bool wait(Smem* sm, uint64_t* bar, uint32_t parity, int32_t* status) {
+  if (mbar_wait(bar, parity, &sm->abort, kWaitTimeoutNs)) return true;
+  fail(sm, status);
+  return false;
+}
+
+__device__ __forceinline__ void named_sync_softmax() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// Unit decomposition: virtual unit -> (b, j, head group)
+__device__ __forceinline__ void split_unit(const DecodeParams& p, int64_t unit, int& b, int& j, int& hg) {
+  hg = (int)(unit % p.head_groups);
+  const int64_t u = unit / p.head_groups;
+  b = (int)(u / p.Q);
+  j = (int)(u - (int64_t)b * p.Q);
+}
+
+// ------------------------------------------------------------------ producer
+__device__ void producer_loop(const DecodeParams& p, Smem* sm, uint8_t* ring, int64_t t_begin, int64_t t_end) {
+  const int lane = threadIdx.x & 31;
+  uint32_t issued[kRingStages] = {0, 0, 0, 0};
+  for (int64_t g = t_begin; g < t_end && !sm->abort; ++g) {
+    const int64_t k = g - t_begin;
+    const TileInfo ti = tile_info(p, g, t_begin, t_end);
+    int b, j, hg;
+    split_unit(p, ti.unit, b, j, hg);
+    const int64_t u = (int64_t)b * p.Q + j;
+    const int L = __ldg(p.seq_lens + b);
+    const int causal = L - p.Q + j;
+    const int32_t* idx_row = p.idx + u * p.topk;
+    const int32_t* pt_row = p.page_table + (int64_t)b * p.max_pages;
+    for (int q = 0; q < kRingStages; ++q) {
+      const int e = ti.local * kTileTokens + q * 32 + lane;
+      int idx = -1;
+      if (e < p.topk) idx = __ldg(idx_row + e);
+      bool ok = idx >= 0 && idx < L && idx <= causal;
+      const bool bad_index = (idx != -1) && !ok && e < p.topk;
+      int64_t page = -1;
+      if (ok) {
+        const int col = idx >> 6;
+        if (col < p.max_pages) page = __ldg(pt_row + col);
+        ok = page >= 0 && page < p.num_pages;
+      }
+      const bool bad_page = (idx >= 0 && idx < L && idx <= causal) && !ok;
+      if (hg == 0 && p.status != nullptr) {
+        const uint32_t nbi = __popc(__ballot_sync(0xffffffffu, bad_index));
+        const uint32_t nbp = __popc(__ballot_sync(0xffffffffu, bad_page));
+        if (lane == 0 && nbi) atomicAdd(p.status + 0, (int)nbi);
+        if (lane == 0 && nbp) atomicAdd(p.status + 1, (int)nbp);
+      }
+      const uint32_t mask = __ballot_sync(0xffffffffu, ok);
+      // wait until the dequant warps released this ring stage (previous tile)
+      bool good = true;
+      if (lane == 0) good = wait(sm, &sm->ring_empty[q], (uint32_t)((k & 1) ^ 1), p.status);
+      good = __shfl_sync(0xffffffffu, good, 0);
+      if (!good) break;
+      if (lane == 0) {
+        sm->maskbuf[q] = mask;
+        mbar_arrive_expect_tx(&sm->ring_full[q], (uint32_t)__popc(mask) * kRowBytes);
+      }
+      __syncwarp();
+      if (ok) {
+        const uint8_t* src = p.cache + ((int64_t)page * kPageTokens + (idx & 63)) * kRowBytes;
+        bulk_g2s(ring + q * kRingStageBytes + lane * kRingRowStride, src, kRowBytes, &sm->ring_full[q]);
+      }
+      issued[q] = (uint32_t)(k + 1);
+    }
+    if (sm->abort) break;
+  }
+  // Never leave with bulk copies in flight: wait (bounded) for the last phase issued on each stage.
+  if (lane == 0) {
+    for (int q = 0; q < kRingStages; ++q)
+      if (issued[q] > 0) mbar_wait(&sm->ring_full[q], (issued[q] - 1) & 1, nullptr, kWaitTimeoutNs);
+  }
+  __syncwarp();
+}
+
+// ------------------------------------------------------------------ dequant
+// Thread = one tile row (token). half 0: latent dims 0..255; half 1: dims 256..511 + rope.
+__device__ __forceinline__ void convert_group(const uint8_t* rowp, int g, uint32_t (&r)[32]) {
+  const uint4 n0 = *reinterpret_cast<const uint4*>(rowp + 32 * g);
+  const uint4 n1 = *reinterpret_cast<const uint4*>(rowp + 32 * g + 16);
+  const uint32_t sw = *reinterpret_cast<const uint32_t*>(rowp + kScaleOff + 4 * g);
+  const uint32_t w[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
+#pragma unroll
+  for (int bb = 0; bb < 4; ++bb) {
+    const uint32_t s2 = e4m3x2_to_f16x2(__byte_perm(sw, 0, bb * 0x11));   // (scale, scale)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t byte = w[2 * bb + (i >> 2)] >> (8 * (i & 3));
+      r[8 * bb + i] = hmul2(e2m1x2_to_f16x2(byte), s2);
+    }
+  }
+}
+
+__device__ void dequant_loop(const DecodeParams& p, Smem* sm, const uint8_t* ring, uint8_t* vtile,
+                             int64_t t_begin, int64_t t_end, int warp) {
+  const int lane = threadIdx.x & 31;
+  const int q = warp & 3;               // TMEM lane quarter == ring stage == tile rows 32q..32q+31
+  const int half = (warp - 4) >> 2;
+  const int row = 32 * q + lane;
+  const uint32_t tmem_row = sm->tmem_base + ((uint32_t)(32 * q) << 16);
+  const uint8_t* rowp = ring + q * kRingStageBytes + lane * kRingRowStride;
+  for (int64_t g = t_begin; g < t_end; ++g) {
+    const int64_t k = g - t_begin;
+    bool good = true;
+    if (lane == 0) {
+      good = wait(sm, &sm->ring_full[q], (uint32_t)(k & 1), p.status);
+      if (good) good = wait(sm, &sm->vfree[q], (uint32_t)((k & 1) ^ 1), p.status);
+    }
+    good = __shfl_sync(0xffffffffu, good, 0);
+    if (!good) break;
+    __syncwarp();
+    tc_fence_after();
+    const uint32_t mask = sm->maskbuf[q];
+    const bool valid = (mask >> lane) & 1u;
+    uint32_t r[32];
+#pragma unroll 1
+    for (int gi = 0; gi < 4; ++gi) {
+      const int grp = 4 * half + gi;
+      if (valid) {
+        convert_group(rowp, grp, r);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) r[i] = 0u;
+      }
+      __syncwarp();
+      tmem_st32(tmem_row + kTmemK + 32 * grp, r);
+      uint8_t* vrow = vtile + grp * 16384 + row * 128;
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4*>(vrow + ((c ^ (row & 7)) << 4)) = make_uint4(r[4 * c], r[4 * c + 1], r[4 * c + 2], r[4 * c + 3]);
+    }
+    if (half == 1) {
+      if (valid) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint4 v = *reinterpret_cast<const uint4*>(rowp + kRopeOff + 16 * c);
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            r[8 * c + 2 * i] = e4m3x2_to_f16x2(w[i] & 0xFFFFu);
+            r[8 * c + 2 * i + 1] = e4m3x2_to_f16x2(w[i] >> 16);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) r[i] = 0u;
+      }
+      __syncwarp();
+      tmem_st32(tmem_row + kTmemK + 256, r);
+    }
+    tmem_wait_st();
+    tc_fence_before();
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      if (half == 0) sm->vmask[k & 1][q] = mask;
+      mbar_arrive(&sm->ring_empty[q]);
+      mbar_arrive(&sm->kv_ready);
+    }
+  }
+}
+
+// ------------------------------------------------------------------ MMA issue
+template <int NH>
+__device__ void mma_loop(const DecodeParams& p, Smem* sm, uint8_t* vtile, uint8_t* qs, uint8_t* ps,
+                         int64_t t_begin, int64_t t_end, int which) {
+  constexpr uint32_t kIdQK = idesc_f16(128, NH, false, false, false);
+  constexpr uint32_t kIdPV = idesc_f16(128, NH, true, true, false);
+  constexpr uint32_t kPSw = (NH == 32) ? SW_64B : SW_32B;
+  constexpr uint32_t kPSbo = (NH == 32) ? 512 : 256;       // 8 token rows of P
+  const uint32_t tmem = sm->tmem_base;
+  const uint32_t s_col = tmem + kTmemS + which * NH;
+  const uint32_t o_col = tmem + kTmemS + 2 * NH;
+  const uint64_t qd = sdesc(smem_u32(qs), 16, 1024, SW_128B);
+  const uint64_t vd = sdesc(smem_u32(vtile), 16384, 1024, SW_128B);
+  const uint64_t pd = sdesc(smem_u32(ps), 4096, kPSbo, kPSw);
+  int64_t seg = 0;
+  for (int64_t g = t_begin; g < t_end; ++g) {
+    const int64_t k = g - t_begin;
+    const TileInfo ti = tile_info(p, g, t_begin, t_end);
+    if (ti.first && !wait(sm, &sm->q_ready, (uint32_t)(seg & 1), p.status)) break;
+    if (!wait(sm, &sm->kv_ready, (uint32_t)(k & 1), p.status)) break;
+    tc_fence_after();
+    // S^T = K . Q^T ; issuer 0 takes k-steps 0..17, issuer 1 takes 18..35 (own accumulator each)
+#pragma unroll
+    for (int x = 0; x < 18; ++x) {
+      const int ks = which * 18 + x;
+      const uint64_t b = qd + (uint64_t)((((ks >> 2) * NH * 128) + (ks & 3) * 32) >> 4);
+      umma_ts(s_col, tmem + kTmemK + 8 * ks, b, kIdQK, x > 0 ? 1u : 0u);
+    }
+    umma_commit(&sm->s_full);
+    if (!wait(sm, &sm->p_full, (uint32_t)(k & 1), p.status)) break;
+    tc_fence_after();
+    // O^T += V^T . P^T ; issuer 0 takes M-blocks 0,1, issuer 1 takes 2,3. Row chunk w (tokens 32w..)
+    // is finished by both issuers before vfree[w] fires, so the next tile's rows can be written.
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+#pragma unroll
+      for (int mi = 0; mi < 2; ++mi) {
+        const int mb = which * 2 + mi;
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {
+          const int ks = 2 * w + kk;
+          const uint64_t a = vd + (uint64_t)((mb * 32768 + ks * 2048) >> 4);
+          const uint64_t bdesc = pd + (uint64_t)((ks * 2 * kPSbo) >> 4);
+          umma_ss(o_col + mb * NH, a, bdesc, kIdPV, (ti.first && ks == 0) ? 0u : 1u);
+        }
+      }
+      umma_commit(&sm->vfree[w]);
+    }
+    if (ti.last) {
+      umma_commit(&sm->o_done);
+      ++seg;
+    }
+  }
+  // drain: every UMMA of this thread has completed before TMEM is released
+  umma_commit(&sm->drain);
+  mbar_wait(&sm->drain, 0, nullptr, kWaitTimeoutNs);
+}
+
+// ------------------------------------------------------------------ softmax / epilogue
+// Transpose-reduce 32 values across a warp: afterwards lane l holds the reduction
+// (over the 32 lanes) of element l. op: 0 = max, 1 = sum.
+template <int OP>
+__device__ __forceinline__ float warp_transpose_reduce(float (&v)[32]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int s = 16; s >= 1; s >>= 1) {
+    const bool upper = (lane & s) != 0;
+#pragma unroll
+    for (int i = 0; i < s; ++i) {
+      // keep half [i] (lower) or [i+s] (upper); send the other half
+      const float send = upper ? v[i] : v[i + s];
+      const float keep = upper ? v[i + s] : v[i];
+      const float got = __shfl_xor_sync(0xffffffffu, send, s);
+      v[i] = OP == 0 ? fmaxf(keep, got) : keep + got;
+    }
+  }
+  return v[0];
+}
+
+template <int NH>
+__device__ void softmax_loop(const DecodeParams& p, Smem* sm, uint8_t* qs, uint8_t* ps, int64_t t_begin,
+                             int64_t t_end, int64_t cta) {
+  const int t = threadIdx.x - 384;          // 0..127: tile row / TMEM lane
+  const int w = t >> 5, lane = t & 31;
+  const uint32_t tmem_lane = sm->tmem_base + ((uint32_t)(32 * w) << 16);
+  const uint32_t s_col = kTmemS, o_col = kTmemS + 2 * NH;
+  const float kNegInf = __int_as_float(0xff800000);
+  float l_part[32];
+  float qscale = 0.f;
+  int64_t seg = 0;
+  bool ok = true;
+  for (int64_t g = t_begin; g < t_end && ok; ++g) {
+    const int64_t k = g - t_begin;
+    const TileInfo ti = tile_info(p, g, t_begin, t_end);
+    if (ti.first) {
+      // ---- stage q of this unit as FP16, scaled by 2^e so that max|q| * 2^e is in [2^14, 2^15)
+      int b, j, hg;
+      split_unit(p, ti.unit, b, j, hg);
+      const uint16_t* qsrc = p.q + (((int64_t)b * p.Q + j) * p.H + (int64_t)hg * NH) * kQK;
+      constexpr int kChunks = NH * (kQK / 8);
+      float mx = 0.f;
+      for (int c = t; c < kChunks; c += 128) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(qsrc) + c);
+        const uint32_t ww[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(ww[i] << 16)), fabsf(__uint_as_float(ww[i] & 0xFFFF0000u))));
+      }
+#pragma unroll
+      for (int s = 16; s >= 1; s >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, s));
+      if (lane == 0) sm->qmax[w] = mx;
+      named_sync_softmax();
+      mx = fmaxf(fmaxf(sm->qmax[0], sm->qmax[1]), fmaxf(sm->qmax[2], sm->qmax[3]));
+      int e = 0;
+      if (mx > 0.f && isfinite(mx)) {
+        int E;
+        frexpf(mx, &E);                    // mx in [2^(E-1), 2^E)
+        e = 15 - E;
+      }
+      const float up = ldexpf(1.f, e);
+      for (int c = t; c < kChunks; c += 128) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(qsrc) + c);
+        const uint32_t ww[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const __half2 h = __floats2half2_rn(__uint_as_float(ww[i] << 16) * up, __uint_as_float(ww[i] & 0xFFFF0000u) * up);
+          o[i] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        const int h = c / (kQK / 8), cc = c % (kQK / 8);
+        const int atom = cc >> 3, ch = cc & 7;
+        *reinterpret_cast<uint4*>(qs + atom * (NH * 128) + h * 128 + ((ch ^ (h & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+      fence_proxy_async_smem();
+      qscale = p.scale_log2 * ldexpf(1.f, -e);
+#pragma unroll
+      for (int h = 0; h < 32; ++h) l_part[h] = 0.f;
+      if (t < 32) sm->m_used[t] = kNegInf;
+      named_sync_softmax();
+      mbar_arrive(&sm->q_ready);
+    }
+    // ---- scores of this tile
+    if (wait(sm, &sm->kv_ready, (uint32_t)(k & 1), p.status)) wait(sm, &sm->s_full, (uint32_t)(k & 1), p.status);
+    named_sync_softmax();               // every thread sees the same abort flag after this
+    if (sm->abort) {
+      ok = false;
+      break;
+    }
+    tc_fence_after();
+    __syncwarp();
+    float z[32];
+    {
+      uint32_t ra[32], rb[32];
+      if (NH == 32) {
+        tmem_ld32(tmem_lane + s_col, ra);
+        tmem_ld32(tmem_lane + s_col + NH, rb);
+      } else {
+        uint32_t (&ra16)[16] = *reinterpret_cast<uint32_t(*)[16]>(ra);
+        uint32_t (&rb16)[16] = *reinterpret_cast<uint32_t(*)[16]>(rb);
+        tmem_ld16(tmem_lane + s_col, ra16);
+        tmem_ld16(tmem_lane + s_col + NH, rb16);
+      }
+      tmem_wait_ld();
+      const bool valid = (sm->vmask[k & 1][w] >> lane) & 1u;
+#pragma unroll
+      for (int h = 0; h < 32; ++h)
+        z[h] = (h < NH && valid) ? (__uint_as_float(ra[h]) + __uint_as_float(rb[h])) * qscale : kNegInf;
+    }
+    // tile max per head
+    {
+      float v[32];
+#pragma unroll
+      for (int h = 0; h < 32; ++h) v[h] = z[h];
+      const float wm = warp_transpose_reduce<0>(v);   // lane l: max over this warp's rows of head l
+      sm->red[w][lane] = wm;
+    }
+    named_sync_softmax();
+    if (w == 0) {
+      const float tmax = fmaxf(fmaxf(sm->red[0][lane], sm->red[1][lane]), fmaxf(sm->red[2][lane], sm->red[3][lane]));
+      const float mold = sm->m_used[lane];
+      float mnew = mold, alpha = 1.f;
+      if (tmax > mold + 8.f) {             // lazy rescale: keep the stale max unless it grows by 2^8
+        mnew = tmax;
+        alpha = (mold == kNegInf) ? 0.f : ex2_approx(mold - mnew);
+      }
+      sm->m_used[lane] = mnew;
+      sm->alpha[lane] = alpha;
+      const bool any = __any_sync(0xffffffffu, lane < NH && alpha != 1.f && mold != kNegInf);
+      if (lane == 0) sm->need_rescale = any ? 1 : 0;
+    }
+    named_sync_softmax();
+    uint32_t pk[16];
+#pragma unroll
+    for (int h = 0; h < 32; h += 4) {
+      const float4 mv = *reinterpret_cast<const float4*>(&sm->m_used[h]);
+      const float4 av = *reinterpret_cast<const float4*>(&sm->alpha[h]);
+      const float mm[4] = {mv.x, mv.y, mv.z, mv.w};
+      const float aa[4] = {av.x, av.y, av.z, av.w};
+      float pp[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        pp[i] = (mm[i] == kNegInf) ? 0.f : ex2_approx(z[h + i] - mm[i]);
+        l_part[h + i] = l_part[h + i] * aa[i] + pp[i];
+      }
+      const __half2 h01 = __floats2half2_rn(pp[0], pp[1]);
+      const __half2 h23 = __floats2half2_rn(pp[2], pp[3]);
+      pk[h >> 1] = *reinterpret_cast<const uint32_t*>(&h01);
+      pk[(h >> 1) + 1] = *reinterpret_cast<const uint32_t*>(&h23);
+    }
+    // P row t, MN-major (heads contiguous): SW64 for 32 heads, SW32 for 16
+    if (NH == 32) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        *reinterpret_cast<uint4*>(ps + t * 64 + ((c ^ ((t >> 1) & 3)) << 4)) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+    } else {
+#pragma unroll
+      for (int c = 0; c < 2; ++c)
+        *reinterpret_cast<uint4*>(ps + t * 32 + ((c ^ ((t >> 2) & 1)) << 4)) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+    }
+    __syncwarp();
+    if (sm->need_rescale && !ti.first) {
+      // O^T[dim, h] *= alpha[h]; all PV of earlier tiles are complete (they precede this tile's QK)
+#pragma unroll 1
+      for (int mb = 0; mb < 4; ++mb) {
+        uint32_t r[32];
+        if (NH == 32) {
+          tmem_ld32(tmem_lane + o_col + mb * NH, r);
+        } else {
+          tmem_ld16(tmem_lane + o_col + mb * NH, *reinterpret_cast<uint32_t(*)[16]>(r));
+        }
+        tmem_wait_ld();
+#pragma unroll
+        for (int h = 0; h < NH; ++h) r[h] = __float_as_uint(__uint_as_float(r[h]) * sm->alpha[h]);
+        if (NH == 32) tmem_st32(tmem_lane + o_col + mb * NH, r);
+        else tmem_st16(tmem_lane + o_col + mb * NH, *reinterpret_cast<uint32_t(*)[16]>(r));
+      }
+      tmem_wait_st();
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    mbar_arrive(&sm->p_full);
+
+    if (ti.last) {
+      // ---- epilogue: write this segment's unnormalised partial
+      wait(sm, &sm->o_done, (uint32_t)(seg & 1), p.status);
+      named_sync_softmax();
+      if (sm->abort) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int64_t slot = cta + ti.unit;
+      float* po = p.part_o + slot * (int64_t)NH * kLatent;
+      {
+        float v[32];
+#pragma unroll
+        for (int h = 0; h < 32; ++h) v[h] = l_part[h];
+        const float ws = warp_transpose_reduce<1>(v);
+        sm->red[w][lane] = ws;
+      }
+      named_sync_softmax();
+      if (t < NH) {
+        const float lsum = sm->red[0][t] + sm->red[1][t] + sm->red[2][t] + sm->red[3][t];
+        p.part_ml[(slot * NH + t) * 2 + 0] = sm->m_used[t];
+        p.part_ml[(slot * NH + t) * 2 + 1] = lsum;
+      }
+      __syncwarp();
+#pragma unroll 1
+      for (int mb = 0; mb < 4; ++mb) {
+        uint32_t r[32];
+        if (NH == 32) {
+          tmem_ld32(tmem_lane + o_col + mb * NH, r);
+        } else {
+          tmem_ld16(tmem_lane + o_col + mb * NH, *reinterpret_cast<uint32_t(*)[16]>(r));
+        }
+        tmem_wait_ld();
+        const int dim = mb * 128 + t;
+#pragma unroll
+        for (int h = 0; h < NH; ++h) po[(int64_t)h * kLatent + dim] = __uint_as_float(r[h]);
+      }
+      tc_fence_before();
+      named_sync_softmax();
+      ++seg;
+    }
+  }
+}
+
+template <int NH>
+__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* vtile = base;                                   // 131072
+  uint8_t* qs = vtile + kVBytes;                           // 9 * NH * 128
+  uint8_t* ps = qs + 9 * NH * 128;                         // 128 * NH * 2
+  uint8_t* ring = ps + 128 * NH * 2;                       // 4 * 32 * 368
+  static_assert((kRingStages * kRingStageBytes) % 16 == 0, "control block must stay 16-byte aligned");
+  Smem* sm = reinterpret_cast<Smem*>(ring + kRingStages * kRingStageBytes);
+
+  const int warp = threadIdx.x >> 5;
+  const int64_t cta = blockIdx.x;
+  const int64_t t_begin = cta * p.total_tiles / p.ctas;
+  const int64_t t_end = (cta + 1) * p.total_tiles / p.ctas;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kRingStages; ++i) {
+      mbar_init(&sm->ring_full[i], 1);
+      mbar_init(&sm->ring_empty[i], 2);
+    }
+    for (int i = 0; i < 4; ++i) mbar_init(&sm->vfree[i], 2);
+    mbar_init(&sm->kv_ready, 8);
+    mbar_init(&sm->s_full, 2);
+    mbar_init(&sm->p_full, 128);
+    mbar_init(&sm->o_done, 2);
+    mbar_init(&sm->q_ready, 128);
+    mbar_init(&sm->drain, 2);
+    sm->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&sm->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  if (warp == 0) {
+    producer_loop(p, sm, ring, t_begin, t_end);
+  } else if (warp == 1 || warp == 2) {
+    if ((threadIdx.x & 31) == 0) mma_loop<NH>(p, sm, vtile, qs, ps, t_begin, t_end, warp - 1);
+    __syncwarp();
+  } else if (warp >= 4 && warp < 12) {
+    dequant_loop(p, sm, ring, vtile, t_begin, t_end, warp);
+  } else if (warp >= 12) {
+    softmax_loop<NH>(p, sm, qs, ps, t_begin, t_end, cta);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(sm->tmem_base, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ merge
+// One block per (virtual unit, head): combine the partials of the CTAs that
+// covered the unit with the log-sum-exp rule; write bf16 out and fp32 LSE.
+template <int NH>
+__global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int64_t unit = blockIdx.x;
+  const int h = blockIdx.y;
+  const int64_t g0 = unit * p.tiles_per_unit, g1 = g0 + p.tiles_per_unit - 1;
+  const int64_t c_lo = ((g0 + 1) * p.ctas - 1) / p.total_tiles;
+  const int64_t c_hi = ((g1 + 1) * p.ctas - 1) / p.total_tiles;
+  const float kNegInf = __int_as_float(0xff800000);
+  float mstar = kNegInf;
+  for (int64_t c = c_lo; c <= c_hi; ++c) {
+    const int64_t slot = c + unit;
+    const float m = p.part_ml[(slot * NH + h) * 2];
+    const float l = p.part_ml[(slot * NH + h) * 2 + 1];
+    if (l > 0.f) mstar = fmaxf(mstar, m);
+  }
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float lsum = 0.f;
+  if (mstar != kNegInf) {
+    for (int64_t c = c_lo; c <= c_hi; ++c) {
+      const int64_t slot = c + unit;
+      const float m = p.part_ml[(slot * NH + h) * 2];
+      const float l = p.part_ml[(slot * NH + h) * 2 + 1];
+      if (!(l > 0.f)) continue;
+      const float wgt = exp2f(m - mstar);
+      lsum += wgt * l;
+      const float4 o = reinterpret_cast<const float4*>(p.part_o + (slot * NH + h) * (int64_t)kLatent)[threadIdx.x];
+      acc.x += wgt * o.x; acc.y += wgt * o.y; acc.z += wgt * o.z; acc.w += wgt * o.w;
+    }
+  }
+  int b, j, hg;
+  split_unit(p, unit, b, j, hg);
+  const int64_t row = ((int64_t)b * p.Q + j) * p.H + (int64_t)hg * NH + h;
+  const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+  const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+  const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+  uint2 packed;
+  packed.x = *reinterpret_cast<const uint32_t*>(&lo);
+  packed.y = *reinterpret_cast<const uint32_t*>(&hi);
+  reinterpret_cast<uint2*>(p.out + row * kLatent)[threadIdx.x] = packed;
+  if (threadIdx.x == 0) p.lse[row] = lsum > 0.f ? (mstar + log2f(lsum)) * 0.69314718055994530942f : kNegInf;
+}
+
+template <int NH>
+constexpr size_t decode_smem_bytes() {
+  return 1024 + kVBytes + 9 * NH * 128 + 128 * NH * 2 + kRingStages * kRingStageBytes + sizeof(Smem);
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream) {
+  cudaError_t err;
+  if (p.heads_per_cta == 32) {
+    constexpr size_t smem = decode_smem_bytes<32>();
+    err = cudaFuncSetAttribute(decode_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    decode_kernel<32><<<p.ctas, kThreads, smem, stream>>>(p);
+  } else {
+    constexpr size_t smem = decode_smem_bytes<16>();
+    err = cudaFuncSetAttribute(decode_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    decode_kernel<16><<<p.ctas, kThreads, smem, stream>>>(p);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_merge(const DecodeParams& p, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)p.units, (unsigned)p.heads_per_cta, 1);
+  cfg.blockDim = dim3(128, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (p.heads_per_cta == 32) return cudaLaunchKernelEx(&cfg, merge_kernel<32>, p);
+  return cudaLaunchKernelEx(&cfg, merge_kernel<16>, p);
+}
+
+}  // namespace nvfp4mla

@@ -1,0 +1,63 @@
+// Internal declarations shared by the host API and the kernels.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace nvfp4mla {
+
+constexpr int kLatent = 512;
+constexpr int kRope = 64;
+constexpr int kQK = 576;
+constexpr int kRowBytes = 352;
+constexpr int kPageTokens = 64;
+constexpr int kScaleOff = 256;
+constexpr int kRopeOff = 288;
+
+constexpr int kTileTokens = 128;      // tokens per decode tile (UMMA M)
+constexpr int kHeadsPerCta = 32;      // heads handled by one decode CTA (UMMA N <= 32)
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;   // bounded in-kernel waits: 2 s
+
+// Work split of the decode kernel: the tiles of all (unit, head-group) pairs
+// form one sequence, cut into `ctas` contiguous ranges (stream-K style).
+struct DecodeSchedule {
+  int64_t units;           // B * Q * head_groups
+  int tiles_per_unit;      // ceil(topk / 128)
+  int64_t total_tiles;     // units * tiles_per_unit
+  int ctas;                // grid size
+  int64_t partial_slots;   // ctas + units - 1
+};
+
+DecodeSchedule make_schedule(int B, int Q, int H, int topk, int num_sms, int max_ctas);
+size_t workspace_bytes_for(const DecodeSchedule& s, int H);
+
+struct DecodeParams {
+  const uint16_t* q;          // bf16 [B, Q, H, 576]
+  const uint8_t* cache;       // [num_pages, 64, 352]
+  int64_t num_pages;
+  const int32_t* page_table;  // [B, max_pages]
+  int64_t max_pages;
+  const int32_t* idx;         // [B, Q, topk] index lists
+  const int32_t* seq_lens;    // [B]
+  int B, Q, H, topk;
+  int heads_per_cta;          // 16 or 32
+  int head_groups;            // H / heads_per_cta
+  float scale_log2;           // softmax_scale * log2(e)
+  uint16_t* out;              // bf16 [B, Q, H, 512]
+  float* lse;                 // [B, Q, H]
+  float* part_o;              // [slots, heads_per_cta, 512]
+  float* part_ml;             // [slots, heads_per_cta, 2]  (running max in log2 units, sum)
+  int32_t* status;            // optional
+  int64_t units, total_tiles;
+  int tiles_per_unit, ctas;
+};
+
+cudaError_t launch_pack(const uint16_t* latent, int64_t lstride, const uint16_t* rope, int64_t rstride,
+                        const int64_t* slots, int64_t n, uint8_t* cache, int64_t num_pages, int32_t* status,
+                        cudaStream_t stream);
+cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_merge(const DecodeParams& p, cudaStream_t stream);
+
+int device_sm_count();
+
+}  // namespace nvfp4mla

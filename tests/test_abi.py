@@ -1,0 +1,99 @@
+"""The C-ABI library builds, loads and exports every symbol its header declares;
+host-side argument checks return the documented codes (CPU only: no call here
+reaches a kernel launch)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import nvfp4_compressed_sparse_gb300 as m
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "nvfp4mla.h")
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_ ]*?[\s\*]+([A-Za-z_][A-Za-z0-9_]*)\s*\(", text, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "defined")))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return m.load_library()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared_functions()
+    assert set(names) >= {"mla_kv_pack", "sparse_mla_decode", "sparse_mla_decode_workspace_size",
+                          "nvfp4mla_status_string"}
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    assert m.status_string(0) == "ok"
+    for code in range(1, 6):
+        assert m.status_string(code) not in ("ok", "unknown status")
+    assert m.status_string(99) == "unknown status"
+
+
+def test_workspace_size_formula(lib):
+    # 152 SMs, B=64, Q=1, H=32, topk=2048: 64 units x 16 tiles; 152 CTAs; 215 partial slots
+    n = lib.sparse_mla_decode_workspace_size(64, 1, 32, 2048, 152)
+    slots = 152 + 64 - 1
+    o = slots * 32 * 512 * 4
+    ml = slots * 32 * 2 * 4
+    r = lambda x: (x + 255) // 256 * 256
+    assert n == r(o) + r(ml)
+    # fewer tiles than SMs: one CTA per tile
+    assert lib.sparse_mla_decode_workspace_size(1, 1, 16, 256, 152) == r((2 + 1 - 1) * 16 * 512 * 4) + r(2 * 16 * 2 * 4)
+    # H=128 -> 4 head groups of 32
+    assert lib.sparse_mla_decode_workspace_size(2, 1, 128, 128, 152) == r((8 + 8 - 1) * 32 * 512 * 4) + r(15 * 32 * 8)
+    for bad in [(0, 1, 32, 2048), (1, 0, 32, 2048), (1, 17, 32, 2048), (1, 1, 48, 2048), (1, 1, 32, 0), (1, 1, 32, 8193)]:
+        assert lib.sparse_mla_decode_workspace_size(*bad, 152) == 0
+
+
+V = ctypes.c_void_p
+
+
+def _pack(lib, lat=16, lstride=512, rope=16, rstride=64, slots=8, n=1, cache=16, pages=1, status=None):
+    return lib.mla_kv_pack(V(lat), lstride, V(rope), rstride, V(slots), n, V(cache), pages,
+                           V(status) if status else None, None)
+
+
+def test_pack_host_checks(lib):
+    A = 1 << 20     # a fake, well aligned address (never dereferenced: every call fails its checks or n == 0)
+    assert _pack(lib, A, n=0) == 0
+    assert _pack(lib, A, n=-1) == 1
+    assert _pack(lib, 0, rope=A, slots=A, cache=A) == 1
+    assert _pack(lib, A, rope=0, slots=A, cache=A) == 1
+    assert _pack(lib, A, rope=A, slots=0, cache=A) == 1
+    assert _pack(lib, A, rope=A, slots=A, cache=0) == 1
+    assert _pack(lib, A, rope=A, slots=A, cache=A, pages=0) == 1
+    assert _pack(lib, A, lstride=500, rope=A, slots=A, cache=A) == 1
+    assert _pack(lib, A + 8, rope=A, slots=A, cache=A) == 2
+    assert _pack(lib, A, lstride=516, rope=A, slots=A, cache=A) == 2
+    assert _pack(lib, A, rope=A + 2, slots=A, cache=A) == 2
+    assert _pack(lib, A, rope=A, rstride=65, slots=A, cache=A) == 2
+    assert _pack(lib, A, rope=A, slots=A + 4, cache=A) == 2
+    assert _pack(lib, A, rope=A, slots=A, cache=A + 8) == 2
+
+
+def _dec(lib, q=1 << 20, cache=1 << 20, pages=10, pt=1 << 20, maxp=4, idx=1 << 20, sl=1 << 20, B=1, Q=1, H=32,
+         K=128, scale=0.07, out=1 << 20, lse=1 << 20, ws=1 << 20, wsb=1 << 30, status=None, flags=0):
+    return lib.sparse_mla_decode(V(q), V(cache), pages, V(pt), maxp, V(idx), V(sl), B, Q, H, K, ctypes.c_float(scale),
+                                 V(out), V(lse), V(ws), wsb, V(status) if status else None, flags, None)
+
+
+def test_decode_host_checks(lib):
+    A = 1 << 20
+    for kw in [dict(B=0), dict(Q=0), dict(Q=17), dict(H=8), dict(H=48), dict(K=0), dict(K=9000), dict(q=0),
+               dict(cache=0), dict(pt=0), dict(idx=0), dict(sl=0), dict(out=0), dict(lse=0), dict(pages=0),
+               dict(maxp=0), dict(scale=0.0), dict(scale=-1.0), dict(scale=float("nan"))]:
+        assert _dec(lib, **kw) == 1, kw
+    for kw in [dict(q=A + 8), dict(cache=A + 4), dict(out=A + 2), dict(pt=A + 2), dict(idx=A + 1), dict(sl=A + 2),
+               dict(lse=A + 2)]:
+        assert _dec(lib, **kw) == 2, kw

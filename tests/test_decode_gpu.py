@@ -1,0 +1,194 @@
+"""sparse_mla_decode on the GPU vs the CPU oracle.
+
+Outputs within |out - ref| <= 2e-3 + 1e-2 |ref| and |lse - ref| <= 1e-3, where
+the reference is fp64 attention over the same dequantised cache; index and page
+handling bit-exact (bitwise invariance under page permutation, exact
+single-token output, exact status counts)."""
+import numpy as np
+import pytest
+import torch
+
+import nvfp4_compressed_sparse_gb300 as m
+import workloads
+from oracle import attention, pack
+from tests.gpu_util import (assert_close, bf16_dev, bits_of, decode_inputs, i32,
+                            oracle_units_from_device_rows)
+
+pytestmark = pytest.mark.gpu
+
+
+def _host_cache(case):
+    lat, rope = workloads.host_rows(case, np.arange(case.num_pages))
+    rows = pack.encode_rows(lat, rope).reshape(case.num_pages, 64, 352)
+    return lat, rope, rows
+
+
+def _gpu_cache(lat, rope, num_pages):
+    cache = torch.zeros((num_pages, 64, 352), dtype=torch.uint8, device="cuda")
+    m.mla_kv_pack(bf16_dev(lat), bf16_dev(rope), torch.arange(num_pages * 64, device="cuda"), cache)
+    return cache
+
+
+def _decode(case, cache, **kw):
+    q, pt, tk, sl = decode_inputs(case)
+    out, lse = m.sparse_mla_decode(q, cache, pt, tk, sl, case.softmax_scale, **kw)
+    torch.cuda.synchronize()
+    return out, lse
+
+
+SMALL = [
+    dict(B=2, Q=1, H=16, topk=200, L=(700, 1000)),                       # ragged tail: 128 + 72
+    dict(B=2, Q=1, H=32, topk=300, L=(2000, 900)),
+    dict(B=1, Q=4, H=32, topk=256, L=(3000,)),                            # causal across 4 query tokens
+    dict(B=3, Q=2, H=64, topk=130, L=(500, 600, 700)),                    # two head groups
+    dict(B=1, Q=1, H=128, topk=129, L=(400,)),                            # four head groups
+    dict(B=2, Q=2, H=32, topk=384, L=(1500, 1400), invalid_frac=0.25, dup=True, causal_tail=True),
+    dict(B=4, Q=1, H=16, topk=50, L=(40, 60, 2000, 64)),                  # short contexts leave -1 entries
+]
+
+
+@pytest.mark.parametrize("spec", SMALL, ids=lambda s: "B{B}Q{Q}H{H}K{topk}".format(**s))
+@pytest.mark.parametrize("max_ctas", [0, 1, 3])
+def test_small_cases_match_oracle(spec, max_ctas):
+    case = workloads.small_case(seed=100 + len(str(spec)), **spec)
+    lat, rope, rows = _host_cache(case)
+    cache = _gpu_cache(lat, rope, case.num_pages)
+    np.testing.assert_array_equal(cache.cpu().numpy(), rows)
+    out, lse = _decode(case, cache, max_ctas=max_ctas)
+    ref_out, ref_lse = attention.sparse_decode(case.q_bits, rows, case.page_table, case.topk_indices,
+                                               case.seq_lens, case.softmax_scale)
+    assert_close(out, lse, ref_out, ref_lse, f"{spec} max_ctas={max_ctas}")
+
+
+def test_all_entries_unused_gives_zero_and_neg_inf():
+    case = workloads.small_case(B=2, Q=1, H=32, topk=300, L=(500, 600), seed=3)
+    case.topk_indices[:] = -1
+    case.topk_indices[1, 0, 5] = 10**6          # past seq_len: also unused
+    lat, rope, rows = _host_cache(case)
+    cache = _gpu_cache(lat, rope, case.num_pages)
+    status = torch.zeros(4, dtype=torch.int32, device="cuda")
+    out, lse = _decode(case, cache, dev_status=status)
+    assert bool((out == 0).all())
+    assert bool(torch.isneginf(lse).all())
+    assert status.cpu().tolist() == [1, 0, 0, 0]
+
+
+def test_single_valid_entry_is_exact():
+    case = workloads.small_case(B=1, Q=1, H=16, topk=128, L=(300,), seed=4)
+    case.topk_indices[:] = -1
+    case.topk_indices[0, 0, 77] = 201
+    lat, rope, rows = _host_cache(case)
+    cache = _gpu_cache(lat, rope, case.num_pages)
+    out, lse = _decode(case, cache)
+    c = attention.dequant_rows(rows[case.page_table[0][201 // 64], 201 % 64][None])[0]
+    # the dequantised row is exact in bf16, so the output equals it exactly (as values: the sign of
+    # a zero is not kept through fp32 accumulation)
+    np.testing.assert_array_equal(out.float().cpu().numpy()[0, 0], np.broadcast_to(c[:512], (16, 512)))
+    ref_out, ref_lse = attention.sparse_decode(case.q_bits, rows, case.page_table, case.topk_indices,
+                                               case.seq_lens, case.softmax_scale)
+    assert np.abs(lse.cpu().numpy() - ref_lse).max() <= 1e-3
+
+
+def test_deterministic_and_page_permutation_bitwise():
+    case = workloads.small_case(B=2, Q=1, H=32, topk=500, L=(3000, 2500), seed=8)
+    lat, rope, rows = _host_cache(case)
+    cache = _gpu_cache(lat, rope, case.num_pages)
+    out1, lse1 = _decode(case, cache)
+    out2, lse2 = _decode(case, cache)
+    assert torch.equal(out1, out2) and torch.equal(lse1, lse2)
+    perm = np.random.default_rng(1).permutation(case.num_pages)
+    cache_p = torch.empty_like(cache)
+    cache_p[torch.from_numpy(perm).cuda()] = cache
+    case_p = workloads.small_case(B=2, Q=1, H=32, topk=500, L=(3000, 2500), seed=8)
+    case_p.page_table = np.where(case.page_table >= 0, perm[np.clip(case.page_table, 0, None)], -1).astype(np.int32)
+    out3, lse3 = _decode(case_p, cache_p)
+    assert torch.equal(out1, out3) and torch.equal(lse1, lse3)
+
+
+def test_status_counts_bad_indices_and_pages():
+    case = workloads.small_case(B=2, Q=2, H=64, topk=200, L=(900, 700), seed=12)
+    tk = case.topk_indices
+    tk[0, 0, :10] = 5000            # past seq_len            -> bad index
+    tk[0, 1, 10:13] = -3            # negative, not -1        -> bad index
+    tk[1, 0, 0:4] = 699             # past causal for j = 0   -> bad index
+    tk[1, 1, 50:60] = -1            # unused                  -> not counted
+    case.page_table[1, 2] = -1      # positions 128..191 of request 1 -> bad page
+    case.page_table[0, 3] = 10**6   # positions 192..255 of request 0 -> bad page
+    lat, rope, rows = _host_cache(case)
+    cache = _gpu_cache(lat, rope, case.num_pages)
+    status = torch.zeros(4, dtype=torch.int32, device="cuda")
+    out, lse = _decode(case, cache, dev_status=status)
+    bad_idx = bad_page = 0
+    for b in range(2):
+        L = int(case.seq_lens[b])
+        for j in range(2):
+            for idx in tk[b, j]:
+                if idx == -1:
+                    continue
+                if idx < 0 or idx >= L or idx > L - 2 + j:
+                    bad_idx += 1
+                    continue
+                pg = case.page_table[b][idx // 64]
+                if pg < 0 or pg >= case.num_pages:
+                    bad_page += 1
+    assert status.cpu().tolist() == [bad_idx, bad_page, 0, 0]
+    ref_out, ref_lse = attention.sparse_decode(case.q_bits, rows, case.page_table, tk, case.seq_lens,
+                                               case.softmax_scale)
+    assert_close(out, lse, ref_out, ref_lse, "status case")
+
+
+def test_two_streams_with_event_order():
+    case = workloads.small_case(B=2, Q=1, H=32, topk=256, L=(1200, 1300), seed=21)
+    lat, rope, rows = _host_cache(case)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    cache = torch.zeros((case.num_pages, 64, 352), dtype=torch.uint8, device="cuda")
+    latd, roped = bf16_dev(lat), bf16_dev(rope)
+    slots = torch.arange(case.num_pages * 64, device="cuda")
+    q, pt, tk, sl = decode_inputs(case)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s1):
+        m.mla_kv_pack(latd, roped, slots, cache, stream=s1)
+        ev = torch.cuda.Event()
+        ev.record(s1)
+    s2.wait_event(ev)
+    with torch.cuda.stream(s2):
+        out, lse = m.sparse_mla_decode(q, cache, pt, tk, sl, case.softmax_scale, stream=s2)
+    torch.cuda.synchronize()
+    ref_out, ref_lse = attention.sparse_decode(case.q_bits, rows, case.page_table, case.topk_indices,
+                                               case.seq_lens, case.softmax_scale)
+    assert_close(out, lse, ref_out, ref_lse, "two streams")
+
+
+def test_dense_control_equals_dense_oracle():
+    case = workloads.make_case("4d")
+    lat, rope, rows = _host_cache(case)
+    cache = _gpu_cache(lat, rope, case.num_pages)
+    out, lse = _decode(case, cache)
+    ref_out, ref_lse = attention.dense_decode(case.q_bits, rows, case.page_table, case.seq_lens, case.softmax_scale)
+    assert_close(out, lse, ref_out, ref_lse, "dense control")
+
+
+@pytest.mark.parametrize("cfg", [0, 1, 2, 3, 4])
+def test_full_size_case_sampled(cfg):
+    """The five cases at full size, in the launch configuration the bench uses;
+    the cache is packed on the device from device-drawn bf16 rows, and sampled
+    query tokens are checked against the oracle (which re-encodes the selected
+    rows from the same bf16 inputs)."""
+    case = workloads.make_case(cfg)
+    rows_total = case.num_pages * 64
+    lat, rope = workloads.device_rows(case, rows_total, "cuda")
+    cache = torch.empty((case.num_pages, 64, 352), dtype=torch.uint8, device="cuda")
+    m.mla_kv_pack(lat, rope, torch.arange(rows_total, device="cuda"), cache)
+    status = torch.zeros(4, dtype=torch.int32, device="cuda")
+    out, lse = _decode(case, cache, dev_status=status)
+    assert status.cpu().tolist() == [0, 0, 0, 0]
+    rng = np.random.default_rng(cfg)
+    units = [(0, 0), (case.B - 1, case.Q - 1)]
+    units += [(int(rng.integers(case.B)), int(rng.integers(case.Q))) for _ in range(4)]
+    ref = oracle_units_from_device_rows(case, units, lat, rope)
+    o = out.float().cpu().numpy()
+    l = lse.cpu().numpy()
+    for (b, j), (ro, rl) in ref.items():
+        assert_close(o[b, j], l[b, j], ro, rl, f"cfg {cfg} unit {(b, j)}")
+    # every output finite; lse finite where the query has usable entries
+    assert np.isfinite(o).all()

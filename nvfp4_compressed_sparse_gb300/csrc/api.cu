@@ -45,12 +45,23 @@ DecodeSchedule make_schedule(int B, int Q, int H, int topk, int num_sms, int max
 
 static inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-size_t workspace_bytes_for(const DecodeSchedule& s, int H) {
+// Workspace: partial O [slots, nh, 512] f32 | partial (max, sum) [slots, nh, 2] f32 |
+// FP16 q images [units, 9 * nh * 128] | q scales [units] f32; each part 256-byte aligned.
+struct WorkspaceLayout {
+  size_t o, ml, q16, qscale, total;
+};
+static WorkspaceLayout layout_for(const DecodeSchedule& s, int H) {
   const int nh = H < kHeadsPerCta ? H : kHeadsPerCta;
-  const size_t o = (size_t)s.partial_slots * nh * kLatent * sizeof(float);
-  const size_t ml = (size_t)s.partial_slots * nh * 2 * sizeof(float);
-  return align256(o) + align256(ml);
+  WorkspaceLayout w;
+  w.o = 0;
+  w.ml = w.o + align256((size_t)s.partial_slots * nh * kLatent * sizeof(float));
+  w.q16 = w.ml + align256((size_t)s.partial_slots * nh * 2 * sizeof(float));
+  w.qscale = w.q16 + align256((size_t)s.units * 9 * nh * 128);
+  w.total = w.qscale + align256((size_t)s.units * sizeof(float));
+  return w;
 }
+
+size_t workspace_bytes_for(const DecodeSchedule& s, int H) { return layout_for(s, H).total; }
 
 static bool sizes_ok(int B, int Q, int H, int topk) {
   if (B < 1 || Q < 1 || Q > 16 || topk < 1 || topk > NVFP4MLA_MAX_TOPK) return false;
@@ -143,9 +154,12 @@ int sparse_mla_decode(const void* q, const void* kv_cache, int64_t num_pages, co
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
   p.out = static_cast<uint16_t*>(out);
   p.lse = lse;
-  const size_t o_bytes = (size_t)s.partial_slots * p.heads_per_cta * kLatent * sizeof(float);
-  p.part_o = static_cast<float*>(workspace);
-  p.part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + align256(o_bytes));
+  const WorkspaceLayout wl = layout_for(s, H);
+  uint8_t* wsb = static_cast<uint8_t*>(workspace);
+  p.part_o = reinterpret_cast<float*>(wsb + wl.o);
+  p.part_ml = reinterpret_cast<float*>(wsb + wl.ml);
+  p.q16 = wsb + wl.q16;
+  p.qscale = reinterpret_cast<float*>(wsb + wl.qscale);
   p.status = dev_status;
   p.units = s.units;
   p.total_tiles = s.total_tiles;

@@ -57,7 +57,7 @@ struct alignas(16) Smem {
   uint64_t s_full;
   uint64_t p_full;
   uint64_t o_done;
-  uint64_t q_ready;
+  uint64_t q_full;
   uint64_t drain;
   uint32_t tmem_base;
   volatile int abort;
@@ -65,7 +65,6 @@ struct alignas(16) Smem {
   uint32_t vmask[2][4];              // dequant -> softmax: valid rows of the tile, by tile parity
   float red[4][32];                  // softmax group: per-warp partial reductions
   int need_rescale;
-  float qmax[4];
 };
 
 struct TileInfo {
@@ -107,41 +106,74 @@ __device__ __forceinline__ void split_unit(const DecodeParams& p, int64_t unit, 
 }
 
 // ------------------------------------------------------------------ producer
-__device__ void producer_loop(const DecodeParams& p, Smem* sm, uint8_t* ring, int64_t t_begin, int64_t t_end) {
+// Index resolution is software-pipelined two tiles ahead: while tile g's rows
+// are issued, the page-table words of tile g+1 and the index words of tile g+2
+// are already in flight, so the dependent index -> page -> row chain never
+// stalls the gathers.
+struct TileIdx {
+  int idx[4];     // this lane's entries of the tile's four 32-row stages
+  int L, causal;  // sequence length, causal limit of the query
+  int b;
+};
+
+__device__ __forceinline__ void load_tile_idx(const DecodeParams& p, int64_t g, int lane, TileIdx& t) {
+  const int64_t unit = g / p.tiles_per_unit;
+  const int local = (int)(g - unit * p.tiles_per_unit);
+  int b, j, hg;
+  split_unit(p, unit, b, j, hg);
+  t.b = b;
+  t.L = __ldg(p.seq_lens + b);
+  t.causal = t.L - p.Q + j;
+  const int32_t* row = p.idx + ((int64_t)b * p.Q + j) * p.topk;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int e = local * kTileTokens + q * 32 + lane;
+    t.idx[q] = e < p.topk ? __ldg(row + e) : -1;
+  }
+}
+
+__device__ __forceinline__ void load_tile_pages(const DecodeParams& p, const TileIdx& t, int (&pg)[4]) {
+  const int32_t* pt_row = p.page_table + (int64_t)t.b * p.max_pages;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int idx = t.idx[q];
+    const bool in_range = idx >= 0 && idx < t.L && idx <= t.causal;
+    pg[q] = (in_range && (idx >> 6) < p.max_pages) ? __ldg(pt_row + (idx >> 6)) : -1;
+  }
+}
+
+__device__ void producer_loop(const DecodeParams& p, Smem* sm, uint8_t* ring, uint8_t* qs, int64_t t_begin,
+                              int64_t t_end) {
   const int lane = threadIdx.x & 31;
+  const uint32_t qbytes = 9u * (uint32_t)p.heads_per_cta * 128u;
   uint32_t issued[kRingStages] = {0, 0, 0, 0};
+  uint32_t q_issued = 0;
+  TileIdx A0, A1, A2;
+  int pg0[4], pg1[4];
+  if (t_begin < t_end) load_tile_idx(p, t_begin, lane, A0);
+  if (t_begin + 1 < t_end) load_tile_idx(p, t_begin + 1, lane, A1);
+  if (t_begin < t_end) load_tile_pages(p, A0, pg0);
+  asm volatile("griddepcontrol.wait;" ::: "memory");   // q16 / qscale come from the prep kernel
   for (int64_t g = t_begin; g < t_end && !sm->abort; ++g) {
     const int64_t k = g - t_begin;
     const TileInfo ti = tile_info(p, g, t_begin, t_end);
-    int b, j, hg;
-    split_unit(p, ti.unit, b, j, hg);
-    const int64_t u = (int64_t)b * p.Q + j;
-    const int L = __ldg(p.seq_lens + b);
-    const int causal = L - p.Q + j;
-    const int32_t* idx_row = p.idx + u * p.topk;
-    const int32_t* pt_row = p.page_table + (int64_t)b * p.max_pages;
+    if (g + 1 < t_end) load_tile_pages(p, A1, pg1);
+    if (g + 2 < t_end) load_tile_idx(p, g + 2, lane, A2);
+    int hg = (int)(ti.unit % p.head_groups);
+    bool good = true;
     for (int q = 0; q < kRingStages; ++q) {
-      const int e = ti.local * kTileTokens + q * 32 + lane;
-      int idx = -1;
-      if (e < p.topk) idx = __ldg(idx_row + e);
-      bool ok = idx >= 0 && idx < L && idx <= causal;
-      const bool bad_index = (idx != -1) && !ok && e < p.topk;
-      int64_t page = -1;
-      if (ok) {
-        const int col = idx >> 6;
-        if (col < p.max_pages) page = __ldg(pt_row + col);
-        ok = page >= 0 && page < p.num_pages;
-      }
-      const bool bad_page = (idx >= 0 && idx < L && idx <= causal) && !ok;
+      const int idx = A0.idx[q];
+      const int page = pg0[q];
+      const bool in_range = idx >= 0 && idx < A0.L && idx <= A0.causal;
+      const bool ok = in_range && page >= 0 && page < p.num_pages;
       if (hg == 0 && p.status != nullptr) {
-        const uint32_t nbi = __popc(__ballot_sync(0xffffffffu, bad_index));
-        const uint32_t nbp = __popc(__ballot_sync(0xffffffffu, bad_page));
+        const int e = ti.local * kTileTokens + q * 32 + lane;
+        const uint32_t nbi = __popc(__ballot_sync(0xffffffffu, idx != -1 && !in_range && e < p.topk));
+        const uint32_t nbp = __popc(__ballot_sync(0xffffffffu, in_range && !ok));
         if (lane == 0 && nbi) atomicAdd(p.status + 0, (int)nbi);
         if (lane == 0 && nbp) atomicAdd(p.status + 1, (int)nbp);
       }
       const uint32_t mask = __ballot_sync(0xffffffffu, ok);
-      // wait until the dequant warps released this ring stage (previous tile)
-      bool good = true;
       if (lane == 0) good = wait(sm, &sm->ring_empty[q], (uint32_t)((k & 1) ^ 1), p.status);
       good = __shfl_sync(0xffffffffu, good, 0);
       if (!good) break;
@@ -156,12 +188,30 @@ __device__ void producer_loop(const DecodeParams& p, Smem* sm, uint8_t* ring, in
       }
       issued[q] = (uint32_t)(k + 1);
     }
-    if (sm->abort) break;
+    if (!good || sm->abort) break;
+    if (ti.first) {
+      // The unit changes: copy its pre-converted q image once the previous tile's QK is done with the buffer.
+      if (lane == 0) {
+        good = (k == 0) || wait(sm, &sm->s_full, (uint32_t)(((k - 1) & 1)), p.status);
+        if (good) {
+          mbar_arrive_expect_tx(&sm->q_full, qbytes);
+          bulk_g2s(qs, p.q16 + ti.unit * (int64_t)qbytes, qbytes, &sm->q_full);
+          ++q_issued;
+        }
+      }
+      good = __shfl_sync(0xffffffffu, good, 0);
+      if (!good) break;
+    }
+    A0 = A1;
+    A1 = A2;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) pg0[q] = pg1[q];
   }
-  // Never leave with bulk copies in flight: wait (bounded) for the last phase issued on each stage.
+  // Never leave with bulk copies in flight: wait (bounded) for the last phase issued on each barrier.
   if (lane == 0) {
     for (int q = 0; q < kRingStages; ++q)
       if (issued[q] > 0) mbar_wait(&sm->ring_full[q], (issued[q] - 1) & 1, nullptr, kWaitTimeoutNs);
+    if (q_issued > 0) mbar_wait(&sm->q_full, (q_issued - 1) & 1, nullptr, kWaitTimeoutNs);
   }
   __syncwarp();
 }
@@ -271,7 +321,7 @@ __device__ void mma_loop(const DecodeParams& p, Smem* sm, uint8_t* vtile, uint8_
   for (int64_t g = t_begin; g < t_end; ++g) {
     const int64_t k = g - t_begin;
     const TileInfo ti = tile_info(p, g, t_begin, t_end);
-    if (ti.first && !wait(sm, &sm->q_ready, (uint32_t)(seg & 1), p.status)) break;
+    if (ti.first && !wait(sm, &sm->q_full, (uint32_t)(seg & 1), p.status)) break;
     if (!wait(sm, &sm->kv_ready, (uint32_t)(k & 1), p.status)) break;
     tc_fence_after();
     // S^T = K . Q^T ; issuer 0 takes k-steps 0..17, issuer 1 takes 18..35 (own accumulator each)
@@ -344,55 +394,16 @@ __device__ void softmax_loop(const DecodeParams& p, Smem* sm, uint8_t* qs, uint8
   float qscale = 0.f;
   int64_t seg = 0;
   bool ok = true;
+  asm volatile("griddepcontrol.wait;" ::: "memory");   // qscale comes from the prep kernel
   for (int64_t g = t_begin; g < t_end && ok; ++g) {
     const int64_t k = g - t_begin;
     const TileInfo ti = tile_info(p, g, t_begin, t_end);
     if (ti.first) {
-      // ---- stage q of this unit as FP16, scaled by 2^e so that max|q| * 2^e is in [2^14, 2^15)
-      int b, j, hg;
-      split_unit(p, ti.unit, b, j, hg);
-      const uint16_t* qsrc = p.q + (((int64_t)b * p.Q + j) * p.H + (int64_t)hg * NH) * kQK;
-      constexpr int kChunks = NH * (kQK / 8);
-      float mx = 0.f;
-      for (int c = t; c < kChunks; c += 128) {
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(qsrc) + c);
-        const uint32_t ww[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(ww[i] << 16)), fabsf(__uint_as_float(ww[i] & 0xFFFF0000u))));
-      }
-#pragma unroll
-      for (int s = 16; s >= 1; s >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, s));
-      if (lane == 0) sm->qmax[w] = mx;
-      named_sync_softmax();
-      mx = fmaxf(fmaxf(sm->qmax[0], sm->qmax[1]), fmaxf(sm->qmax[2], sm->qmax[3]));
-      int e = 0;
-      if (mx > 0.f && isfinite(mx)) {
-        int E;
-        frexpf(mx, &E);                    // mx in [2^(E-1), 2^E)
-        e = 15 - E;
-      }
-      const float up = ldexpf(1.f, e);
-      for (int c = t; c < kChunks; c += 128) {
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(qsrc) + c);
-        const uint32_t ww[4] = {v.x, v.y, v.z, v.w};
-        uint32_t o[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const __half2 h = __floats2half2_rn(__uint_as_float(ww[i] << 16) * up, __uint_as_float(ww[i] & 0xFFFF0000u) * up);
-          o[i] = *reinterpret_cast<const uint32_t*>(&h);
-        }
-        const int h = c / (kQK / 8), cc = c % (kQK / 8);
-        const int atom = cc >> 3, ch = cc & 7;
-        *reinterpret_cast<uint4*>(qs + atom * (NH * 128) + h * 128 + ((ch ^ (h & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-      }
-      fence_proxy_async_smem();
-      qscale = p.scale_log2 * ldexpf(1.f, -e);
+      qscale = p.qscale[ti.unit];
 #pragma unroll
       for (int h = 0; h < 32; ++h) l_part[h] = 0.f;
       if (t < 32) sm->m_used[t] = kNegInf;
       named_sync_softmax();
-      mbar_arrive(&sm->q_ready);
     }
     // ---- scores of this tile
     if (wait(sm, &sm->kv_ready, (uint32_t)(k & 1), p.status)) wait(sm, &sm->s_full, (uint32_t)(k & 1), p.status);
@@ -553,6 +564,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
 
   const int warp = threadIdx.x >> 5;
   const int64_t cta = blockIdx.x;
+  // Every decode CTA is resident once all of them reach this point, so letting the
+  // merge grid be scheduled now cannot take resources a decode CTA still needs.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int64_t t_begin = cta * p.total_tiles / p.ctas;
   const int64_t t_end = (cta + 1) * p.total_tiles / p.ctas;
 
@@ -566,7 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
     mbar_init(&sm->s_full, 2);
     mbar_init(&sm->p_full, 128);
     mbar_init(&sm->o_done, 2);
-    mbar_init(&sm->q_ready, 128);
+    mbar_init(&sm->q_full, 1);
     mbar_init(&sm->drain, 2);
     sm->abort = 0;
     fence_barrier_init();
@@ -580,7 +594,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
   tc_fence_after();
 
   if (warp == 0) {
-    producer_loop(p, sm, ring, t_begin, t_end);
+    producer_loop(p, sm, ring, qs, t_begin, t_end);
   } else if (warp == 1 || warp == 2) {
     if ((threadIdx.x & 31) == 0) mma_loop<NH>(p, sm, vtile, qs, ps, t_begin, t_end, warp - 1);
     __syncwarp();
@@ -597,36 +611,88 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
   }
 }
 
-// ------------------------------------------------------------------ merge
-// One block per (virtual unit, head): combine the partials of the CTAs that
-// covered the unit with the log-sum-exp rule; write bf16 out and fp32 LSE.
+// ------------------------------------------------------------------ q prep
+// One block per (query, head group): q (bf16) -> FP16 scaled by 2^e so that
+// max|q| * 2^e lies in [2^14, 2^15), written as the exact shared-memory image
+// the decode CTA uses as the UMMA B operand (K-major, 128-byte swizzle: 9 atoms
+// of NH rows x 128 B). qscale = softmax_scale * log2(e) * 2^-e.
 template <int NH>
-__global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(256) q_prep_kernel(const DecodeParams p) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  __shared__ float wmax[8];
+  const int64_t unit = blockIdx.x;
+  int b, j, hg;
+  split_unit(p, unit, b, j, hg);
+  const uint16_t* src = p.q + (((int64_t)b * p.Q + j) * p.H + (int64_t)hg * NH) * kQK;
+  uint8_t* dst = p.q16 + unit * (int64_t)(9 * NH * 128);
+  constexpr int kChunks = NH * (kQK / 8);
+  float mx = 0.f;
+  for (int c = threadIdx.x; c < kChunks; c += 256) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(src) + c);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(w[i] << 16)), fabsf(__uint_as_float(w[i] & 0xFFFF0000u))));
+  }
+#pragma unroll
+  for (int s = 16; s >= 1; s >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, s));
+  if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = mx;
+  __syncthreads();
+  mx = wmax[0];
+#pragma unroll
+  for (int i = 1; i < 8; ++i) mx = fmaxf(mx, wmax[i]);
+  int e = 0;
+  if (mx > 0.f && isfinite(mx)) {
+    int E;
+    frexpf(mx, &E);     // mx in [2^(E-1), 2^E)
+    e = 15 - E;
+  }
+  const float up = ldexpf(1.f, e);
+  for (int c = threadIdx.x; c < kChunks; c += 256) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(src) + c);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __half2 h = __floats2half2_rn(__uint_as_float(w[i] << 16) * up, __uint_as_float(w[i] & 0xFFFF0000u) * up);
+      o[i] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    const int h = c / (kQK / 8), cc = c % (kQK / 8);
+    const int atom = cc >> 3, ch = cc & 7;
+    *reinterpret_cast<uint4*>(dst + atom * (NH * 128) + h * 128 + ((ch ^ (h & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+  if (threadIdx.x == 0) p.qscale[unit] = p.scale_log2 * ldexpf(1.f, -e);
+}
+
+// ------------------------------------------------------------------ merge
+// Block (virtual unit, group of 4 heads), 512 threads: 128 threads per head,
+// 4 latent dims each. Combines the partials of the CTAs that covered the unit
+// with the log-sum-exp rule; writes bf16 out and fp32 LSE (natural log).
+template <int NH>
+__global__ void __launch_bounds__(512) merge_kernel(const DecodeParams p) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int64_t unit = blockIdx.x;
-  const int h = blockIdx.y;
+  const int h = blockIdx.y * 4 + (threadIdx.x >> 7);
+  const int d4 = threadIdx.x & 127;
   const int64_t g0 = unit * p.tiles_per_unit, g1 = g0 + p.tiles_per_unit - 1;
   const int64_t c_lo = ((g0 + 1) * p.ctas - 1) / p.total_tiles;
   const int64_t c_hi = ((g1 + 1) * p.ctas - 1) / p.total_tiles;
   const float kNegInf = __int_as_float(0xff800000);
   float mstar = kNegInf;
   for (int64_t c = c_lo; c <= c_hi; ++c) {
-    const int64_t slot = c + unit;
-    const float m = p.part_ml[(slot * NH + h) * 2];
-    const float l = p.part_ml[(slot * NH + h) * 2 + 1];
-    if (l > 0.f) mstar = fmaxf(mstar, m);
+    const float2 ml = reinterpret_cast<const float2*>(p.part_ml)[(c + unit) * NH + h];
+    if (ml.y > 0.f) mstar = fmaxf(mstar, ml.x);
   }
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float lsum = 0.f;
   if (mstar != kNegInf) {
     for (int64_t c = c_lo; c <= c_hi; ++c) {
       const int64_t slot = c + unit;
-      const float m = p.part_ml[(slot * NH + h) * 2];
-      const float l = p.part_ml[(slot * NH + h) * 2 + 1];
-      if (!(l > 0.f)) continue;
-      const float wgt = exp2f(m - mstar);
-      lsum += wgt * l;
-      const float4 o = reinterpret_cast<const float4*>(p.part_o + (slot * NH + h) * (int64_t)kLatent)[threadIdx.x];
+      const float2 ml = reinterpret_cast<const float2*>(p.part_ml)[slot * NH + h];
+      if (!(ml.y > 0.f)) continue;
+      const float wgt = exp2f(ml.x - mstar);
+      lsum += wgt * ml.y;
+      const float4 o = reinterpret_cast<const float4*>(p.part_o + (slot * NH + h) * (int64_t)kLatent)[d4];
       acc.x += wgt * o.x; acc.y += wgt * o.y; acc.z += wgt * o.z; acc.w += wgt * o.w;
     }
   }
@@ -639,8 +705,8 @@ __global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p) {
   uint2 packed;
   packed.x = *reinterpret_cast<const uint32_t*>(&lo);
   packed.y = *reinterpret_cast<const uint32_t*>(&hi);
-  reinterpret_cast<uint2*>(p.out + row * kLatent)[threadIdx.x] = packed;
-  if (threadIdx.x == 0) p.lse[row] = lsum > 0.f ? (mstar + log2f(lsum)) * 0.69314718055994530942f : kNegInf;
+  reinterpret_cast<uint2*>(p.out + row * kLatent)[d4] = packed;
+  if (d4 == 0) p.lse[row] = lsum > 0.f ? (mstar + log2f(lsum)) * 0.69314718055994530942f : kNegInf;
 }
 
 template <int NH>
@@ -650,31 +716,44 @@ constexpr size_t decode_smem_bytes() {
 
 }  // namespace
 
+static cudaLaunchAttribute pdl_attr() {
+  cudaLaunchAttribute a;
+  a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  a.val.programmaticStreamSerializationAllowed = 1;
+  return a;
+}
+
+// q prep (ordinary launch) -> decode (PDL) -> merge (PDL): each dependent grid is
+// launched early and waits with griddepcontrol.wait before reading its inputs.
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream) {
   cudaError_t err;
-  if (p.heads_per_cta == 32) {
-    constexpr size_t smem = decode_smem_bytes<32>();
-    err = cudaFuncSetAttribute(decode_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (err != cudaSuccess) return err;
-    decode_kernel<32><<<p.ctas, kThreads, smem, stream>>>(p);
-  } else {
-    constexpr size_t smem = decode_smem_bytes<16>();
-    err = cudaFuncSetAttribute(decode_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (err != cudaSuccess) return err;
-    decode_kernel<16><<<p.ctas, kThreads, smem, stream>>>(p);
-  }
-  return cudaGetLastError();
+  const bool h32 = p.heads_per_cta == 32;
+  if (h32) q_prep_kernel<32><<<(unsigned)p.units, 256, 0, stream>>>(p);
+  else q_prep_kernel<16><<<(unsigned)p.units, 256, 0, stream>>>(p);
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  const size_t smem = h32 ? decode_smem_bytes<32>() : decode_smem_bytes<16>();
+  const void* fn = h32 ? (const void*)decode_kernel<32> : (const void*)decode_kernel<16>;
+  err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)p.ctas, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1] = {pdl_attr()};
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (h32) return cudaLaunchKernelEx(&cfg, decode_kernel<32>, p);
+  return cudaLaunchKernelEx(&cfg, decode_kernel<16>, p);
 }
 
 cudaError_t launch_merge(const DecodeParams& p, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)p.units, (unsigned)p.heads_per_cta, 1);
-  cfg.blockDim = dim3(128, 1, 1);
+  cfg.gridDim = dim3((unsigned)p.units, (unsigned)(p.heads_per_cta / 4), 1);
+  cfg.blockDim = dim3(512, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[1] = {pdl_attr()};
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (p.heads_per_cta == 32) return cudaLaunchKernelEx(&cfg, merge_kernel<32>, p);

@@ -47,6 +47,8 @@ struct DecodeParams {
   float* lse;                 // [B, Q, H]
   float* part_o;              // [slots, heads_per_cta, 512]
   float* part_ml;             // [slots, heads_per_cta, 2]  (running max in log2 units, sum)
+  uint8_t* q16;               // [units, 9 * heads_per_cta * 128]: FP16 q image in UMMA B layout
+  float* qscale;              // [units]: softmax_scale * log2(e) * 2^-e for the unit's q scaling
   int32_t* status;            // optional
   int64_t units, total_tiles;
   int tiles_per_unit, ctas;

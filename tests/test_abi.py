@@ -40,18 +40,18 @@ def test_status_strings(lib):
     assert m.status_string(99) == "unknown status"
 
 
+def _ws(slots, units, nh):
+    r = lambda x: (x + 255) // 256 * 256
+    return r(slots * nh * 512 * 4) + r(slots * nh * 2 * 4) + r(units * 9 * nh * 128) + r(units * 4)
+
+
 def test_workspace_size_formula(lib):
     # 152 SMs, B=64, Q=1, H=32, topk=2048: 64 units x 16 tiles; 152 CTAs; 215 partial slots
-    n = lib.sparse_mla_decode_workspace_size(64, 1, 32, 2048, 152)
-    slots = 152 + 64 - 1
-    o = slots * 32 * 512 * 4
-    ml = slots * 32 * 2 * 4
-    r = lambda x: (x + 255) // 256 * 256
-    assert n == r(o) + r(ml)
+    assert lib.sparse_mla_decode_workspace_size(64, 1, 32, 2048, 152) == _ws(152 + 64 - 1, 64, 32)
     # fewer tiles than SMs: one CTA per tile
-    assert lib.sparse_mla_decode_workspace_size(1, 1, 16, 256, 152) == r((2 + 1 - 1) * 16 * 512 * 4) + r(2 * 16 * 2 * 4)
+    assert lib.sparse_mla_decode_workspace_size(1, 1, 16, 256, 152) == _ws(2 + 1 - 1, 1, 16)
     # H=128 -> 4 head groups of 32
-    assert lib.sparse_mla_decode_workspace_size(2, 1, 128, 128, 152) == r((8 + 8 - 1) * 32 * 512 * 4) + r(15 * 32 * 8)
+    assert lib.sparse_mla_decode_workspace_size(2, 1, 128, 128, 152) == _ws(8 + 8 - 1, 8, 32)
     for bad in [(0, 1, 32, 2048), (1, 0, 32, 2048), (1, 17, 32, 2048), (1, 1, 48, 2048), (1, 1, 32, 0), (1, 1, 32, 8193)]:
         assert lib.sparse_mla_decode_workspace_size(*bad, 152) == 0
 

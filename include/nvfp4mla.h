@@ -157,6 +157,34 @@ int sparse_mla_decode(const void* q, const void* kv_cache, int64_t num_pages, co
                       int Q, int H, int topk, float softmax_scale, void* out, float* lse, void* workspace,
                       size_t workspace_bytes, int32_t* dev_status, uint32_t flags, void* stream);
 
+/*
+ * sparse_mla_decode_noalloc: sparse_mla_decode for callers that cannot
+ * allocate device memory. (The pages describe no such call; this is a
+ * deployment convenience of this library.)
+ *
+ * Some callers cannot allocate or pass a scratch buffer: an operator running
+ * inside a serving engine that has reserved all device memory for its own
+ * pool, a plugin whose enqueue signature has no workspace argument, or a path
+ * that must never enter the CUDA allocator. This call computes exactly what
+ * sparse_mla_decode computes, with the same arguments minus the workspace; its
+ * scratch is a fixed NVFP4MLA_NOALLOC_SCRATCH_BYTES region of device memory
+ * that the library reserves statically on every GPU where it is loaded (held
+ * until the process exits). It allocates nothing.
+ *   - The first call on a device looks up that region's address on the
+ *     current device; make the first call before any stream capture starts.
+ *   - All calls on a device share the region: calls whose work overlaps on the
+ *     GPU race. Order them on one stream (or with events).
+ *   - The region needs no initialisation; each call writes what it reads.
+ *   - Returns NVFP4MLA_ERR_WORKSPACE, before enqueuing anything, when the sizes
+ *     need more scratch than the region holds (see
+ *     sparse_mla_decode_workspace_size); otherwise as sparse_mla_decode.
+ */
+#define NVFP4MLA_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+int sparse_mla_decode_noalloc(const void* q, const void* kv_cache, int64_t num_pages, const int32_t* page_table,
+                              int64_t max_pages_per_seq, const int32_t* topk_indices, const int32_t* seq_lens, int B,
+                              int Q, int H, int topk, float softmax_scale, void* out, float* lse, int32_t* dev_status,
+                              uint32_t flags, void* stream);
+
 /* Human-readable name of a return code (static string, never NULL). */
 const char* nvfp4mla_status_string(int status);
 

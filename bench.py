@@ -350,9 +350,9 @@ def run_gpu(args, world, rank, local):
                      "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic_from_profile(),
                      "peak_kind": peak_kind, "algorithmic_bytes": nbytes, "algorithmic_flops": flops,
                      "roofline_us": max(roof_hbm_us, roof_tc_us), "tensor_roofline_us": roof_tc_us,
-                     "timed_unit": "sparse_mla_decode call (decode kernel + merge kernel)"},
+                     "timed_unit": "sparse_mla_decode call (q prep + decode + merge kernels)"},
         "e2e": {"value": e2e_ms * 1000.0, "unit": "us/step", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": 2 * K,
+        "gpu_launches": 3 * K,
         "clocks": clk,
         "pack": {"rows": pack_rows, "us": pack_ms * 1000.0, "gbs": pack_bytes / (pack_ms * 1e-3) / 1e9,
                  "frac_of_hbm": pack_bytes / (pack_ms * 1e-3) / 1e9 / hbm},

@@ -70,6 +70,37 @@ static bool sizes_ok(int B, int Q, int H, int topk) {
 
 static inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// cuTensorMapEncodeTiled, fetched once through the runtime (no link-time libcuda dependency).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+static EncodeTiledFn encode_tiled_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+// The cache as a 2-D tensor of uint32: rows of 88 words (352 B), one row per token slot. Row gathers use
+// TMA tile::gather4 with a one-row box; rows outside [0, rows) (the -1 of unused entries) read as zeros.
+static bool encode_cache_map(CUtensorMap* map, const void* cache, int64_t num_pages) {
+  EncodeTiledFn fn = encode_tiled_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)(kRowBytes / 4), (cuuint64_t)(num_pages * kPageTokens)};
+  const cuuint64_t strides[1] = {(cuuint64_t)kRowBytes};
+  const cuuint32_t box[2] = {(cuuint32_t)(kRowBytes / 4), 1};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(cache), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace nvfp4mla
 
 using namespace nvfp4mla;
@@ -136,8 +167,10 @@ int sparse_mla_decode(const void* q, const void* kv_cache, int64_t num_pages, co
   const size_t need = workspace_bytes_for(s, H);
   if (workspace == nullptr || workspace_bytes < need) return NVFP4MLA_ERR_WORKSPACE;
   if (!aligned(workspace, 256)) return NVFP4MLA_ERR_ALIGNMENT;
+  if (num_pages * kPageTokens > (int64_t)INT32_MAX) return NVFP4MLA_ERR_UNSUPPORTED;   // int32 row coordinates
 
   DecodeParams p{};
+  if (!encode_cache_map(&p.cache_map, kv_cache, num_pages)) return NVFP4MLA_ERR_CUDA;
   p.q = static_cast<const uint16_t*>(q);
   p.cache = static_cast<const uint8_t*>(kv_cache);
   p.num_pages = num_pages;

@@ -1,4 +1,4 @@
-// sparse_mla_decode kernels: NVFP4 sparse MLA decode on sm_103a (tcgen05 + TMEM).
+// sparse_mla_decode kernels: NVFP4 sparse MLA decode on sm_103a (tcgen05 + TMEM + TMA).
 //
 // What is computed ("Prime Inference", translated page, "Native NVFP4 sparse MLA
 // decode kernel"; "Serving GLM-5.3 ...", "A kernel that reads four bits
@@ -6,20 +6,24 @@
 // selects, unpacks them on chip, and computes softmax attention with 16-bit
 // operands and FP32 accumulation. -1 entries are not loaded.
 //
-// GB300 design (see the design notes for the measurements behind it):
+// GB300 design:
 //  * Tokens on the UMMA M axis (M = 128 rows per tile), heads on N (16 or 32):
 //    S^T[tok, h] = K[tok, :] . q[h, :] and O^T[dim, h] = sum_tok V[tok, dim] P[tok, h].
-//  * The dequantised tile is written once per row by the thread that owns the
-//    row: the 576-wide K row into TMEM (A operand of the QK UMMA, read from
-//    TMEM), the 512-wide latent into shared memory (the V operand of PV, read
-//    MN-major from the same bytes).
-//  * Two MMA issuer threads (a single issuing thread caps out near 46-49
-//    cycles per M=128 UMMA; two reach the operand-bandwidth bound).
-//  * Rows are gathered with cp.async.bulk (352 B each, one per selected entry)
-//    into a 4-stage ring; -1 and other unusable entries issue no load and are
-//    zero-filled in V and masked in the softmax.
-//  * Work is cut stream-K style: the tiles of all (query, head-group) units
-//    form one sequence split evenly across the CTAs; each CTA writes one
+//  * Rows are gathered by TMA (tile::gather4: four arbitrary 352-byte cache rows
+//    per instruction, issued by two producer warps) into a one-tile ring;
+//    unusable entries use row -1, which the TMA unit zero-fills.
+//  * Eight dequant warps (thread = tile row) convert each row once into the fp16
+//    K tile in TMEM (pass A: the A operand of the QK UMMA) and later copy its
+//    latent part from TMEM into the V tile in shared memory (pass B: the A
+//    operand of PV, read MN-major).
+//  * The 576 K columns are split into two halves (latent 0..255; latent
+//    256..511 + rope), each with its own dequant warps, MMA issuer, and
+//    barriers, so the halves pipeline independently and meet only in the
+//    softmax group (which adds the two partial score accumulators).
+//  * Four softmax warps keep a lazily raised running max per head, write P
+//    (fp16) to shared memory and accumulate the row sums.
+//  * Work is cut stream-K style: the tiles of all (query, head-group) units form
+//    one sequence split evenly across the CTAs; each CTA writes one
 //    unnormalised partial (O, running max, sum) per unit it touches, and the
 //    merge kernel combines them with the log-sum-exp rule.
 //  * Operands are FP16: the dequantised e2m1 x E4M3 products are exact in FP16,
@@ -39,8 +43,8 @@ using namespace ptx;
 
 constexpr int kThreads = 512;
 constexpr int kRingStages = 4;            // one tile of 4 x 32 rows
-constexpr int kRingRowStride = 368;       // 352 padded to 23 x 16 B (bank-conflict-free row reads)
-constexpr int kRingStageBytes = 32 * kRingRowStride;
+constexpr int kRingRowStride = kRowBytes; // rows land densely: gather4 writes 4 x 352 B per instruction
+constexpr int kRingStageBytes = 32 * kRingRowStride;   // 11264 = 88 x 128 B
 constexpr int kVBytes = 8 * 128 * 128;    // 8 SW128 atoms x 128 rows x 128 B
 constexpr int kTmemCols = 512;
 constexpr int kTmemK = 0;                 // K tile: 288 columns (576 fp16 per lane)
@@ -50,20 +54,29 @@ constexpr int kTmemS = 288;               // S_a, S_b: NH columns each
 struct alignas(16) Smem {
   alignas(16) float m_used[32];      // running max per head (log2 units); read as float4
   alignas(16) float alpha[32];       // rescale factor of this tile per head; read as float4
-  uint64_t ring_full[kRingStages];
-  uint64_t ring_empty[kRingStages];
-  uint64_t vfree[4];
-  uint64_t kv_ready;
-  uint64_t s_full;
-  uint64_t p_full;
-  uint64_t o_done;
-  uint64_t q_full;
-  uint64_t drain;
+  uint64_t ring_full[kRingStages];   // gathered rows of a 32-row stage have landed
+  uint64_t ring_empty[kRingStages];  // ... and have been converted (both dequant warps of the stage)
+  // Half h of a tile = latent dims 256h..256h+255 (half 1 also carries the rope dims). Each half has
+  // its own dequant warps and MMA issuer, so the two halves pipeline independently and only meet
+  // in the softmax.
+  uint64_t vfree[2][4];              // PV of half h has finished reading V rows 32w..32w+31 (1 commit)
+  uint64_t kv_ready[2];              // half h of the K tile is in TMEM (4 dequant warps)
+  uint64_t kfree[2];                 // QK of half h complete: that half of the K tile may be rewritten
+  uint64_t s_full;                   // QK of both halves complete (2 commits)
+  uint64_t s_free;                   // softmax has read S of a tile (4 warps): S may be overwritten
+  uint64_t v_ready[2];               // half h of the V rows of a tile is in shared memory (4 warps)
+  uint64_t mask_full[2];             // vmask of a tile written (4 warps), by tile parity
+  uint64_t p_full[2];                // P of a tile written (128 threads), double-buffered by tile parity
+  uint64_t o_done;                   // last PV of a unit segment complete (2 issuers)
+  uint64_t o_free;                   // epilogue has read O (128 threads)
+  uint64_t q_full;                   // q image of the unit copied in
+  uint64_t drain;                    // every UMMA of both issuers complete
   uint32_t tmem_base;
   volatile int abort;
-  uint32_t maskbuf[kRingStages];     // producer -> dequant: valid rows of each ring stage
-  uint32_t vmask[2][4];              // dequant -> softmax: valid rows of the tile, by tile parity
+  uint32_t maskbuf[kRingStages];     // producer -> dequant: usable rows of each ring stage
+  uint32_t vmask[2][4];              // dequant -> softmax: usable rows of the tile, by tile parity
   float red[4][32];                  // softmax group: per-warp partial reductions
+  int vote[4];                       // softmax group: does a warp see a score above max + kLazy
   int need_rescale;
 };
 
@@ -106,17 +119,21 @@ __device__ __forceinline__ void split_unit(const DecodeParams& p, int64_t unit, 
 }
 
 // ------------------------------------------------------------------ producer
+// Two producer warps; warp pw owns ring stages 2pw and 2pw+1 of every tile.
+// Rows are gathered by TMA tile::gather4 (four arbitrary cache rows per
+// instruction; lanes 0..7 each issue one per 32-row stage). Unusable entries
+// get row -1, which the TMA unit fills with zeros without reading memory, so
+// every stage always lands exactly 32 x 352 bytes.
 // Index resolution is software-pipelined two tiles ahead: while tile g's rows
 // are issued, the page-table words of tile g+1 and the index words of tile g+2
-// are already in flight, so the dependent index -> page -> row chain never
-// stalls the gathers.
+// are already in flight.
 struct TileIdx {
-  int idx[4];     // this lane's entries of the tile's four 32-row stages
+  int idx[2];     // this lane's entries of the warp's two 32-row stages
   int L, causal;  // sequence length, causal limit of the query
   int b;
 };
 
-__device__ __forceinline__ void load_tile_idx(const DecodeParams& p, int64_t g, int lane, TileIdx& t) {
+__device__ __forceinline__ void load_tile_idx(const DecodeParams& p, int64_t g, int lane, int q0, TileIdx& t) {
   const int64_t unit = g / p.tiles_per_unit;
   const int local = (int)(g - unit * p.tiles_per_unit);
   int b, j, hg;
@@ -126,44 +143,55 @@ __device__ __forceinline__ void load_tile_idx(const DecodeParams& p, int64_t g, 
   t.causal = t.L - p.Q + j;
   const int32_t* row = p.idx + ((int64_t)b * p.Q + j) * p.topk;
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const int e = local * kTileTokens + q * 32 + lane;
-    t.idx[q] = e < p.topk ? __ldg(row + e) : -1;
+  for (int qq = 0; qq < 2; ++qq) {
+    const int e = local * kTileTokens + (q0 + qq) * 32 + lane;
+    t.idx[qq] = e < p.topk ? __ldg(row + e) : -1;
   }
 }
 
-__device__ __forceinline__ void load_tile_pages(const DecodeParams& p, const TileIdx& t, int (&pg)[4]) {
+__device__ __forceinline__ void load_tile_pages(const DecodeParams& p, const TileIdx& t, int (&pg)[2]) {
   const int32_t* pt_row = p.page_table + (int64_t)t.b * p.max_pages;
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const int idx = t.idx[q];
+  for (int qq = 0; qq < 2; ++qq) {
+    const int idx = t.idx[qq];
     const bool in_range = idx >= 0 && idx < t.L && idx <= t.causal;
-    pg[q] = (in_range && (idx >> 6) < p.max_pages) ? __ldg(pt_row + (idx >> 6)) : -1;
+    pg[qq] = (in_range && (idx >> 6) < p.max_pages) ? __ldg(pt_row + (idx >> 6)) : -1;
   }
+}
+
+__device__ __forceinline__ void gather4(void* dst, const CUtensorMap* map, int r0, int r1, int r2, int r3,
+                                        uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar))
+      : "memory");
 }
 
 __device__ void producer_loop(const DecodeParams& p, Smem* sm, uint8_t* ring, uint8_t* qs, int64_t t_begin,
-                              int64_t t_end) {
+                              int64_t t_end, int pw) {
   const int lane = threadIdx.x & 31;
+  const int q0 = 2 * pw;
   const uint32_t qbytes = 9u * (uint32_t)p.heads_per_cta * 128u;
-  uint32_t issued[kRingStages] = {0, 0, 0, 0};
+  uint32_t issued[2] = {0, 0};
   uint32_t q_issued = 0;
   TileIdx A0, A1, A2;
-  int pg0[4], pg1[4];
-  if (t_begin < t_end) load_tile_idx(p, t_begin, lane, A0);
-  if (t_begin + 1 < t_end) load_tile_idx(p, t_begin + 1, lane, A1);
+  int pg0[2], pg1[2];
+  if (t_begin < t_end) load_tile_idx(p, t_begin, lane, q0, A0);
+  if (t_begin + 1 < t_end) load_tile_idx(p, t_begin + 1, lane, q0, A1);
   if (t_begin < t_end) load_tile_pages(p, A0, pg0);
-  asm volatile("griddepcontrol.wait;" ::: "memory");   // q16 / qscale come from the prep kernel
   for (int64_t g = t_begin; g < t_end && !sm->abort; ++g) {
     const int64_t k = g - t_begin;
     const TileInfo ti = tile_info(p, g, t_begin, t_end);
     if (g + 1 < t_end) load_tile_pages(p, A1, pg1);
-    if (g + 2 < t_end) load_tile_idx(p, g + 2, lane, A2);
-    int hg = (int)(ti.unit % p.head_groups);
+    if (g + 2 < t_end) load_tile_idx(p, g + 2, lane, q0, A2);
+    const int hg = (int)(ti.unit % p.head_groups);
     bool good = true;
-    for (int q = 0; q < kRingStages; ++q) {
-      const int idx = A0.idx[q];
-      const int page = pg0[q];
+#pragma unroll
+    for (int qq = 0; qq < 2; ++qq) {
+      const int q = q0 + qq;
+      const int idx = A0.idx[qq];
+      const int page = pg0[qq];
       const bool in_range = idx >= 0 && idx < A0.L && idx <= A0.causal;
       const bool ok = in_range && page >= 0 && page < p.num_pages;
       if (hg == 0 && p.status != nullptr) {
@@ -174,24 +202,28 @@ __device__ void producer_loop(const DecodeParams& p, Smem* sm, uint8_t* ring, ui
         if (lane == 0 && nbp) atomicAdd(p.status + 1, (int)nbp);
       }
       const uint32_t mask = __ballot_sync(0xffffffffu, ok);
+      const int row = ok ? page * kPageTokens + (idx & 63) : -1;
       if (lane == 0) good = wait(sm, &sm->ring_empty[q], (uint32_t)((k & 1) ^ 1), p.status);
       good = __shfl_sync(0xffffffffu, good, 0);
       if (!good) break;
       if (lane == 0) {
         sm->maskbuf[q] = mask;
-        mbar_arrive_expect_tx(&sm->ring_full[q], (uint32_t)__popc(mask) * kRowBytes);
+        mbar_arrive_expect_tx(&sm->ring_full[q], (uint32_t)kRingStageBytes);
       }
       __syncwarp();
-      if (ok) {
-        const uint8_t* src = p.cache + ((int64_t)page * kPageTokens + (idx & 63)) * kRowBytes;
-        bulk_g2s(ring + q * kRingStageBytes + lane * kRingRowStride, src, kRowBytes, &sm->ring_full[q]);
-      }
-      issued[q] = (uint32_t)(k + 1);
+      const int r0 = __shfl_sync(0xffffffffu, row, (4 * lane + 0) & 31);
+      const int r1 = __shfl_sync(0xffffffffu, row, (4 * lane + 1) & 31);
+      const int r2 = __shfl_sync(0xffffffffu, row, (4 * lane + 2) & 31);
+      const int r3 = __shfl_sync(0xffffffffu, row, (4 * lane + 3) & 31);
+      if (lane < 8) gather4(ring + q * kRingStageBytes + lane * 4 * kRowBytes, &p.cache_map, r0, r1, r2, r3, &sm->ring_full[q]);
+      issued[qq] = (uint32_t)(k + 1);
     }
     if (!good || sm->abort) break;
-    if (ti.first) {
+    if (pw == 0 && ti.first) {
       // The unit changes: copy its pre-converted q image once the previous tile's QK is done with the buffer.
       if (lane == 0) {
+        // q16 comes from the prep grid: only this copy has to wait for it, the row gathers do not.
+        if (q_issued == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
         good = (k == 0) || wait(sm, &sm->s_full, (uint32_t)(((k - 1) & 1)), p.status);
         if (good) {
           mbar_arrive_expect_tx(&sm->q_full, qbytes);
@@ -204,13 +236,13 @@ __device__ void producer_loop(const DecodeParams& p, Smem* sm, uint8_t* ring, ui
     }
     A0 = A1;
     A1 = A2;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) pg0[q] = pg1[q];
+    pg0[0] = pg1[0];
+    pg0[1] = pg1[1];
   }
   // Never leave with bulk copies in flight: wait (bounded) for the last phase issued on each barrier.
   if (lane == 0) {
-    for (int q = 0; q < kRingStages; ++q)
-      if (issued[q] > 0) mbar_wait(&sm->ring_full[q], (issued[q] - 1) & 1, nullptr, kWaitTimeoutNs);
+    for (int qq = 0; qq < 2; ++qq)
+      if (issued[qq] > 0) mbar_wait(&sm->ring_full[q0 + qq], (issued[qq] - 1) & 1, nullptr, kWaitTimeoutNs);
     if (q_issued > 0) mbar_wait(&sm->q_full, (q_issued - 1) & 1, nullptr, kWaitTimeoutNs);
   }
   __syncwarp();
@@ -218,6 +250,7 @@ __device__ void producer_loop(const DecodeParams& p, Smem* sm, uint8_t* ring, ui
 
 // ------------------------------------------------------------------ dequant
 // Thread = one tile row (token). half 0: latent dims 0..255; half 1: dims 256..511 + rope.
+// One group = 64 values (32 nibble bytes) sharing four block scales.
 __device__ __forceinline__ void convert_group(const uint8_t* rowp, int g, uint32_t (&r)[32]) {
   const uint4 n0 = *reinterpret_cast<const uint4*>(rowp + 32 * g);
   const uint4 n1 = *reinterpret_cast<const uint4*>(rowp + 32 * g + 16);
@@ -234,6 +267,11 @@ __device__ __forceinline__ void convert_group(const uint8_t* rowp, int g, uint32
   }
 }
 
+// Each dequant warp owns one TMEM lane quarter (tile rows 32q..32q+31) and half of the columns.
+// Pass A converts its rows into the fp16 K tile in TMEM (the A operand of the QK UMMA) and then
+// releases the ring stage. Pass B copies the latent part of those K rows from TMEM into the
+// V tile in shared memory (the A operand of PV, read MN-major) once PV of the previous tile is done
+// with those V rows, so the compressed rows are converted only once and leave the ring early.
 __device__ void dequant_loop(const DecodeParams& p, Smem* sm, const uint8_t* ring, uint8_t* vtile,
                              int64_t t_begin, int64_t t_end, int warp) {
   const int lane = threadIdx.x & 31;
@@ -244,98 +282,139 @@ __device__ void dequant_loop(const DecodeParams& p, Smem* sm, const uint8_t* rin
   const uint8_t* rowp = ring + q * kRingStageBytes + lane * kRingRowStride;
   for (int64_t g = t_begin; g < t_end; ++g) {
     const int64_t k = g - t_begin;
+    // ---- pass A: compressed rows -> fp16 K rows in TMEM
     bool good = true;
     if (lane == 0) {
       good = wait(sm, &sm->ring_full[q], (uint32_t)(k & 1), p.status);
-      if (good) good = wait(sm, &sm->vfree[q], (uint32_t)((k & 1) ^ 1), p.status);
+      // this half of the K tile may be rewritten once the previous tile's QK of the half is done
+      if (good && k > 0) good = wait(sm, &sm->kfree[half], (uint32_t)((k - 1) & 1), p.status);
     }
     good = __shfl_sync(0xffffffffu, good, 0);
     if (!good) break;
     __syncwarp();
     tc_fence_after();
     const uint32_t mask = sm->maskbuf[q];
-    const bool valid = (mask >> lane) & 1u;
     uint32_t r[32];
+    // Rows of unusable entries arrive zero-filled (scale bytes 0), so they dequantise to zeros.
 #pragma unroll 1
     for (int gi = 0; gi < 4; ++gi) {
       const int grp = 4 * half + gi;
-      if (valid) {
-        convert_group(rowp, grp, r);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) r[i] = 0u;
-      }
+      convert_group(rowp, grp, r);
       __syncwarp();
       tmem_st32(tmem_row + kTmemK + 32 * grp, r);
-      uint8_t* vrow = vtile + grp * 16384 + row * 128;
-#pragma unroll
-      for (int c = 0; c < 8; ++c)
-        *reinterpret_cast<uint4*>(vrow + ((c ^ (row & 7)) << 4)) = make_uint4(r[4 * c], r[4 * c + 1], r[4 * c + 2], r[4 * c + 3]);
     }
     if (half == 1) {
-      if (valid) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint4 v = *reinterpret_cast<const uint4*>(rowp + kRopeOff + 16 * c);
-          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      for (int c = 0; c < 4; ++c) {
+        const uint4 v = *reinterpret_cast<const uint4*>(rowp + kRopeOff + 16 * c);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            r[8 * c + 2 * i] = e4m3x2_to_f16x2(w[i] & 0xFFFFu);
-            r[8 * c + 2 * i + 1] = e4m3x2_to_f16x2(w[i] >> 16);
-          }
+        for (int i = 0; i < 4; ++i) {
+          r[8 * c + 2 * i] = e4m3x2_to_f16x2(w[i] & 0xFFFFu);
+          r[8 * c + 2 * i + 1] = e4m3x2_to_f16x2(w[i] >> 16);
         }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) r[i] = 0u;
       }
       __syncwarp();
       tmem_st32(tmem_row + kTmemK + 256, r);
     }
     tmem_wait_st();
     tc_fence_before();
-    fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
-      if (half == 0) sm->vmask[k & 1][q] = mask;
+      if (half == 0) {
+        sm->vmask[k & 1][q] = mask;
+        mbar_arrive(&sm->mask_full[k & 1]);
+      }
       mbar_arrive(&sm->ring_empty[q]);
-      mbar_arrive(&sm->kv_ready);
+      mbar_arrive(&sm->kv_ready[half]);
     }
+    // ---- pass B: latent K rows (TMEM) -> V rows (shared memory, SW128 K-major atoms)
+    if (lane == 0) good = wait(sm, &sm->vfree[half][q], (uint32_t)((k & 1) ^ 1), p.status);
+    good = __shfl_sync(0xffffffffu, good, 0);
+    if (!good) break;
+    __syncwarp();
+    tc_fence_after();
+#pragma unroll 1
+    for (int gi = 0; gi < 4; ++gi) {
+      const int grp = 4 * half + gi;
+      tmem_ld32(tmem_row + kTmemK + 32 * grp, r);
+      tmem_wait_ld();
+      uint8_t* vrow = vtile + grp * 16384 + row * 128;
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4*>(vrow + ((c ^ (row & 7)) << 4)) = make_uint4(r[4 * c], r[4 * c + 1], r[4 * c + 2], r[4 * c + 3]);
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm->v_ready[half]);
   }
 }
 
 // ------------------------------------------------------------------ MMA issue
+// Two issuing threads, one per half: issuer h computes the half-h part of QK (K columns of that
+// half, into its own S accumulator; the softmax adds the two) and the half-h part of PV (the two
+// M-blocks of output dims 256h..256h+255).
 template <int NH>
-__device__ void mma_loop(const DecodeParams& p, Smem* sm, uint8_t* vtile, uint8_t* qs, uint8_t* ps,
-                         int64_t t_begin, int64_t t_end, int which) {
-  constexpr uint32_t kIdQK = idesc_f16(128, NH, false, false, false);
-  constexpr uint32_t kIdPV = idesc_f16(128, NH, true, true, false);
-  constexpr uint32_t kPSw = (NH == 32) ? SW_64B : SW_32B;
-  constexpr uint32_t kPSbo = (NH == 32) ? 512 : 256;       // 8 token rows of P
-  const uint32_t tmem = sm->tmem_base;
-  const uint32_t s_col = tmem + kTmemS + which * NH;
-  const uint32_t o_col = tmem + kTmemS + 2 * NH;
-  const uint64_t qd = sdesc(smem_u32(qs), 16, 1024, SW_128B);
-  const uint64_t vd = sdesc(smem_u32(vtile), 16384, 1024, SW_128B);
-  const uint64_t pd = sdesc(smem_u32(ps), 4096, kPSbo, kPSw);
-  int64_t seg = 0;
-  for (int64_t g = t_begin; g < t_end; ++g) {
-    const int64_t k = g - t_begin;
-    const TileInfo ti = tile_info(p, g, t_begin, t_end);
-    if (ti.first && !wait(sm, &sm->q_full, (uint32_t)(seg & 1), p.status)) break;
-    if (!wait(sm, &sm->kv_ready, (uint32_t)(k & 1), p.status)) break;
+struct MmaIssuer {
+  static constexpr uint32_t kIdQK = idesc_f16(128, NH, false, false, false);
+  static constexpr uint32_t kIdPV = idesc_f16(128, NH, true, true, false);
+  static constexpr uint32_t kPSw = (NH == 32) ? SW_64B : SW_32B;
+  static constexpr uint32_t kPSbo = (NH == 32) ? 512 : 256;      // 8 token rows of P
+  static constexpr uint32_t kPBytes = 128 * NH * 2;
+  const DecodeParams& p;
+  Smem* sm;
+  int which;
+  uint32_t tmem, s_col, o_col;
+  uint64_t qd, vd, pd0;
+  int64_t t_begin, t_end;
+  int64_t ofree_waits = 0;
+
+  __device__ __forceinline__ MmaIssuer(const DecodeParams& p_, Smem* sm_, uint8_t* vtile, uint8_t* qs, uint8_t* ps, int64_t tb,
+                       int64_t te, int which_)
+      : p(p_), sm(sm_), which(which_), t_begin(tb), t_end(te) {
+    tmem = sm->tmem_base;
+    s_col = tmem + kTmemS + which * NH;
+    o_col = tmem + kTmemS + 2 * NH;
+    qd = sdesc(smem_u32(qs), 16, 1024, SW_128B);
+    vd = sdesc(smem_u32(vtile), 16384, 1024, SW_128B);
+    pd0 = sdesc(smem_u32(ps), 4096, kPSbo, kPSw);
+  }
+
+  // QK(k) of this half may be issued once the half is in TMEM and the softmax group has read S of
+  // tile k-1.
+  __device__ __forceinline__ bool qk_ready(int64_t k) {
+    return mbar_test(&sm->kv_ready[which], (uint32_t)(k & 1)) &&
+           (k == 0 || mbar_test(&sm->s_free, (uint32_t)((k - 1) & 1)));
+  }
+  __device__ __forceinline__ void qk_step(int ks, uint32_t acc) {
+    const uint64_t b = qd + (uint64_t)((((ks >> 2) * NH * 128) + (ks & 3) * 32) >> 4);
+    umma_ts(s_col, tmem + kTmemK + 8 * ks, b, kIdQK, acc);
+  }
+  __device__ __forceinline__ void qk(int64_t k) {
     tc_fence_after();
-    // S^T = K . Q^T ; issuer 0 takes k-steps 0..17, issuer 1 takes 18..35 (own accumulator each)
+    if (which == 0) {
 #pragma unroll
-    for (int x = 0; x < 18; ++x) {
-      const int ks = which * 18 + x;
-      const uint64_t b = qd + (uint64_t)((((ks >> 2) * NH * 128) + (ks & 3) * 32) >> 4);
-      umma_ts(s_col, tmem + kTmemK + 8 * ks, b, kIdQK, x > 0 ? 1u : 0u);
+      for (int x = 0; x < 16; ++x) qk_step(x, x > 0 ? 1u : 0u);          // latent dims 0..255
+    } else {
+#pragma unroll
+      for (int x = 0; x < 20; ++x) qk_step(16 + x, x > 0 ? 1u : 0u);     // latent 256..511, rope
     }
+    umma_commit(&sm->kfree[which]);
     umma_commit(&sm->s_full);
-    if (!wait(sm, &sm->p_full, (uint32_t)(k & 1), p.status)) break;
+  }
+
+  // PV(k) may be issued once P(k) and the V rows of tile k are in shared memory and, when tile k
+  // starts a new unit, the epilogue of the previous unit has read O.
+  __device__ __forceinline__ bool pv_ready(int64_t k, const TileInfo& ti) {
+    return mbar_test(&sm->p_full[k & 1], (uint32_t)((k >> 1) & 1)) && mbar_test(&sm->v_ready[which], (uint32_t)(k & 1)) &&
+           !(ti.first && k > 0 && !mbar_test(&sm->o_free, (uint32_t)(ofree_waits & 1)));
+  }
+  __device__ __forceinline__ void pv(int64_t k, const TileInfo& ti) {
+    if (ti.first && k > 0) ++ofree_waits;
     tc_fence_after();
-    // O^T += V^T . P^T ; issuer 0 takes M-blocks 0,1, issuer 1 takes 2,3. Row chunk w (tokens 32w..)
-    // is finished by both issuers before vfree[w] fires, so the next tile's rows can be written.
+    const uint64_t pd = pd0 + (uint64_t)(((k & 1) * kPBytes) >> 4);
+    // Row chunk w (tokens 32w..) of this half is released as soon as its UMMAs complete.
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
 #pragma unroll
@@ -349,11 +428,55 @@ __device__ void mma_loop(const DecodeParams& p, Smem* sm, uint8_t* vtile, uint8_
           umma_ss(o_col + mb * NH, a, bdesc, kIdPV, (ti.first && ks == 0) ? 0u : 1u);
         }
       }
-      umma_commit(&sm->vfree[w]);
+      umma_commit(&sm->vfree[which][w]);
     }
-    if (ti.last) {
-      umma_commit(&sm->o_done);
-      ++seg;
+    if (ti.last) umma_commit(&sm->o_done);
+  }
+};
+
+// Each issuer polls (without suspending) and issues whichever of QK(kq) and PV(kp) is ready, so PV
+// of one tile never waits behind QK of the next. QK runs at most one tile ahead of PV; that bound
+// also keeps every polled barrier within one phase of the parity being tested.
+template <int NH>
+__device__ void mma_loop(const DecodeParams& p, Smem* sm, uint8_t* vtile, uint8_t* qs, uint8_t* ps,
+                         int64_t t_begin, int64_t t_end, int which) {
+  MmaIssuer<NH> m(p, sm, vtile, qs, ps, t_begin, t_end, which);
+  const int64_t n = t_end - t_begin;
+  int64_t kq = 0, kp = 0, segs = 0;
+  uint64_t t_idle = 0;
+  uint32_t idle = 0;
+  while (kp < n) {
+    bool progressed = false;
+    if (kq < n && kq <= kp + 1) {
+      const TileInfo ti = tile_info(p, t_begin + kq, t_begin, t_end);
+      if ((!ti.first || mbar_test(&sm->q_full, (uint32_t)(segs & 1))) && m.qk_ready(kq)) {
+        if (ti.first) ++segs;
+        m.qk(kq);
+        ++kq;
+        progressed = true;
+      }
+    }
+    if (!progressed && kp < kq) {
+      const TileInfo ti = tile_info(p, t_begin + kp, t_begin, t_end);
+      if (m.pv_ready(kp, ti)) {
+        m.pv(kp, ti);
+        ++kp;
+        progressed = true;
+      }
+    }
+    if (progressed) {
+      idle = 0;
+      continue;
+    }
+    // bounded: give up (and flag a timeout) if nothing became ready for kWaitTimeoutNs
+    if ((++idle & 1023u) == 0) {
+      if (sm->abort) break;
+      const uint64_t t = globaltimer_ns();
+      if (t_idle == 0 || idle == 1024) t_idle = t;
+      else if (t - t_idle > kWaitTimeoutNs) {
+        fail(sm, p.status);
+        break;
+      }
     }
   }
   // drain: every UMMA of this thread has completed before TMEM is released
@@ -382,9 +505,34 @@ __device__ __forceinline__ float warp_transpose_reduce(float (&v)[32]) {
   return v[0];
 }
 
+// Scores of this thread's tile row: S = S_a + S_b (the two issuers' halves of the 576-wide
+// contraction), loaded one after the other into the same registers; unusable rows become -inf.
 template <int NH>
-__device__ void softmax_loop(const DecodeParams& p, Smem* sm, uint8_t* qs, uint8_t* ps, int64_t t_begin,
-                             int64_t t_end, int64_t cta) {
+__device__ __forceinline__ void load_scores(uint32_t taddr, bool valid, float qscale, float (&z)[32]) {
+  const float kNegInf = __int_as_float(0xff800000);
+  uint32_t ra[32];
+  __syncwarp();
+  if (NH == 32) tmem_ld32(taddr, ra);
+  else tmem_ld16(taddr, *reinterpret_cast<uint32_t(*)[16]>(ra));
+  tmem_wait_ld();
+#pragma unroll
+  for (int h = 0; h < 32; ++h) z[h] = h < NH ? __uint_as_float(ra[h]) : 0.f;
+  if (NH == 32) tmem_ld32(taddr + NH, ra);
+  else tmem_ld16(taddr + NH, *reinterpret_cast<uint32_t(*)[16]>(ra));
+  tmem_wait_ld();
+#pragma unroll
+  for (int h = 0; h < 32; ++h) z[h] = (h < NH && valid) ? (z[h] + __uint_as_float(ra[h])) * qscale : kNegInf;
+}
+
+// Softmax group: thread t owns tile row t (a token) and all heads. The running max per head is
+// kept lazily: it is only raised when a score exceeds it by more than kLazy = 15 (log2 units), so
+// most tiles need one group vote instead of a max reduction (and rarely an O rescale), while
+// P = 2^(z - max) stays <= 2^15, inside the fp16 range.
+constexpr float kLazy = 15.f;
+template <int NH>
+__device__ void softmax_loop(const DecodeParams& p, Smem* sm, uint8_t* ps, int64_t t_begin, int64_t t_end,
+                             int64_t cta) {
+  constexpr uint32_t kPBytes = 128 * NH * 2;
   const int t = threadIdx.x - 384;          // 0..127: tile row / TMEM lane
   const int w = t >> 5, lane = t & 31;
   const uint32_t tmem_lane = sm->tmem_base + ((uint32_t)(32 * w) << 16);
@@ -403,11 +551,12 @@ __device__ void softmax_loop(const DecodeParams& p, Smem* sm, uint8_t* qs, uint8
 #pragma unroll
       for (int h = 0; h < 32; ++h) l_part[h] = 0.f;
       if (t < 32) sm->m_used[t] = kNegInf;
-      named_sync_softmax();
     }
-    // ---- scores of this tile
-    if (wait(sm, &sm->kv_ready, (uint32_t)(k & 1), p.status)) wait(sm, &sm->s_full, (uint32_t)(k & 1), p.status);
-    named_sync_softmax();               // every thread sees the same abort flag after this
+    // ---- scores of this tile (one waiting thread per warp; the named barrier releases the group
+    // and makes the abort flag uniform)
+    if (lane == 0 && wait(sm, &sm->mask_full[k & 1], (uint32_t)((k >> 1) & 1), p.status))
+      wait(sm, &sm->s_full, (uint32_t)(k & 1), p.status);
+    named_sync_softmax();
     if (sm->abort) {
       ok = false;
       break;
@@ -415,100 +564,104 @@ __device__ void softmax_loop(const DecodeParams& p, Smem* sm, uint8_t* qs, uint8
     tc_fence_after();
     __syncwarp();
     float z[32];
-    {
-      uint32_t ra[32], rb[32];
-      if (NH == 32) {
-        tmem_ld32(tmem_lane + s_col, ra);
-        tmem_ld32(tmem_lane + s_col + NH, rb);
-      } else {
-        uint32_t (&ra16)[16] = *reinterpret_cast<uint32_t(*)[16]>(ra);
-        uint32_t (&rb16)[16] = *reinterpret_cast<uint32_t(*)[16]>(rb);
-        tmem_ld16(tmem_lane + s_col, ra16);
-        tmem_ld16(tmem_lane + s_col + NH, rb16);
-      }
-      tmem_wait_ld();
-      const bool valid = (sm->vmask[k & 1][w] >> lane) & 1u;
+    const bool valid = (sm->vmask[k & 1][w] >> lane) & 1u;
+    load_scores<NH>(tmem_lane + s_col, valid, qscale, z);
+    // ---- lazy running max: vote whether any score exceeds max + kLazy
+    bool exceed = false;
 #pragma unroll
-      for (int h = 0; h < 32; ++h)
-        z[h] = (h < NH && valid) ? (__uint_as_float(ra[h]) + __uint_as_float(rb[h])) * qscale : kNegInf;
+    for (int h = 0; h < 32; h += 4) {
+      const float4 mv = *reinterpret_cast<const float4*>(&sm->m_used[h]);
+      exceed |= (z[h] > mv.x + kLazy) | (z[h + 1] > mv.y + kLazy) | (z[h + 2] > mv.z + kLazy) | (z[h + 3] > mv.w + kLazy);
     }
-    // tile max per head
-    {
-      float v[32];
-#pragma unroll
-      for (int h = 0; h < 32; ++h) v[h] = z[h];
-      const float wm = warp_transpose_reduce<0>(v);   // lane l: max over this warp's rows of head l
-      sm->red[w][lane] = wm;
-    }
+    const int wv = __any_sync(0xffffffffu, exceed) ? 1 : 0;
+    if (lane == 0) sm->vote[w] = wv;
     named_sync_softmax();
-    if (w == 0) {
-      const float tmax = fmaxf(fmaxf(sm->red[0][lane], sm->red[1][lane]), fmaxf(sm->red[2][lane], sm->red[3][lane]));
-      const float mold = sm->m_used[lane];
-      float mnew = mold, alpha = 1.f;
-      if (tmax > mold + 8.f) {             // lazy rescale: keep the stale max unless it grows by 2^8
-        mnew = tmax;
-        alpha = (mold == kNegInf) ? 0.f : ex2_approx(mold - mnew);
+    const bool raise = (sm->vote[0] | sm->vote[1] | sm->vote[2] | sm->vote[3]) != 0;
+    if (raise) {
+      {
+        const float wm = warp_transpose_reduce<0>(z);   // lane l: max over this warp's rows of head l (z is
+        sm->red[w][lane] = wm;                          // consumed here and reloaded below)
       }
-      sm->m_used[lane] = mnew;
-      sm->alpha[lane] = alpha;
-      const bool any = __any_sync(0xffffffffu, lane < NH && alpha != 1.f && mold != kNegInf);
-      if (lane == 0) sm->need_rescale = any ? 1 : 0;
+      named_sync_softmax();
+      if (w == 0) {
+        const float tmax = fmaxf(fmaxf(sm->red[0][lane], sm->red[1][lane]), fmaxf(sm->red[2][lane], sm->red[3][lane]));
+        const float mold = sm->m_used[lane];
+        float mnew = mold, alpha = 1.f;
+        if (tmax > mold + kLazy) {
+          mnew = tmax;
+          alpha = (mold == kNegInf) ? 0.f : ex2_approx(mold - mnew);
+        }
+        sm->m_used[lane] = mnew;
+        sm->alpha[lane] = alpha;
+        const bool any = __any_sync(0xffffffffu, lane < NH && alpha != 1.f && mold != kNegInf);
+        if (lane == 0) sm->need_rescale = any ? 1 : 0;
+      }
+      named_sync_softmax();
+#pragma unroll
+      for (int h = 0; h < 32; h += 4) {
+        const float4 av = *reinterpret_cast<const float4*>(&sm->alpha[h]);
+        l_part[h] *= av.x; l_part[h + 1] *= av.y; l_part[h + 2] *= av.z; l_part[h + 3] *= av.w;
+      }
+      if (sm->need_rescale && !ti.first) {
+        // O^T[dim, h] *= alpha[h], after PV of the previous tile has finished accumulating into O
+        if (lane == 0 && wait(sm, &sm->vfree[0][3], (uint32_t)((k - 1) & 1), p.status))
+          wait(sm, &sm->vfree[1][3], (uint32_t)((k - 1) & 1), p.status);
+        __syncwarp();
+        tc_fence_after();
+#pragma unroll 1
+        for (int mb = 0; mb < 4; ++mb) {
+          uint32_t r[32];
+          if (NH == 32) {
+            tmem_ld32(tmem_lane + o_col + mb * NH, r);
+          } else {
+            tmem_ld16(tmem_lane + o_col + mb * NH, *reinterpret_cast<uint32_t(*)[16]>(r));
+          }
+          tmem_wait_ld();
+#pragma unroll
+          for (int h = 0; h < NH; ++h) r[h] = __float_as_uint(__uint_as_float(r[h]) * sm->alpha[h]);
+          if (NH == 32) tmem_st32(tmem_lane + o_col + mb * NH, r);
+          else tmem_st16(tmem_lane + o_col + mb * NH, *reinterpret_cast<uint32_t(*)[16]>(r));
+        }
+        tmem_wait_st();
+      }
+      load_scores<NH>(tmem_lane + s_col, valid, qscale, z);
     }
-    named_sync_softmax();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm->s_free);      // S read: the next QK and K tile may proceed
+    // ---- P = 2^(z - m) in fp16, row t of this tile's P buffer (MN-major: heads contiguous)
     uint32_t pk[16];
 #pragma unroll
     for (int h = 0; h < 32; h += 4) {
       const float4 mv = *reinterpret_cast<const float4*>(&sm->m_used[h]);
-      const float4 av = *reinterpret_cast<const float4*>(&sm->alpha[h]);
       const float mm[4] = {mv.x, mv.y, mv.z, mv.w};
-      const float aa[4] = {av.x, av.y, av.z, av.w};
       float pp[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         pp[i] = (mm[i] == kNegInf) ? 0.f : ex2_approx(z[h + i] - mm[i]);
-        l_part[h + i] = l_part[h + i] * aa[i] + pp[i];
+        l_part[h + i] += pp[i];
       }
       const __half2 h01 = __floats2half2_rn(pp[0], pp[1]);
       const __half2 h23 = __floats2half2_rn(pp[2], pp[3]);
       pk[h >> 1] = *reinterpret_cast<const uint32_t*>(&h01);
       pk[(h >> 1) + 1] = *reinterpret_cast<const uint32_t*>(&h23);
     }
-    // P row t, MN-major (heads contiguous): SW64 for 32 heads, SW32 for 16
+    uint8_t* pbuf = ps + (k & 1) * kPBytes;
     if (NH == 32) {
 #pragma unroll
       for (int c = 0; c < 4; ++c)
-        *reinterpret_cast<uint4*>(ps + t * 64 + ((c ^ ((t >> 1) & 3)) << 4)) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        *reinterpret_cast<uint4*>(pbuf + t * 64 + ((c ^ ((t >> 1) & 3)) << 4)) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
     } else {
 #pragma unroll
       for (int c = 0; c < 2; ++c)
-        *reinterpret_cast<uint4*>(ps + t * 32 + ((c ^ ((t >> 2) & 1)) << 4)) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-    }
-    __syncwarp();
-    if (sm->need_rescale && !ti.first) {
-      // O^T[dim, h] *= alpha[h]; all PV of earlier tiles are complete (they precede this tile's QK)
-#pragma unroll 1
-      for (int mb = 0; mb < 4; ++mb) {
-        uint32_t r[32];
-        if (NH == 32) {
-          tmem_ld32(tmem_lane + o_col + mb * NH, r);
-        } else {
-          tmem_ld16(tmem_lane + o_col + mb * NH, *reinterpret_cast<uint32_t(*)[16]>(r));
-        }
-        tmem_wait_ld();
-#pragma unroll
-        for (int h = 0; h < NH; ++h) r[h] = __float_as_uint(__uint_as_float(r[h]) * sm->alpha[h]);
-        if (NH == 32) tmem_st32(tmem_lane + o_col + mb * NH, r);
-        else tmem_st16(tmem_lane + o_col + mb * NH, *reinterpret_cast<uint32_t(*)[16]>(r));
-      }
-      tmem_wait_st();
+        *reinterpret_cast<uint4*>(pbuf + t * 32 + ((c ^ ((t >> 2) & 1)) << 4)) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
     }
     fence_proxy_async_smem();
-    tc_fence_before();
-    mbar_arrive(&sm->p_full);
+    mbar_arrive(&sm->p_full[k & 1]);
 
     if (ti.last) {
       // ---- epilogue: write this segment's unnormalised partial
-      wait(sm, &sm->o_done, (uint32_t)(seg & 1), p.status);
+      if (lane == 0) wait(sm, &sm->o_done, (uint32_t)(seg & 1), p.status);
       named_sync_softmax();
       if (sm->abort) {
         ok = false;
@@ -545,6 +698,7 @@ __device__ void softmax_loop(const DecodeParams& p, Smem* sm, uint8_t* qs, uint8
         for (int h = 0; h < NH; ++h) po[(int64_t)h * kLatent + dim] = __uint_as_float(r[h]);
       }
       tc_fence_before();
+      mbar_arrive(&sm->o_free);
       named_sync_softmax();
       ++seg;
     }
@@ -552,13 +706,13 @@ __device__ void softmax_loop(const DecodeParams& p, Smem* sm, uint8_t* qs, uint8
 }
 
 template <int NH>
-__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ DecodeParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* vtile = base;                                   // 131072
   uint8_t* qs = vtile + kVBytes;                           // 9 * NH * 128
-  uint8_t* ps = qs + 9 * NH * 128;                         // 128 * NH * 2
-  uint8_t* ring = ps + 128 * NH * 2;                       // 4 * 32 * 368
+  uint8_t* ps = qs + 9 * NH * 128;                         // 2 x 128 * NH * 2 (P, double-buffered)
+  uint8_t* ring = ps + 2 * 128 * NH * 2;                   // 4 * 32 * 352
   static_assert((kRingStages * kRingStageBytes) % 16 == 0, "control block must stay 16-byte aligned");
   Smem* sm = reinterpret_cast<Smem*>(ring + kRingStages * kRingStageBytes);
 
@@ -575,11 +729,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
       mbar_init(&sm->ring_full[i], 1);
       mbar_init(&sm->ring_empty[i], 2);
     }
-    for (int i = 0; i < 4; ++i) mbar_init(&sm->vfree[i], 2);
-    mbar_init(&sm->kv_ready, 8);
+    for (int h = 0; h < 2; ++h) {
+      for (int i = 0; i < 4; ++i) mbar_init(&sm->vfree[h][i], 1);
+      mbar_init(&sm->kv_ready[h], 4);
+      mbar_init(&sm->kfree[h], 1);
+      mbar_init(&sm->v_ready[h], 4);
+      mbar_init(&sm->mask_full[h], 4);
+    }
     mbar_init(&sm->s_full, 2);
-    mbar_init(&sm->p_full, 128);
+    mbar_init(&sm->s_free, 4);
+    mbar_init(&sm->p_full[0], 128);
+    mbar_init(&sm->p_full[1], 128);
     mbar_init(&sm->o_done, 2);
+    mbar_init(&sm->o_free, 128);
     mbar_init(&sm->q_full, 1);
     mbar_init(&sm->drain, 2);
     sm->abort = 0;
@@ -593,15 +755,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
   __syncthreads();
   tc_fence_after();
 
-  if (warp == 0) {
-    producer_loop(p, sm, ring, qs, t_begin, t_end);
+  if (warp == 0 || warp == 3) {
+    producer_loop(p, sm, ring, qs, t_begin, t_end, warp == 0 ? 0 : 1);
   } else if (warp == 1 || warp == 2) {
     if ((threadIdx.x & 31) == 0) mma_loop<NH>(p, sm, vtile, qs, ps, t_begin, t_end, warp - 1);
     __syncwarp();
   } else if (warp >= 4 && warp < 12) {
     dequant_loop(p, sm, ring, vtile, t_begin, t_end, warp);
   } else if (warp >= 12) {
-    softmax_loop<NH>(p, sm, qs, ps, t_begin, t_end, cta);
+    softmax_loop<NH>(p, sm, ps, t_begin, t_end, cta);
   }
   tc_fence_before();
   __syncthreads();
@@ -625,14 +787,22 @@ __global__ void __launch_bounds__(256) q_prep_kernel(const DecodeParams p) {
   split_unit(p, unit, b, j, hg);
   const uint16_t* src = p.q + (((int64_t)b * p.Q + j) * p.H + (int64_t)hg * NH) * kQK;
   uint8_t* dst = p.q16 + unit * (int64_t)(9 * NH * 128);
-  constexpr int kChunks = NH * (kQK / 8);
-  float mx = 0.f;
-  for (int c = threadIdx.x; c < kChunks; c += 256) {
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(src) + c);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  constexpr int kChunks = NH * (kQK / 8);           // 16-byte chunks of the unit's q block
+  constexpr int kPer = (kChunks + 255) / 256;
+  // every load is issued before any is used: one memory round trip, values kept in registers
+  uint4 v[kPer];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-      mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(w[i] << 16)), fabsf(__uint_as_float(w[i] & 0xFFFF0000u))));
+  for (int i = 0; i < kPer; ++i) {
+    const int c = threadIdx.x + 256 * i;
+    v[i] = c < kChunks ? __ldg(reinterpret_cast<const uint4*>(src) + c) : make_uint4(0u, 0u, 0u, 0u);
+  }
+  float mx = 0.f;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+    for (int t = 0; t < 4; ++t)
+      mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(w[t] << 16)), fabsf(__uint_as_float(w[t] & 0xFFFF0000u))));
   }
 #pragma unroll
   for (int s = 16; s >= 1; s >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, s));
@@ -648,14 +818,16 @@ __global__ void __launch_bounds__(256) q_prep_kernel(const DecodeParams p) {
     e = 15 - E;
   }
   const float up = ldexpf(1.f, e);
-  for (int c = threadIdx.x; c < kChunks; c += 256) {
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(src) + c);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int c = threadIdx.x + 256 * i;
+    if (c >= kChunks) break;
+    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
     uint32_t o[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const __half2 h = __floats2half2_rn(__uint_as_float(w[i] << 16) * up, __uint_as_float(w[i] & 0xFFFF0000u) * up);
-      o[i] = *reinterpret_cast<const uint32_t*>(&h);
+    for (int t = 0; t < 4; ++t) {
+      const __half2 h = __floats2half2_rn(__uint_as_float(w[t] << 16) * up, __uint_as_float(w[t] & 0xFFFF0000u) * up);
+      o[t] = *reinterpret_cast<const uint32_t*>(&h);
     }
     const int h = c / (kQK / 8), cc = c % (kQK / 8);
     const int atom = cc >> 3, ch = cc & 7;
@@ -711,7 +883,7 @@ __global__ void __launch_bounds__(512) merge_kernel(const DecodeParams p) {
 
 template <int NH>
 constexpr size_t decode_smem_bytes() {
-  return 1024 + kVBytes + 9 * NH * 128 + 128 * NH * 2 + kRingStages * kRingStageBytes + sizeof(Smem);
+  return 1024 + kVBytes + 9 * NH * 128 + 2 * 128 * NH * 2 + kRingStages * kRingStageBytes + sizeof(Smem);
 }
 
 }  // namespace

@@ -2,6 +2,7 @@
 #pragma once
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace nvfp4mla {
@@ -32,6 +33,7 @@ DecodeSchedule make_schedule(int B, int Q, int H, int topk, int num_sms, int max
 size_t workspace_bytes_for(const DecodeSchedule& s, int H);
 
 struct DecodeParams {
+  CUtensorMap cache_map;      // 2-D view of the cache: [num_pages*64 rows, 88 x uint32], one-row box
   const uint16_t* q;          // bf16 [B, Q, H, 576]
   const uint8_t* cache;       // [num_pages, 64, 352]
   int64_t num_pages;

@@ -143,7 +143,9 @@ size_t sparse_mla_decode_workspace_size(int B, int Q, int H, int topk, int num_s
   if (!sizes_ok(B, Q, H, topk)) return 0;
   if (num_sms <= 0) num_sms = device_sm_count();
   if (num_sms <= 0) return 0;
-  return workspace_bytes_for(make_schedule(B, Q, H, topk, num_sms, 0), H);
+  const DecodeSchedule s = make_schedule(B, Q, H, topk, num_sms, 0);
+  if (s.total_tiles > (int64_t)INT32_MAX) return 0;
+  return workspace_bytes_for(s, H);
 }
 
 int sparse_mla_decode(const void* q, const void* kv_cache, int64_t num_pages, const int32_t* page_table,
@@ -168,6 +170,7 @@ int sparse_mla_decode(const void* q, const void* kv_cache, int64_t num_pages, co
   if (workspace == nullptr || workspace_bytes < need) return NVFP4MLA_ERR_WORKSPACE;
   if (!aligned(workspace, 256)) return NVFP4MLA_ERR_ALIGNMENT;
   if (num_pages * kPageTokens > (int64_t)INT32_MAX) return NVFP4MLA_ERR_UNSUPPORTED;   // int32 row coordinates
+  if (s.total_tiles > (int64_t)INT32_MAX) return NVFP4MLA_ERR_UNSUPPORTED;               // int32 tile numbers
 
   DecodeParams p{};
   if (!encode_cache_map(&p.cache_map, kv_cache, num_pages)) return NVFP4MLA_ERR_CUDA;

@@ -55,7 +55,8 @@ struct alignas(16) Smem {
   alignas(16) float m_used[32];      // running max per head (log2 units); read as float4
   alignas(16) float alpha[32];       // rescale factor of this tile per head; read as float4
   uint64_t ring_full[kRingStages];   // gathered rows of a 32-row stage have landed
-  uint64_t ring_empty[kRingStages];  // ... and have been converted (both dequant warps of the stage)
+  uint64_t rows_full;                // row numbers + masks of a tile resolved (2 producer warps)
+  uint64_t rows_empty;               // every stage of that tile has been requested (4 issuing warps)
   // Half h of a tile = latent dims 256h..256h+255 (half 1 also carries the rope dims). Each half has
   // its own dequant warps and MMA issuer, so the two halves pipeline independently and only meet
   // in the softmax.
@@ -69,11 +70,13 @@ struct alignas(16) Smem {
   uint64_t p_full[2];                // P of a tile written (128 threads), double-buffered by tile parity
   uint64_t o_done;                   // last PV of a unit segment complete (2 issuers)
   uint64_t o_free;                   // epilogue has read O (128 threads)
-  uint64_t q_full;                   // q image of the unit copied in
+  uint64_t q_full[2];                // half h of the unit's q image copied in (issuer h's copy)
   uint64_t drain;                    // every UMMA of both issuers complete
   uint32_t tmem_base;
   volatile int abort;
-  uint32_t maskbuf[kRingStages];     // producer -> dequant: usable rows of each ring stage
+  alignas(16) int32_t rowbuf[kTileTokens];  // producer -> dequant: cache row of every tile entry (-1: unusable)
+  uint32_t maskbuf[2][kRingStages];  // producer -> dequant: usable rows of each 32-row stage, by tile parity
+  uint32_t stage_cnt[kRingStages];   // dequant warps done with a ring stage (2 per tile)
   uint32_t vmask[2][4];              // dequant -> softmax: usable rows of the tile, by tile parity
   float red[4][32];                  // softmax group: per-warp partial reductions
   int vote[4];                       // softmax group: does a warp see a score above max + kLazy
@@ -86,10 +89,12 @@ struct TileInfo {
   bool first, last; // first/last tile of this CTA's segment of the unit
 };
 
+// Tile numbers fit in 32 bits (the host rejects larger problems), so unsigned 32-bit division is used.
 __device__ __forceinline__ TileInfo tile_info(const DecodeParams& p, int64_t g, int64_t t_begin, int64_t t_end) {
   TileInfo ti;
-  ti.unit = g / p.tiles_per_unit;
-  ti.local = (int)(g - ti.unit * p.tiles_per_unit);
+  const uint32_t u = (uint32_t)g / (uint32_t)p.tiles_per_unit;
+  ti.unit = u;
+  ti.local = (int)((uint32_t)g - u * (uint32_t)p.tiles_per_unit);
   ti.first = (g == t_begin) || (ti.local == 0);
   ti.last = (g == t_end - 1) || (ti.local == p.tiles_per_unit - 1);
   return ti;
@@ -168,13 +173,9 @@ __device__ __forceinline__ void gather4(void* dst, const CUtensorMap* map, int r
       : "memory");
 }
 
-__device__ void producer_loop(const DecodeParams& p, Smem* sm, uint8_t* ring, uint8_t* qs, int64_t t_begin,
-                              int64_t t_end, int pw) {
+__device__ void producer_loop(const DecodeParams& p, Smem* sm, int64_t t_begin, int64_t t_end, int pw) {
   const int lane = threadIdx.x & 31;
   const int q0 = 2 * pw;
-  const uint32_t qbytes = 9u * (uint32_t)p.heads_per_cta * 128u;
-  uint32_t issued[2] = {0, 0};
-  uint32_t q_issued = 0;
   TileIdx A0, A1, A2;
   int pg0[2], pg1[2];
   if (t_begin < t_end) load_tile_idx(p, t_begin, lane, q0, A0);
@@ -182,11 +183,17 @@ __device__ void producer_loop(const DecodeParams& p, Smem* sm, uint8_t* ring, ui
   if (t_begin < t_end) load_tile_pages(p, A0, pg0);
   for (int64_t g = t_begin; g < t_end && !sm->abort; ++g) {
     const int64_t k = g - t_begin;
+    const int b = (int)(k & 1);
     const TileInfo ti = tile_info(p, g, t_begin, t_end);
     if (g + 1 < t_end) load_tile_pages(p, A1, pg1);
     if (g + 2 < t_end) load_tile_idx(p, g + 2, lane, q0, A2);
     const int hg = (int)(ti.unit % p.head_groups);
+    // The row table is free once every stage of tile k-1 has been requested; by then tile k-2's
+    // masks (the other parity) have been read too.
     bool good = true;
+    if (lane == 0 && k >= 1) good = wait(sm, &sm->rows_empty, (uint32_t)((k - 1) & 1), p.status);
+    good = __shfl_sync(0xffffffffu, good, 0);
+    if (!good) break;
 #pragma unroll
     for (int qq = 0; qq < 2; ++qq) {
       const int q = q0 + qq;
@@ -202,59 +209,48 @@ __device__ void producer_loop(const DecodeParams& p, Smem* sm, uint8_t* ring, ui
         if (lane == 0 && nbp) atomicAdd(p.status + 1, (int)nbp);
       }
       const uint32_t mask = __ballot_sync(0xffffffffu, ok);
-      const int row = ok ? page * kPageTokens + (idx & 63) : -1;
-      if (lane == 0) good = wait(sm, &sm->ring_empty[q], (uint32_t)((k & 1) ^ 1), p.status);
-      good = __shfl_sync(0xffffffffu, good, 0);
-      if (!good) break;
-      if (lane == 0) {
-        sm->maskbuf[q] = mask;
-        mbar_arrive_expect_tx(&sm->ring_full[q], (uint32_t)kRingStageBytes);
-      }
-      __syncwarp();
-      const int r0 = __shfl_sync(0xffffffffu, row, (4 * lane + 0) & 31);
-      const int r1 = __shfl_sync(0xffffffffu, row, (4 * lane + 1) & 31);
-      const int r2 = __shfl_sync(0xffffffffu, row, (4 * lane + 2) & 31);
-      const int r3 = __shfl_sync(0xffffffffu, row, (4 * lane + 3) & 31);
-      if (lane < 8) gather4(ring + q * kRingStageBytes + lane * 4 * kRowBytes, &p.cache_map, r0, r1, r2, r3, &sm->ring_full[q]);
-      issued[qq] = (uint32_t)(k + 1);
+      sm->rowbuf[q * 32 + lane] = ok ? page * kPageTokens + (idx & 63) : -1;
+      if (lane == 0) sm->maskbuf[b][q] = mask;
     }
-    if (!good || sm->abort) break;
-    if (pw == 0 && ti.first) {
-      // The unit changes: copy its pre-converted q image once the previous tile's QK is done with the buffer.
-      if (lane == 0) {
-        // q16 comes from the prep grid: only this copy has to wait for it, the row gathers do not.
-        if (q_issued == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
-        good = (k == 0) || wait(sm, &sm->s_full, (uint32_t)(((k - 1) & 1)), p.status);
-        if (good) {
-          mbar_arrive_expect_tx(&sm->q_full, qbytes);
-          bulk_g2s(qs, p.q16 + ti.unit * (int64_t)qbytes, qbytes, &sm->q_full);
-          ++q_issued;
-        }
-      }
-      good = __shfl_sync(0xffffffffu, good, 0);
-      if (!good) break;
-    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm->rows_full);
     A0 = A1;
     A1 = A2;
     pg0[0] = pg1[0];
     pg0[1] = pg1[1];
   }
-  // Never leave with bulk copies in flight: wait (bounded) for the last phase issued on each barrier.
+}
+
+// Refill ring stage q with the 32 rows of tile k (8 gather4 copies, lanes 0..7), once the producer
+// has resolved them. Returns false on timeout/abort.
+__device__ __forceinline__ bool issue_stage(const DecodeParams& p, Smem* sm, uint8_t* ring, int64_t k, int q, int lane) {
+  bool good = true;
   if (lane == 0) {
-    for (int qq = 0; qq < 2; ++qq)
-      if (issued[qq] > 0) mbar_wait(&sm->ring_full[q0 + qq], (issued[qq] - 1) & 1, nullptr, kWaitTimeoutNs);
-    if (q_issued > 0) mbar_wait(&sm->q_full, (q_issued - 1) & 1, nullptr, kWaitTimeoutNs);
+    good = wait(sm, &sm->rows_full, (uint32_t)(k & 1), p.status);
+    if (good) mbar_arrive_expect_tx(&sm->ring_full[q], (uint32_t)kRingStageBytes);
   }
-  __syncwarp();
+  good = __shfl_sync(0xffffffffu, good, 0);
+  if (!good) return false;
+  if (lane < 8) {
+    const int4 r = *reinterpret_cast<const int4*>(&sm->rowbuf[q * 32 + 4 * lane]);
+    gather4(ring + q * kRingStageBytes + lane * 4 * kRowBytes, &p.cache_map, r.x, r.y, r.z, r.w, &sm->ring_full[q]);
+  }
+  __syncwarp();   // every lane has read its row numbers before the table is released
+  if (lane == 0) mbar_arrive(&sm->rows_empty);
+  return true;
 }
 
 // ------------------------------------------------------------------ dequant
 // Thread = one tile row (token). half 0: latent dims 0..255; half 1: dims 256..511 + rope.
-// One group = 64 values (32 nibble bytes) sharing four block scales.
-__device__ __forceinline__ void convert_group(const uint8_t* rowp, int g, uint32_t (&r)[32]) {
-  const uint4 n0 = *reinterpret_cast<const uint4*>(rowp + 32 * g);
-  const uint4 n1 = *reinterpret_cast<const uint4*>(rowp + 32 * g + 16);
-  const uint32_t sw = *reinterpret_cast<const uint32_t*>(rowp + kScaleOff + 4 * g);
+// One group = 64 values (32 nibble bytes) sharing four block scales (sw).
+// Ring rows are 352 B apart, so lanes l and l+4 of a 16-byte load phase hit the same banks;
+// lanes with bit 2 set (odd) read the group's two 16-byte chunks in the opposite order, which
+// makes both loads conflict-free.
+__device__ __forceinline__ void convert_group(const uint8_t* rowp, int g, uint32_t sw, bool odd, uint32_t (&r)[32]) {
+  const uint4 x0 = *reinterpret_cast<const uint4*>(rowp + 32 * g + (odd ? 16 : 0));
+  const uint4 x1 = *reinterpret_cast<const uint4*>(rowp + 32 * g + (odd ? 0 : 16));
+  const uint4 n0 = odd ? x1 : x0;
+  const uint4 n1 = odd ? x0 : x1;
   const uint32_t w[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
 #pragma unroll
   for (int bb = 0; bb < 4; ++bb) {
@@ -272,7 +268,7 @@ __device__ __forceinline__ void convert_group(const uint8_t* rowp, int g, uint32
 // releases the ring stage. Pass B copies the latent part of those K rows from TMEM into the
 // V tile in shared memory (the A operand of PV, read MN-major) once PV of the previous tile is done
 // with those V rows, so the compressed rows are converted only once and leave the ring early.
-__device__ void dequant_loop(const DecodeParams& p, Smem* sm, const uint8_t* ring, uint8_t* vtile,
+__device__ void dequant_loop(const DecodeParams& p, Smem* sm, uint8_t* ring, uint8_t* vtile,
                              int64_t t_begin, int64_t t_end, int warp) {
   const int lane = threadIdx.x & 31;
   const int q = warp & 3;               // TMEM lane quarter == ring stage == tile rows 32q..32q+31
@@ -280,7 +276,17 @@ __device__ void dequant_loop(const DecodeParams& p, Smem* sm, const uint8_t* rin
   const int row = 32 * q + lane;
   const uint32_t tmem_row = sm->tmem_base + ((uint32_t)(32 * q) << 16);
   const uint8_t* rowp = ring + q * kRingStageBytes + lane * kRingRowStride;
-  for (int64_t g = t_begin; g < t_end; ++g) {
+  const bool odd = (lane >> 2) & 1;
+  int64_t n = t_end - t_begin;
+  int64_t issued = 0;   // tiles whose rows this warp has requested for stage q
+  // The ring is refilled by the dequant warps themselves: the second of the two warps that read a
+  // stage issues the stage's gathers for the next tile as soon as both are done with it. The lo
+  // warp of each quarter issues tile 0.
+  if (half == 0 && n > 0) {
+    if (!issue_stage(p, sm, ring, 0, q, lane)) n = 0;
+    else issued = 1;
+  }
+  for (int64_t g = t_begin; g < t_begin + n; ++g) {
     const int64_t k = g - t_begin;
     // ---- pass A: compressed rows -> fp16 K rows in TMEM
     bool good = true;
@@ -293,21 +299,31 @@ __device__ void dequant_loop(const DecodeParams& p, Smem* sm, const uint8_t* rin
     if (!good) break;
     __syncwarp();
     tc_fence_after();
-    const uint32_t mask = sm->maskbuf[q];
+    const uint32_t mask = sm->maskbuf[k & 1][q];
     uint32_t r[32];
+    // the 16 block scales of this half: one 16-byte load instead of four word loads
+    const uint4 sc = *reinterpret_cast<const uint4*>(rowp + kScaleOff + 16 * half);
     // Rows of unusable entries arrive zero-filled (scale bytes 0), so they dequantise to zeros.
 #pragma unroll 1
     for (int gi = 0; gi < 4; ++gi) {
       const int grp = 4 * half + gi;
-      convert_group(rowp, grp, r);
+      const uint32_t sw = gi == 0 ? sc.x : gi == 1 ? sc.y : gi == 2 ? sc.z : sc.w;
+      convert_group(rowp, grp, sw, odd, r);
       __syncwarp();
       tmem_st32(tmem_row + kTmemK + 32 * grp, r);
     }
     if (half == 1) {
+      uint4 rv[4];
+#pragma unroll
+      for (int c = 0; c < 4; c += 2) {   // chunk pairs in lane-dependent order (conflict-free)
+        const uint4 x0 = *reinterpret_cast<const uint4*>(rowp + kRopeOff + 16 * c + (odd ? 16 : 0));
+        const uint4 x1 = *reinterpret_cast<const uint4*>(rowp + kRopeOff + 16 * c + (odd ? 0 : 16));
+        rv[c] = odd ? x1 : x0;
+        rv[c + 1] = odd ? x0 : x1;
+      }
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        const uint4 v = *reinterpret_cast<const uint4*>(rowp + kRopeOff + 16 * c);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        const uint32_t w[4] = {rv[c].x, rv[c].y, rv[c].z, rv[c].w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           r[8 * c + 2 * i] = e4m3x2_to_f16x2(w[i] & 0xFFFFu);
@@ -325,8 +341,17 @@ __device__ void dequant_loop(const DecodeParams& p, Smem* sm, const uint8_t* rin
         sm->vmask[k & 1][q] = mask;
         mbar_arrive(&sm->mask_full[k & 1]);
       }
-      mbar_arrive(&sm->ring_empty[q]);
       mbar_arrive(&sm->kv_ready[half]);
+    }
+    // ---- refill: the second warp done with stage q requests tile k+1's rows into it
+    {
+      uint32_t old = 0;
+      if (lane == 0) asm volatile("atom.add.acq_rel.cta.shared::cta.u32 %0, [%1], 1;" : "=r"(old) : "r"(smem_u32(&sm->stage_cnt[q])) : "memory");
+      old = __shfl_sync(0xffffffffu, old, 0);
+      if ((old & 1u) && k + 1 < n) {
+        if (!issue_stage(p, sm, ring, k + 1, q, lane)) break;
+        issued = k + 2;
+      }
     }
     // ---- pass B: latent K rows (TMEM) -> V rows (shared memory, SW128 K-major atoms)
     if (lane == 0) good = wait(sm, &sm->vfree[half][q], (uint32_t)((k & 1) ^ 1), p.status);
@@ -349,6 +374,9 @@ __device__ void dequant_loop(const DecodeParams& p, Smem* sm, const uint8_t* rin
     __syncwarp();
     if (lane == 0) mbar_arrive(&sm->v_ready[half]);
   }
+  // After an abort, never leave with gathers in flight: wait (bounded) for the last refill issued.
+  if (lane == 0 && issued > 0 && sm->abort) mbar_wait(&sm->ring_full[q], (uint32_t)((issued - 1) & 1), nullptr, kWaitTimeoutNs);
+  __syncwarp();
 }
 
 // ------------------------------------------------------------------ MMA issue
@@ -369,6 +397,17 @@ struct MmaIssuer {
   uint64_t qd, vd, pd0;
   int64_t t_begin, t_end;
   int64_t ofree_waits = 0;
+  uint8_t* q_smem;
+
+  // Copy this half's part of the unit's pre-converted q image (atoms 0..3 for half 0, 4..8 for
+  // half 1: exactly the K-steps this issuer's QK reads) into the shared q buffer.
+  __device__ __forceinline__ void request_q(int64_t unit) {
+    const uint32_t atom_bytes = (uint32_t)NH * 128u;
+    const uint32_t off = which == 0 ? 0u : 4u * atom_bytes;
+    const uint32_t bytes = (which == 0 ? 4u : 5u) * atom_bytes;
+    mbar_arrive_expect_tx(&sm->q_full[which], bytes);
+    bulk_g2s(q_smem + off, p.q16 + unit * (int64_t)(9u * atom_bytes) + off, bytes, &sm->q_full[which]);
+  }
 
   __device__ __forceinline__ MmaIssuer(const DecodeParams& p_, Smem* sm_, uint8_t* vtile, uint8_t* qs, uint8_t* ps, int64_t tb,
                        int64_t te, int which_)
@@ -377,6 +416,7 @@ struct MmaIssuer {
     s_col = tmem + kTmemS + which * NH;
     o_col = tmem + kTmemS + 2 * NH;
     qd = sdesc(smem_u32(qs), 16, 1024, SW_128B);
+    q_smem = qs;
     vd = sdesc(smem_u32(vtile), 16384, 1024, SW_128B);
     pd0 = sdesc(smem_u32(ps), 4096, kPSbo, kPSw);
   }
@@ -442,43 +482,51 @@ __device__ void mma_loop(const DecodeParams& p, Smem* sm, uint8_t* vtile, uint8_
                          int64_t t_begin, int64_t t_end, int which) {
   MmaIssuer<NH> m(p, sm, vtile, qs, ps, t_begin, t_end, which);
   const int64_t n = t_end - t_begin;
-  int64_t kq = 0, kp = 0, segs = 0;
+  int64_t kq = 0, kp = 0, q_copies = 0;
+  bool q_pending = false;
+  TileInfo tq = tile_info(p, t_begin, t_begin, t_end), tp = tq;
   uint64_t t_idle = 0;
   uint32_t idle = 0;
   while (kp < n) {
-    bool progressed = false;
-    if (kq < n && kq <= kp + 1) {
-      const TileInfo ti = tile_info(p, t_begin + kq, t_begin, t_end);
-      if ((!ti.first || mbar_test(&sm->q_full, (uint32_t)(segs & 1))) && m.qk_ready(kq)) {
-        if (ti.first) ++segs;
-        m.qk(kq);
-        ++kq;
-        progressed = true;
-      }
+    // A new unit's q overwrites the q buffer once this half's QK of the previous tile is complete
+    // (this thread issued that QK last, so its kfree phase is the newest one possible).
+    if (kq < n && kq <= kp + 1 && tq.first && !q_pending &&
+        (kq == 0 || mbar_test(&sm->kfree[which], (uint32_t)((kq - 1) & 1)))) {
+      if (q_copies == 0) asm volatile("griddepcontrol.wait;" ::: "memory");   // q16 comes from the prep grid
+      m.request_q(tq.unit);
+      ++q_copies;
+      q_pending = true;
     }
-    if (!progressed && kp < kq) {
-      const TileInfo ti = tile_info(p, t_begin + kp, t_begin, t_end);
-      if (m.pv_ready(kp, ti)) {
-        m.pv(kp, ti);
-        ++kp;
-        progressed = true;
-      }
-    }
-    if (progressed) {
+    if (kq < n && kq <= kp + 1 &&
+        (!tq.first || (q_pending && mbar_test(&sm->q_full[which], (uint32_t)((q_copies - 1) & 1)))) &&
+        m.qk_ready(kq)) {
+      if (tq.first) q_pending = false;
+      m.qk(kq);
+      if (++kq < n) tq = tile_info(p, t_begin + kq, t_begin, t_end);
       idle = 0;
       continue;
     }
-    // bounded: give up (and flag a timeout) if nothing became ready for kWaitTimeoutNs
-    if ((++idle & 1023u) == 0) {
+    if (kp < kq && m.pv_ready(kp, tp)) {
+      m.pv(kp, tp);
+      if (++kp < n) tp = tile_info(p, t_begin + kp, t_begin, t_end);
+      idle = 0;
+      continue;
+    }
+    // Nothing ready: back off briefly so the polling thread leaves issue slots to the warps that
+    // share its scheduler, and give up (flagging a timeout) after kWaitTimeoutNs.
+    __nanosleep(20);
+    if ((++idle & 255u) == 0) {
       if (sm->abort) break;
       const uint64_t t = globaltimer_ns();
-      if (t_idle == 0 || idle == 1024) t_idle = t;
+      if (idle == 256) t_idle = t;
       else if (t - t_idle > kWaitTimeoutNs) {
         fail(sm, p.status);
         break;
       }
     }
   }
+  // never leave with a q copy in flight (abort path)
+  if (q_copies > 0) mbar_wait(&sm->q_full[which], (uint32_t)((q_copies - 1) & 1), nullptr, kWaitTimeoutNs);
   // drain: every UMMA of this thread has completed before TMEM is released
   umma_commit(&sm->drain);
   mbar_wait(&sm->drain, 0, nullptr, kWaitTimeoutNs);
@@ -727,8 +775,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   if (threadIdx.x == 0) {
     for (int i = 0; i < kRingStages; ++i) {
       mbar_init(&sm->ring_full[i], 1);
-      mbar_init(&sm->ring_empty[i], 2);
+      sm->stage_cnt[i] = 0;
     }
+    mbar_init(&sm->rows_full, 2);
+    mbar_init(&sm->rows_empty, 4);
     for (int h = 0; h < 2; ++h) {
       for (int i = 0; i < 4; ++i) mbar_init(&sm->vfree[h][i], 1);
       mbar_init(&sm->kv_ready[h], 4);
@@ -742,7 +792,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     mbar_init(&sm->p_full[1], 128);
     mbar_init(&sm->o_done, 2);
     mbar_init(&sm->o_free, 128);
-    mbar_init(&sm->q_full, 1);
+    mbar_init(&sm->q_full[0], 1);
+    mbar_init(&sm->q_full[1], 1);
     mbar_init(&sm->drain, 2);
     sm->abort = 0;
     fence_barrier_init();
@@ -756,7 +807,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   tc_fence_after();
 
   if (warp == 0 || warp == 3) {
-    producer_loop(p, sm, ring, qs, t_begin, t_end, warp == 0 ? 0 : 1);
+    producer_loop(p, sm, t_begin, t_end, warp == 0 ? 0 : 1);
   } else if (warp == 1 || warp == 2) {
     if ((threadIdx.x & 31) == 0) mma_loop<NH>(p, sm, vtile, qs, ps, t_begin, t_end, warp - 1);
     __syncwarp();
@@ -885,6 +936,7 @@ template <int NH>
 constexpr size_t decode_smem_bytes() {
   return 1024 + kVBytes + 9 * NH * 128 + 2 * 128 * NH * 2 + kRingStages * kRingStageBytes + sizeof(Smem);
 }
+static_assert(decode_smem_bytes<32>() <= 232448, "decode CTA exceeds the 227 KB shared-memory limit");
 
 }  // namespace
 
@@ -900,6 +952,18 @@ static cudaLaunchAttribute pdl_attr() {
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream) {
   cudaError_t err;
   const bool h32 = p.heads_per_cta == 32;
+  // The prep and merge grids ask for the same (maximum) shared-memory carveout as the decode grid,
+  // so an SM does not have to be drained and reconfigured between the three kernels.
+  static bool carveout_set = false;
+  if (!carveout_set) {
+    const void* small[4] = {(const void*)q_prep_kernel<32>, (const void*)q_prep_kernel<16>,
+                            (const void*)merge_kernel<32>, (const void*)merge_kernel<16>};
+    for (const void* f : small) {
+      err = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+      if (err != cudaSuccess) return err;
+    }
+    carveout_set = true;
+  }
   if (h32) q_prep_kernel<32><<<(unsigned)p.units, 256, 0, stream>>>(p);
   else q_prep_kernel<16><<<(unsigned)p.units, 256, 0, stream>>>(p);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;

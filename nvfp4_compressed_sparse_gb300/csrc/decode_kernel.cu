@@ -78,7 +78,7 @@ struct alignas(16) Smem {
   uint32_t maskbuf[2][kRingStages];  // producer -> dequant: usable rows of each 32-row stage, by tile parity
   uint32_t stage_cnt[kRingStages];   // dequant warps done with a ring stage (2 per tile)
   uint32_t vmask[2][4];              // dequant -> softmax: usable rows of the tile, by tile parity
-  float red[4][32];                  // softmax group: per-warp partial reductions
+  alignas(16) float red[4][32];      // softmax group: per-warp partial reductions (float4 stores)
   int vote[4];                       // softmax group: does a warp see a score above max + kLazy
   int need_rescale;
 };
@@ -533,6 +533,13 @@ __device__ void mma_loop(const DecodeParams& p, Smem* sm, uint8_t* vtile, uint8_
 }
 
 // ------------------------------------------------------------------ softmax / epilogue
+// Maximum of v over the 32 lanes of the warp (every lane gets it).
+__device__ __forceinline__ float redux_max(float v) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
+}
+
 // Transpose-reduce 32 values across a warp: afterwards lane l holds the reduction
 // (over the 32 lanes) of element l. op: 0 = max, 1 = sum.
 template <int OP>
@@ -614,21 +621,31 @@ __device__ void softmax_loop(const DecodeParams& p, Smem* sm, uint8_t* ps, int64
     float z[32];
     const bool valid = (sm->vmask[k & 1][w] >> lane) & 1u;
     load_scores<NH>(tmem_lane + s_col, valid, qscale, z);
-    // ---- lazy running max: vote whether any score exceeds max + kLazy
-    bool exceed = false;
+    // ---- lazy running max: vote whether any score exceeds max + kLazy (the first tile of a unit
+    // always sets the max, so it skips the vote)
+    bool raise = ti.first;
+    if (!raise) {
+      bool exceed = false;
 #pragma unroll
-    for (int h = 0; h < 32; h += 4) {
-      const float4 mv = *reinterpret_cast<const float4*>(&sm->m_used[h]);
-      exceed |= (z[h] > mv.x + kLazy) | (z[h + 1] > mv.y + kLazy) | (z[h + 2] > mv.z + kLazy) | (z[h + 3] > mv.w + kLazy);
+      for (int h = 0; h < 32; h += 4) {
+        const float4 mv = *reinterpret_cast<const float4*>(&sm->m_used[h]);
+        exceed |= (z[h] > mv.x + kLazy) | (z[h + 1] > mv.y + kLazy) | (z[h + 2] > mv.z + kLazy) | (z[h + 3] > mv.w + kLazy);
+      }
+      const int wv = __any_sync(0xffffffffu, exceed) ? 1 : 0;
+      if (lane == 0) sm->vote[w] = wv;
+      named_sync_softmax();
+      raise = (sm->vote[0] | sm->vote[1] | sm->vote[2] | sm->vote[3]) != 0;
     }
-    const int wv = __any_sync(0xffffffffu, exceed) ? 1 : 0;
-    if (lane == 0) sm->vote[w] = wv;
-    named_sync_softmax();
-    const bool raise = (sm->vote[0] | sm->vote[1] | sm->vote[2] | sm->vote[3]) != 0;
     if (raise) {
-      {
-        const float wm = warp_transpose_reduce<0>(z);   // lane l: max over this warp's rows of head l (z is
-        sm->red[w][lane] = wm;                          // consumed here and reloaded below)
+      // per-warp maximum of every head over the warp's 32 rows (warp reductions; z stays intact)
+#pragma unroll
+      for (int h = 0; h < 32; h += 4) {
+        float4 wm;
+        wm.x = redux_max(z[h]);
+        wm.y = redux_max(z[h + 1]);
+        wm.z = redux_max(z[h + 2]);
+        wm.w = redux_max(z[h + 3]);
+        if (lane == 0) *reinterpret_cast<float4*>(&sm->red[w][h]) = wm;
       }
       named_sync_softmax();
       if (w == 0) {
@@ -671,8 +688,9 @@ __device__ void softmax_loop(const DecodeParams& p, Smem* sm, uint8_t* ps, int64
           else tmem_st16(tmem_lane + o_col + mb * NH, *reinterpret_cast<uint32_t(*)[16]>(r));
         }
         tmem_wait_st();
+        // z was not kept across the rescale (register pressure): reload this tile's scores
+        load_scores<NH>(tmem_lane + s_col, valid, qscale, z);
       }
-      load_scores<NH>(tmem_lane + s_col, valid, qscale, z);
     }
     tc_fence_before();
     __syncwarp();

@@ -33,6 +33,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <mutex>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -918,23 +920,49 @@ __global__ void __launch_bounds__(512) merge_kernel(const DecodeParams p) {
   const int64_t g0 = unit * p.tiles_per_unit, g1 = g0 + p.tiles_per_unit - 1;
   const int64_t c_lo = ((g0 + 1) * p.ctas - 1) / p.total_tiles;
   const int64_t c_hi = ((g1 + 1) * p.ctas - 1) / p.total_tiles;
+  const int n = (int)(c_hi - c_lo + 1);   // CTAs (partial slots) that covered the unit
   const float kNegInf = __int_as_float(0xff800000);
-  float mstar = kNegInf;
-  for (int64_t c = c_lo; c <= c_hi; ++c) {
-    const float2 ml = reinterpret_cast<const float2*>(p.part_ml)[(c + unit) * NH + h];
-    if (ml.y > 0.f) mstar = fmaxf(mstar, ml.x);
-  }
+  const float2* ml_base = reinterpret_cast<const float2*>(p.part_ml) + (c_lo + unit) * NH + h;
+  const float4* o_base = reinterpret_cast<const float4*>(p.part_o + ((c_lo + unit) * NH + h) * (int64_t)kLatent) + d4;
+  constexpr int64_t kSlotO = (int64_t)NH * kLatent / 4;   // float4 stride between slots
+  float mstar = kNegInf, lsum = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float lsum = 0.f;
-  if (mstar != kNegInf) {
-    for (int64_t c = c_lo; c <= c_hi; ++c) {
-      const int64_t slot = c + unit;
-      const float2 ml = reinterpret_cast<const float2*>(p.part_ml)[slot * NH + h];
-      if (!(ml.y > 0.f)) continue;
-      const float wgt = exp2f(ml.x - mstar);
-      lsum += wgt * ml.y;
-      const float4 o = reinterpret_cast<const float4*>(p.part_o + (slot * NH + h) * (int64_t)kLatent)[d4];
-      acc.x += wgt * o.x; acc.y += wgt * o.y; acc.z += wgt * o.z; acc.w += wgt * o.w;
+  constexpr int kMax = 8;
+  if (n <= kMax) {
+    // every load is issued before any is used: one memory round trip
+    float2 ml[kMax];
+    float4 o[kMax];
+#pragma unroll
+    for (int i = 0; i < kMax; ++i) {
+      ml[i] = i < n ? ml_base[(int64_t)i * NH] : make_float2(kNegInf, 0.f);
+      o[i] = i < n ? o_base[(int64_t)i * kSlotO] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int i = 0; i < kMax; ++i)
+      if (ml[i].y > 0.f) mstar = fmaxf(mstar, ml[i].x);
+    if (mstar != kNegInf) {
+#pragma unroll
+      for (int i = 0; i < kMax; ++i) {
+        if (!(ml[i].y > 0.f)) continue;
+        const float wgt = exp2f(ml[i].x - mstar);
+        lsum += wgt * ml[i].y;
+        acc.x += wgt * o[i].x; acc.y += wgt * o[i].y; acc.z += wgt * o[i].z; acc.w += wgt * o[i].w;
+      }
+    }
+  } else {
+    for (int i = 0; i < n; ++i) {
+      const float2 ml = ml_base[(int64_t)i * NH];
+      if (ml.y > 0.f) mstar = fmaxf(mstar, ml.x);
+    }
+    if (mstar != kNegInf) {
+      for (int i = 0; i < n; ++i) {
+        const float2 ml = ml_base[(int64_t)i * NH];
+        if (!(ml.y > 0.f)) continue;
+        const float wgt = exp2f(ml.x - mstar);
+        lsum += wgt * ml.y;
+        const float4 o = o_base[(int64_t)i * kSlotO];
+        acc.x += wgt * o.x; acc.y += wgt * o.y; acc.z += wgt * o.z; acc.w += wgt * o.w;
+      }
     }
   }
   int b, j, hg;
@@ -965,30 +993,52 @@ static cudaLaunchAttribute pdl_attr() {
   return a;
 }
 
+// Kernel attributes are set once per device (a cudaFuncSetAttribute between the prep launch and the
+// decode launch would keep the decode grid from starting while the prep grid runs).
+static cudaError_t set_attributes() {
+  cudaError_t result = cudaSuccess;
+  const void* small[4] = {(const void*)q_prep_kernel<32>, (const void*)q_prep_kernel<16>,
+                          (const void*)merge_kernel<32>, (const void*)merge_kernel<16>};
+  // The prep and merge grids ask for the same (maximum) shared-memory carveout as the decode grid,
+  // so an SM does not have to be reconfigured between the three kernels.
+  for (const void* f : small) {
+    const cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e != cudaSuccess && result == cudaSuccess) result = e;
+  }
+  cudaError_t e = cudaFuncSetAttribute((const void*)decode_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)decode_smem_bytes<32>());
+  if (e != cudaSuccess && result == cudaSuccess) result = e;
+  e = cudaFuncSetAttribute((const void*)decode_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)decode_smem_bytes<16>());
+  if (e != cudaSuccess && result == cudaSuccess) result = e;
+  return result;
+}
+
+static cudaError_t set_attributes_once() {
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static bool done[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= kMaxDevices) return set_attributes();
+  std::lock_guard<std::mutex> lock(mu);
+  if (done[dev]) return cudaSuccess;
+  err = set_attributes();
+  if (err == cudaSuccess) done[dev] = true;
+  return err;
+}
+
 // q prep (ordinary launch) -> decode (PDL) -> merge (PDL): each dependent grid is
 // launched early and waits with griddepcontrol.wait before reading its inputs.
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream) {
-  cudaError_t err;
+  cudaError_t err = set_attributes_once();
+  if (err != cudaSuccess) return err;
   const bool h32 = p.heads_per_cta == 32;
-  // The prep and merge grids ask for the same (maximum) shared-memory carveout as the decode grid,
-  // so an SM does not have to be drained and reconfigured between the three kernels.
-  static bool carveout_set = false;
-  if (!carveout_set) {
-    const void* small[4] = {(const void*)q_prep_kernel<32>, (const void*)q_prep_kernel<16>,
-                            (const void*)merge_kernel<32>, (const void*)merge_kernel<16>};
-    for (const void* f : small) {
-      err = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-      if (err != cudaSuccess) return err;
-    }
-    carveout_set = true;
-  }
   if (h32) q_prep_kernel<32><<<(unsigned)p.units, 256, 0, stream>>>(p);
   else q_prep_kernel<16><<<(unsigned)p.units, 256, 0, stream>>>(p);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   const size_t smem = h32 ? decode_smem_bytes<32>() : decode_smem_bytes<16>();
-  const void* fn = h32 ? (const void*)decode_kernel<32> : (const void*)decode_kernel<16>;
-  err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)p.ctas, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);

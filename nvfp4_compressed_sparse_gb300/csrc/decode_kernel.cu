@@ -856,6 +856,18 @@ __global__ void __launch_bounds__(256) q_prep_kernel(const DecodeParams p) {
   const int64_t unit = blockIdx.x;
   int b, j, hg;
   split_unit(p, unit, b, j, hg);
+  if (hg == 0) {
+    // Warm L2 with this query's index list and (once per request) the request's page-table row:
+    // the decode grid resolves its first tiles from them while this grid runs.
+    const char* tk = reinterpret_cast<const char*>(p.idx + ((int64_t)b * p.Q + j) * p.topk);
+    const int64_t tk_bytes = (int64_t)p.topk * 4;
+    for (int64_t o = (int64_t)threadIdx.x * 128; o < tk_bytes; o += 256 * 128) prefetch_l2(tk + o);
+    if (j == 0) {
+      const char* pt = reinterpret_cast<const char*>(p.page_table + (int64_t)b * p.max_pages);
+      const int64_t pt_bytes = p.max_pages * 4;
+      for (int64_t o = (int64_t)threadIdx.x * 128; o < pt_bytes; o += 256 * 128) prefetch_l2(pt + o);
+    }
+  }
   const uint16_t* src = p.q + (((int64_t)b * p.Q + j) * p.H + (int64_t)hg * NH) * kQK;
   uint8_t* dst = p.q16 + unit * (int64_t)(9 * NH * 128);
   constexpr int kChunks = NH * (kQK / 8);           // 16-byte chunks of the unit's q block

@@ -920,34 +920,37 @@ __global__ void __launch_bounds__(256) q_prep_kernel(const DecodeParams p) {
 }
 
 // ------------------------------------------------------------------ merge
-// Block (virtual unit, group of 4 heads), 512 threads: 128 threads per head,
-// 4 latent dims each. Combines the partials of the CTAs that covered the unit
-// with the log-sum-exp rule; writes bf16 out and fp32 LSE (natural log).
+// Block (virtual unit, group of 8 heads), 512 threads: 64 threads per head, 8 latent dims each,
+// so the whole grid fits on the GPU at once. Combines the partials of the CTAs that covered the
+// unit with the log-sum-exp rule (m* = max m_s, w_s = 2^(m_s - m*), O = sum w_s O_s / sum w_s l_s);
+// writes bf16 out and fp32 LSE (natural log). For units covered by up to kMax CTAs every load is
+// issued before any is used (one memory round trip).
 template <int NH>
 __global__ void __launch_bounds__(512) merge_kernel(const DecodeParams p) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int64_t unit = blockIdx.x;
-  const int h = blockIdx.y * 4 + (threadIdx.x >> 7);
-  const int d4 = threadIdx.x & 127;
+  const int h = blockIdx.y * 8 + (threadIdx.x >> 6);
+  const int d8 = threadIdx.x & 63;                 // dims 8*d8 .. 8*d8+7
   const int64_t g0 = unit * p.tiles_per_unit, g1 = g0 + p.tiles_per_unit - 1;
   const int64_t c_lo = ((g0 + 1) * p.ctas - 1) / p.total_tiles;
   const int64_t c_hi = ((g1 + 1) * p.ctas - 1) / p.total_tiles;
   const int n = (int)(c_hi - c_lo + 1);   // CTAs (partial slots) that covered the unit
   const float kNegInf = __int_as_float(0xff800000);
   const float2* ml_base = reinterpret_cast<const float2*>(p.part_ml) + (c_lo + unit) * NH + h;
-  const float4* o_base = reinterpret_cast<const float4*>(p.part_o + ((c_lo + unit) * NH + h) * (int64_t)kLatent) + d4;
+  const float4* o_base = reinterpret_cast<const float4*>(p.part_o + ((c_lo + unit) * NH + h) * (int64_t)kLatent) + 2 * d8;
   constexpr int64_t kSlotO = (int64_t)NH * kLatent / 4;   // float4 stride between slots
   float mstar = kNegInf, lsum = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  constexpr int kMax = 8;
+  float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+  constexpr int kMax = 4;
   if (n <= kMax) {
-    // every load is issued before any is used: one memory round trip
     float2 ml[kMax];
-    float4 o[kMax];
+    float4 o0[kMax], o1[kMax];
 #pragma unroll
     for (int i = 0; i < kMax; ++i) {
-      ml[i] = i < n ? ml_base[(int64_t)i * NH] : make_float2(kNegInf, 0.f);
-      o[i] = i < n ? o_base[(int64_t)i * kSlotO] : make_float4(0.f, 0.f, 0.f, 0.f);
+      const bool in = i < n;
+      ml[i] = in ? ml_base[(int64_t)i * NH] : make_float2(kNegInf, 0.f);
+      o0[i] = in ? o_base[(int64_t)i * kSlotO] : make_float4(0.f, 0.f, 0.f, 0.f);
+      o1[i] = in ? o_base[(int64_t)i * kSlotO + 1] : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
     for (int i = 0; i < kMax; ++i)
@@ -956,9 +959,10 @@ __global__ void __launch_bounds__(512) merge_kernel(const DecodeParams p) {
 #pragma unroll
       for (int i = 0; i < kMax; ++i) {
         if (!(ml[i].y > 0.f)) continue;
-        const float wgt = exp2f(ml[i].x - mstar);
-        lsum += wgt * ml[i].y;
-        acc.x += wgt * o[i].x; acc.y += wgt * o[i].y; acc.z += wgt * o[i].z; acc.w += wgt * o[i].w;
+        const float w = exp2f(ml[i].x - mstar);
+        lsum += w * ml[i].y;
+        a0.x += w * o0[i].x; a0.y += w * o0[i].y; a0.z += w * o0[i].z; a0.w += w * o0[i].w;
+        a1.x += w * o1[i].x; a1.y += w * o1[i].y; a1.z += w * o1[i].z; a1.w += w * o1[i].w;
       }
     }
   } else {
@@ -970,10 +974,11 @@ __global__ void __launch_bounds__(512) merge_kernel(const DecodeParams p) {
       for (int i = 0; i < n; ++i) {
         const float2 ml = ml_base[(int64_t)i * NH];
         if (!(ml.y > 0.f)) continue;
-        const float wgt = exp2f(ml.x - mstar);
-        lsum += wgt * ml.y;
-        const float4 o = o_base[(int64_t)i * kSlotO];
-        acc.x += wgt * o.x; acc.y += wgt * o.y; acc.z += wgt * o.z; acc.w += wgt * o.w;
+        const float w = exp2f(ml.x - mstar);
+        lsum += w * ml.y;
+        const float4 o0 = o_base[(int64_t)i * kSlotO], o1 = o_base[(int64_t)i * kSlotO + 1];
+        a0.x += w * o0.x; a0.y += w * o0.y; a0.z += w * o0.z; a0.w += w * o0.w;
+        a1.x += w * o1.x; a1.y += w * o1.y; a1.z += w * o1.z; a1.w += w * o1.w;
       }
     }
   }
@@ -981,13 +986,14 @@ __global__ void __launch_bounds__(512) merge_kernel(const DecodeParams p) {
   split_unit(p, unit, b, j, hg);
   const int64_t row = ((int64_t)b * p.Q + j) * p.H + (int64_t)hg * NH + h;
   const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-  const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-  const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
-  uint2 packed;
-  packed.x = *reinterpret_cast<const uint32_t*>(&lo);
-  packed.y = *reinterpret_cast<const uint32_t*>(&hi);
-  reinterpret_cast<uint2*>(p.out + row * kLatent)[d4] = packed;
-  if (d4 == 0) p.lse[row] = lsum > 0.f ? (mstar + log2f(lsum)) * 0.69314718055994530942f : kNegInf;
+  const __nv_bfloat162 v0 = __floats2bfloat162_rn(a0.x * inv, a0.y * inv);
+  const __nv_bfloat162 v1 = __floats2bfloat162_rn(a0.z * inv, a0.w * inv);
+  const __nv_bfloat162 v2 = __floats2bfloat162_rn(a1.x * inv, a1.y * inv);
+  const __nv_bfloat162 v3 = __floats2bfloat162_rn(a1.z * inv, a1.w * inv);
+  reinterpret_cast<uint4*>(p.out + row * kLatent)[d8] =
+      make_uint4(*reinterpret_cast<const uint32_t*>(&v0), *reinterpret_cast<const uint32_t*>(&v1),
+                 *reinterpret_cast<const uint32_t*>(&v2), *reinterpret_cast<const uint32_t*>(&v3));
+  if (d8 == 0) p.lse[row] = lsum > 0.f ? (mstar + log2f(lsum)) * 0.69314718055994530942f : kNegInf;
 }
 
 template <int NH>
@@ -1065,7 +1071,7 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream) {
 
 cudaError_t launch_merge(const DecodeParams& p, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)p.units, (unsigned)(p.heads_per_cta / 4), 1);
+  cfg.gridDim = dim3((unsigned)p.units, (unsigned)(p.heads_per_cta / 8), 1);
   cfg.blockDim = dim3(512, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;

@@ -147,11 +147,18 @@ size_t sparse_mla_decode_workspace_size(int B, int Q, int H, int topk, int num_s
  *                     initialisation and are clobbered
  *   dev_status        optional int32[NVFP4MLA_STATUS_WORDS] (may be NULL)
  *   flags             0, or NVFP4MLA_FLAG_MAX_CTAS(n) to cap the number of
- *                     decode CTAs at n (testing aid; 0 = no cap)
+ *                     decode CTAs at n (testing aid; 0 = no cap), optionally
+ *                     or-ed with NVFP4MLA_FLAG_TEST_TIMEOUT (testing aid: the
+ *                     decode grid withholds one internal signal, so its
+ *                     bounded waits expire after about 2 s; the grid then
+ *                     counts the timeout in dev_status[NVFP4MLA_STAT_TIMEOUT],
+ *                     drains its copies and returns; out and lse are
+ *                     undefined)
  *   stream            cudaStream_t
  * Calls that share a workspace must be ordered on one stream.
  */
 #define NVFP4MLA_FLAG_MAX_CTAS(n) ((uint32_t)(n) & 0xFFFFu)
+#define NVFP4MLA_FLAG_TEST_TIMEOUT (1u << 31)
 int sparse_mla_decode(const void* q, const void* kv_cache, int64_t num_pages, const int32_t* page_table,
                       int64_t max_pages_per_seq, const int32_t* topk_indices, const int32_t* seq_lens, int B,
                       int Q, int H, int topk, float softmax_scale, void* out, float* lse, void* workspace,

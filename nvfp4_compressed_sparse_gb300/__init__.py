@@ -19,6 +19,7 @@ PAGE_TOKENS = 64
 LATENT_DIM = 512
 ROPE_DIM = 64
 QK_DIM = 576
+FLAG_TEST_TIMEOUT = 1 << 31   # NVFP4MLA_FLAG_TEST_TIMEOUT
 STATUS_WORDS = 4
 STAT_BAD_INDEX, STAT_BAD_PAGE, STAT_TIMEOUT, STAT_BAD_SLOT = 0, 1, 2, 3
 
@@ -118,10 +119,12 @@ def sparse_mla_decode_workspace_size(B: int, Q: int, H: int, topk: int, num_sms:
 
 
 def sparse_mla_decode(q, kv_cache, page_table, topk_indices, seq_lens, softmax_scale, out=None, lse=None,
-                      workspace=None, dev_status=None, max_ctas: int = 0, stream=None):
+                      workspace=None, dev_status=None, max_ctas: int = 0, stream=None,
+                      test_timeout: bool = False):
     """One sparse MLA decode step. q bf16 [B,Q,H,576], kv_cache uint8 [P,64,352],
     page_table int32 [B,max_pages], topk_indices int32 [B,Q,K], seq_lens int32 [B].
-    Returns (out bf16 [B,Q,H,512], lse fp32 [B,Q,H])."""
+    Returns (out bf16 [B,Q,H,512], lse fp32 [B,Q,H]). max_ctas and test_timeout are the
+    testing aids NVFP4MLA_FLAG_MAX_CTAS and NVFP4MLA_FLAG_TEST_TIMEOUT."""
     import torch
     _check(q, "q", torch.bfloat16, ndim=4)
     dev = q.device
@@ -147,7 +150,8 @@ def sparse_mla_decode(q, kv_cache, page_table, topk_indices, seq_lens, softmax_s
     rc = load_library().sparse_mla_decode(
         _ptr(q), _ptr(kv_cache), kv_cache.shape[0], _ptr(page_table), page_table.shape[1], _ptr(topk_indices),
         _ptr(seq_lens), B, Q, H, K, float(softmax_scale), _ptr(out), _ptr(lse), _ptr(workspace),
-        workspace.numel() * workspace.element_size(), _ptr(dev_status), int(max_ctas) & 0xFFFF, _stream_ptr(stream))
+        workspace.numel() * workspace.element_size(), _ptr(dev_status),
+        (int(max_ctas) & 0xFFFF) | (FLAG_TEST_TIMEOUT if test_timeout else 0), _stream_ptr(stream))
     if rc != 0:
         raise NvFp4MlaError(rc, "sparse_mla_decode")
     return out, lse

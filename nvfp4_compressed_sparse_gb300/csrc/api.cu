@@ -201,6 +201,7 @@ int sparse_mla_decode(const void* q, const void* kv_cache, int64_t num_pages, co
   p.total_tiles = s.total_tiles;
   p.tiles_per_unit = s.tiles_per_unit;
   p.ctas = s.ctas;
+  p.withhold = (flags & NVFP4MLA_FLAG_TEST_TIMEOUT) ? 1u : 0u;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (launch_decode(p, st) != cudaSuccess) return NVFP4MLA_ERR_CUDA;
   if (launch_merge(p, st) != cudaSuccess) return NVFP4MLA_ERR_CUDA;

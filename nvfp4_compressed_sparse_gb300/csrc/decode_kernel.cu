@@ -116,6 +116,18 @@ __device__ __forceinline__ bool wait(Smem* sm, uint64_t* bar, uint32_t parity, i
 }
 
 __device__ __forceinline__ void named_sync_softmax() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// Softmax-group barrier that also ORs a flag over the group, so every thread gets the same answer
+// (the abort flag can be set by another warp at any time; reading it after a plain barrier could
+// let one warp leave while the others wait at the next barrier).
+__device__ __forceinline__ bool named_sync_softmax_any(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, 1, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v)
+      : "memory");
+  return r != 0;
+}
 
 // Unit decomposition: virtual unit -> (b, j, head group)
 __device__ __forceinline__ void split_unit(const DecodeParams& p, int64_t unit, int& b, int& j, int& hg) {
@@ -215,7 +227,8 @@ __device__ void producer_loop(const DecodeParams& p, Smem* sm, int64_t t_begin, 
       if (lane == 0) sm->maskbuf[b][q] = mask;
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&sm->rows_full);
+    // (testing aid: withholding tile 1's table makes the waits on it expire)
+    if (lane == 0 && !(p.withhold && k == 1)) mbar_arrive(&sm->rows_full);
     A0 = A1;
     A1 = A2;
     pg0[0] = pg1[0];
@@ -609,12 +622,11 @@ __device__ void softmax_loop(const DecodeParams& p, Smem* sm, uint8_t* ps, int64
       for (int h = 0; h < 32; ++h) l_part[h] = 0.f;
       if (t < 32) sm->m_used[t] = kNegInf;
     }
-    // ---- scores of this tile (one waiting thread per warp; the named barrier releases the group
-    // and makes the abort flag uniform)
+    // ---- scores of this tile (one waiting thread per warp; the barrier releases the group and
+    // agrees on the abort flag)
     if (lane == 0 && wait(sm, &sm->mask_full[k & 1], (uint32_t)((k >> 1) & 1), p.status))
       wait(sm, &sm->s_full, (uint32_t)(k & 1), p.status);
-    named_sync_softmax();
-    if (sm->abort) {
+    if (named_sync_softmax_any(sm->abort != 0)) {
       ok = false;
       break;
     }
@@ -730,8 +742,7 @@ __device__ void softmax_loop(const DecodeParams& p, Smem* sm, uint8_t* ps, int64
     if (ti.last) {
       // ---- epilogue: write this segment's unnormalised partial
       if (lane == 0) wait(sm, &sm->o_done, (uint32_t)(seg & 1), p.status);
-      named_sync_softmax();
-      if (sm->abort) {
+      if (named_sync_softmax_any(sm->abort != 0)) {
         ok = false;
         break;
       }

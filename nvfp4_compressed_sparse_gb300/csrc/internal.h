@@ -54,6 +54,7 @@ struct DecodeParams {
   int32_t* status;            // optional
   int64_t units, total_tiles;
   int tiles_per_unit, ctas;
+  uint32_t withhold;          // testing aid: 1 = the producers never publish tile 1's row table
 };
 
 cudaError_t launch_pack(const uint16_t* latent, int64_t lstride, const uint16_t* rope, int64_t rstride,

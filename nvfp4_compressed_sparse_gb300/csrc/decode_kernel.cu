@@ -257,15 +257,12 @@ __device__ __forceinline__ bool issue_stage(const DecodeParams& p, Smem* sm, uin
 
 // ------------------------------------------------------------------ dequant
 // Thread = one tile row (token). half 0: latent dims 0..255; half 1: dims 256..511 + rope.
-// One group = 64 values (32 nibble bytes) sharing four block scales (sw).
-// Ring rows are 352 B apart, so lanes l and l+4 of a 16-byte load phase hit the same banks;
-// lanes with bit 2 set (odd) read the group's two 16-byte chunks in the opposite order, which
-// makes both loads conflict-free.
-__device__ __forceinline__ void convert_group(const uint8_t* rowp, int g, uint32_t sw, bool odd, uint32_t (&r)[32]) {
-  const uint4 x0 = *reinterpret_cast<const uint4*>(rowp + 32 * g + (odd ? 16 : 0));
-  const uint4 x1 = *reinterpret_cast<const uint4*>(rowp + 32 * g + (odd ? 0 : 16));
-  const uint4 n0 = odd ? x1 : x0;
-  const uint4 n1 = odd ? x0 : x1;
+// One group = 64 values (32 nibble bytes) sharing four block scales (sw). Ring rows are 352 B
+// apart, so the 16-byte loads see two-way bank conflicts; undoing a lane-dependent load order
+// would cost more ALU work than the conflicts cost (the pass is bound by its conversions).
+__device__ __forceinline__ void convert_group(const uint8_t* rowp, int g, uint32_t sw, uint32_t (&r)[32]) {
+  const uint4 n0 = *reinterpret_cast<const uint4*>(rowp + 32 * g);
+  const uint4 n1 = *reinterpret_cast<const uint4*>(rowp + 32 * g + 16);
   const uint32_t w[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
 #pragma unroll
   for (int bb = 0; bb < 4; ++bb) {
@@ -291,7 +288,6 @@ __device__ void dequant_loop(const DecodeParams& p, Smem* sm, uint8_t* ring, uin
   const int row = 32 * q + lane;
   const uint32_t tmem_row = sm->tmem_base + ((uint32_t)(32 * q) << 16);
   const uint8_t* rowp = ring + q * kRingStageBytes + lane * kRingRowStride;
-  const bool odd = (lane >> 2) & 1;
   int64_t n = t_end - t_begin;
   int64_t issued = 0;   // tiles whose rows this warp has requested for stage q
   // The ring is refilled by the dequant warps themselves: the second of the two warps that read a
@@ -323,22 +319,15 @@ __device__ void dequant_loop(const DecodeParams& p, Smem* sm, uint8_t* ring, uin
     for (int gi = 0; gi < 4; ++gi) {
       const int grp = 4 * half + gi;
       const uint32_t sw = gi == 0 ? sc.x : gi == 1 ? sc.y : gi == 2 ? sc.z : sc.w;
-      convert_group(rowp, grp, sw, odd, r);
+      convert_group(rowp, grp, sw, r);
       __syncwarp();
       tmem_st32(tmem_row + kTmemK + 32 * grp, r);
     }
     if (half == 1) {
-      uint4 rv[4];
-#pragma unroll
-      for (int c = 0; c < 4; c += 2) {   // chunk pairs in lane-dependent order (conflict-free)
-        const uint4 x0 = *reinterpret_cast<const uint4*>(rowp + kRopeOff + 16 * c + (odd ? 16 : 0));
-        const uint4 x1 = *reinterpret_cast<const uint4*>(rowp + kRopeOff + 16 * c + (odd ? 0 : 16));
-        rv[c] = odd ? x1 : x0;
-        rv[c + 1] = odd ? x0 : x1;
-      }
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        const uint32_t w[4] = {rv[c].x, rv[c].y, rv[c].z, rv[c].w};
+        const uint4 v = *reinterpret_cast<const uint4*>(rowp + kRopeOff + 16 * c);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           r[8 * c + 2 * i] = e4m3x2_to_f16x2(w[i] & 0xFFFFu);

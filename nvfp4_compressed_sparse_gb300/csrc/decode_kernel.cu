@@ -268,9 +268,11 @@ __device__ __forceinline__ void convert_group(const uint8_t* rowp, int g, uint32
   for (int bb = 0; bb < 4; ++bb) {
     const uint32_t s2 = e4m3x2_to_f16x2(__byte_perm(sw, 0, bb * 0x11));   // (scale, scale)
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const uint32_t byte = w[2 * bb + (i >> 2)] >> (8 * (i & 3));
-      r[8 * bb + i] = hmul2(e2m1x2_to_f16x2(byte), s2);
+    for (int h = 0; h < 2; ++h) {
+      uint32_t c[4];
+      e2m1x8_to_f16x2x4(w[2 * bb + h], c);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) r[8 * bb + 4 * h + i] = hmul2(c[i], s2);
     }
   }
 }

@@ -271,6 +271,11 @@ def run_gpu(args, world, rank, local):
     status = torch.zeros(4, dtype=torch.int32, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
+    plan_ctas, plan_cluster = m.sparse_mla_decode_plan(case.B, case.Q, case.H, case.topk)
+    launches_per_step = 1 if plan_cluster > 0 else 3
+    timed_unit = ("sparse_mla_decode call (one cluster-mode decode kernel)" if plan_cluster > 0 else
+                  "sparse_mla_decode call (q prep + decode + merge kernels)")
+
     def step():
         m.sparse_mla_decode(q, cache, pt, tk, sl, case.softmax_scale, out=out, lse=lse, workspace=ws,
                             dev_status=status, stream=stream)
@@ -350,9 +355,9 @@ def run_gpu(args, world, rank, local):
                      "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic_from_profile(),
                      "peak_kind": peak_kind, "algorithmic_bytes": nbytes, "algorithmic_flops": flops,
                      "roofline_us": max(roof_hbm_us, roof_tc_us), "tensor_roofline_us": roof_tc_us,
-                     "timed_unit": "sparse_mla_decode call (q prep + decode + merge kernels)"},
+                     "timed_unit": timed_unit, "decode_ctas": plan_ctas, "cluster": plan_cluster},
         "e2e": {"value": e2e_ms * 1000.0, "unit": "us/step", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": 3 * K,
+        "gpu_launches": launches_per_step * K,
         "clocks": clk,
         "pack": {"rows": pack_rows, "us": pack_ms * 1000.0, "gbs": pack_bytes / (pack_ms * 1e-3) / 1e9,
                  "frac_of_hbm": pack_bytes / (pack_ms * 1e-3) / 1e9 / hbm},

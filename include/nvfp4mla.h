@@ -147,7 +147,10 @@ size_t sparse_mla_decode_workspace_size(int B, int Q, int H, int topk, int num_s
  *                     initialisation and are clobbered
  *   dev_status        optional int32[NVFP4MLA_STATUS_WORDS] (may be NULL)
  *   flags             0, or NVFP4MLA_FLAG_MAX_CTAS(n) to cap the number of
- *                     decode CTAs at n (testing aid; 0 = no cap), optionally
+ *                     decode CTAs at n (testing aid; 0 = no cap; a cap also
+ *                     selects the split schedule), optionally or-ed with
+ *                     NVFP4MLA_FLAG_CLUSTER (allow the cluster schedule, see
+ *                     sparse_mla_decode_plan), optionally
  *                     or-ed with NVFP4MLA_FLAG_TEST_TIMEOUT (testing aid: the
  *                     decode grid withholds one internal signal, so its
  *                     bounded waits expire after about 2 s; the grid then
@@ -159,10 +162,41 @@ size_t sparse_mla_decode_workspace_size(int B, int Q, int H, int topk, int num_s
  */
 #define NVFP4MLA_FLAG_MAX_CTAS(n) ((uint32_t)(n) & 0xFFFFu)
 #define NVFP4MLA_FLAG_TEST_TIMEOUT (1u << 31)
+#define NVFP4MLA_FLAG_CLUSTER (1u << 30)
 int sparse_mla_decode(const void* q, const void* kv_cache, int64_t num_pages, const int32_t* page_table,
                       int64_t max_pages_per_seq, const int32_t* topk_indices, const int32_t* seq_lens, int B,
                       int Q, int H, int topk, float softmax_scale, void* out, float* lse, void* workspace,
                       size_t workspace_bytes, int32_t* dev_status, uint32_t flags, void* stream);
+
+/*
+ * sparse_mla_decode_plan: the decode grid that sparse_mla_decode launches for
+ * these sizes and flags on the current device. (The pages give no such call;
+ * it reports this library's schedule.)
+ *
+ * Source: "Prime Inference" (translated), "Native NVFP4 sparse MLA decode
+ * kernel": the selected rows of one query token are split over a cluster of
+ * SMs whose partial results are merged on chip, the cluster size adapted to
+ * the batch. Two schedules:
+ *   - cluster (*cluster = G >= 1): G CTAs (one thread-block cluster, G <= 8)
+ *     per (query, head group); each takes a contiguous share of its selected
+ *     rows and the partials are merged through distributed shared memory
+ *     inside the same grid. Only with NVFP4MLA_FLAG_CLUSTER, and then when
+ *     one wave of such clusters fits the GPU and no CTA runs more tiles of
+ *     128 rows than under the split schedule. (On GB300 it is not faster than
+ *     the split schedule on the measured shapes, whose q-prep and merge grids
+ *     overlap the decode grid through programmatic dependent launch, so it is
+ *     not the default.)
+ *   - split (*cluster = 0, the default): the 128-row tiles of all queries form one
+ *     sequence cut into *ctas contiguous ranges (one CTA per SM); a q-prep
+ *     grid runs before it and a merge grid combines the partials.
+ *   B, Q, H, topk     as for sparse_mla_decode
+ *   flags             as for sparse_mla_decode
+ *   ctas, cluster     host int pointers (either may be NULL): the grid size
+ *                     and G (0 = split schedule)
+ * Returns NVFP4MLA_OK, NVFP4MLA_ERR_INVALID_ARG for invalid sizes, or
+ * NVFP4MLA_ERR_CUDA when the device cannot be queried.
+ */
+int sparse_mla_decode_plan(int B, int Q, int H, int topk, uint32_t flags, int* ctas, int* cluster);
 
 /*
  * sparse_mla_decode_noalloc: sparse_mla_decode for callers that cannot

@@ -6,7 +6,8 @@ the library cannot be loaded (or built with nvcc), importing the functions
 raises; there is no CPU fallback.
 
 C entry points (see include/nvfp4mla.h): mla_kv_pack,
-sparse_mla_decode_workspace_size, sparse_mla_decode, nvfp4mla_status_string.
+sparse_mla_decode_workspace_size, sparse_mla_decode, sparse_mla_decode_plan,
+nvfp4mla_status_string.
 """
 from __future__ import annotations
 
@@ -20,6 +21,7 @@ LATENT_DIM = 512
 ROPE_DIM = 64
 QK_DIM = 576
 FLAG_TEST_TIMEOUT = 1 << 31   # NVFP4MLA_FLAG_TEST_TIMEOUT
+FLAG_CLUSTER = 1 << 30        # NVFP4MLA_FLAG_CLUSTER
 STATUS_WORDS = 4
 STAT_BAD_INDEX, STAT_BAD_PAGE, STAT_TIMEOUT, STAT_BAD_SLOT = 0, 1, 2, 3
 
@@ -58,6 +60,8 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.sparse_mla_decode.argtypes = [vp, vp, i64, vp, i64, vp, vp, i32, i32, i32, i32, ctypes.c_float,
                                           vp, vp, vp, sz, vp, u32, vp]
         lib.sparse_mla_decode.restype = i32
+        lib.sparse_mla_decode_plan.argtypes = [i32, i32, i32, i32, u32, ctypes.POINTER(i32), ctypes.POINTER(i32)]
+        lib.sparse_mla_decode_plan.restype = i32
         lib.nvfp4mla_status_string.argtypes = [i32]
         lib.nvfp4mla_status_string.restype = ctypes.c_char_p
         _LIB = lib
@@ -118,13 +122,25 @@ def sparse_mla_decode_workspace_size(B: int, Q: int, H: int, topk: int, num_sms:
     return int(load_library().sparse_mla_decode_workspace_size(B, Q, H, topk, num_sms))
 
 
+def sparse_mla_decode_plan(B: int, Q: int, H: int, topk: int, max_ctas: int = 0,
+                           cluster: bool = False) -> tuple[int, int]:
+    """(decode CTAs, cluster size G; 0 = split schedule) that sparse_mla_decode launches on the current device."""
+    flags = (max_ctas & 0xFFFF) | (FLAG_CLUSTER if cluster else 0)
+    ctas, g = ctypes.c_int(0), ctypes.c_int(0)
+    rc = load_library().sparse_mla_decode_plan(B, Q, H, topk, flags, ctypes.byref(ctas), ctypes.byref(g))
+    if rc != 0:
+        raise NvFp4MlaError(rc, "sparse_mla_decode_plan")
+    return ctas.value, g.value
+
+
 def sparse_mla_decode(q, kv_cache, page_table, topk_indices, seq_lens, softmax_scale, out=None, lse=None,
                       workspace=None, dev_status=None, max_ctas: int = 0, stream=None,
-                      test_timeout: bool = False):
+                      test_timeout: bool = False, cluster: bool = False):
     """One sparse MLA decode step. q bf16 [B,Q,H,576], kv_cache uint8 [P,64,352],
     page_table int32 [B,max_pages], topk_indices int32 [B,Q,K], seq_lens int32 [B].
     Returns (out bf16 [B,Q,H,512], lse fp32 [B,Q,H]). max_ctas and test_timeout are the
-    testing aids NVFP4MLA_FLAG_MAX_CTAS and NVFP4MLA_FLAG_TEST_TIMEOUT."""
+    testing aids NVFP4MLA_FLAG_MAX_CTAS and NVFP4MLA_FLAG_TEST_TIMEOUT; cluster=True sets
+    NVFP4MLA_FLAG_CLUSTER (allow the one-grid cluster schedule)."""
     import torch
     _check(q, "q", torch.bfloat16, ndim=4)
     dev = q.device
@@ -151,7 +167,8 @@ def sparse_mla_decode(q, kv_cache, page_table, topk_indices, seq_lens, softmax_s
         _ptr(q), _ptr(kv_cache), kv_cache.shape[0], _ptr(page_table), page_table.shape[1], _ptr(topk_indices),
         _ptr(seq_lens), B, Q, H, K, float(softmax_scale), _ptr(out), _ptr(lse), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(dev_status),
-        (int(max_ctas) & 0xFFFF) | (FLAG_TEST_TIMEOUT if test_timeout else 0), _stream_ptr(stream))
+        (int(max_ctas) & 0xFFFF) | (FLAG_TEST_TIMEOUT if test_timeout else 0) | (FLAG_CLUSTER if cluster else 0),
+        _stream_ptr(stream))
     if rc != 0:
         raise NvFp4MlaError(rc, "sparse_mla_decode")
     return out, lse

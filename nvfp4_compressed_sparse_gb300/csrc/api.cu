@@ -29,7 +29,7 @@ int device_sm_count() {
   return cached[dev];
 }
 
-DecodeSchedule make_schedule(int B, int Q, int H, int topk, int num_sms, int max_ctas) {
+DecodeSchedule make_schedule(int B, int Q, int H, int topk, int num_sms, int max_ctas, bool allow_cluster) {
   DecodeSchedule s{};
   const int nh = H < kHeadsPerCta ? H : kHeadsPerCta;
   s.units = (int64_t)B * Q * (H / nh);
@@ -40,6 +40,23 @@ DecodeSchedule make_schedule(int B, int Q, int H, int topk, int num_sms, int max
   if (g > s.total_tiles) g = s.total_tiles;
   s.ctas = (int)g;
   s.partial_slots = s.ctas + s.units - 1;
+  s.cluster = 0;
+  // Cluster mode when one wave of G CTAs per unit is as balanced as the stream-K split:
+  // G = min(8, SMs / units, tiles per unit). A cluster CTA that runs one tile more than the
+  // busiest stream-K CTA loses more than the separate q-prep and merge launches cost.
+  if (allow_cluster && max_ctas == 0 && num_sms > 0) {
+    int64_t c = num_sms / s.units;
+    if (c > 8) c = 8;
+    if (c > s.tiles_per_unit) c = s.tiles_per_unit;
+    if (c >= 1) {
+      const int64_t per_cta_cluster = (s.tiles_per_unit + c - 1) / c;
+      const int64_t per_cta_split = (s.total_tiles + s.ctas - 1) / s.ctas;
+      if (per_cta_cluster <= per_cta_split) {
+        s.cluster = (int)c;
+        s.ctas = (int)(s.units * c);
+      }
+    }
+  }
   return s;
 }
 
@@ -105,6 +122,21 @@ static bool encode_cache_map(CUtensorMap* map, const void* cache, int64_t num_pa
 
 using namespace nvfp4mla;
 
+// The decode grid for these sizes on the current device: with NVFP4MLA_FLAG_CLUSTER, the cluster
+// schedule when make_schedule picks it and all its clusters can be resident at once (each CTA takes
+// a whole SM); else stream-K.
+static bool plan_on_device(int B, int Q, int H, int topk, uint32_t flags, DecodeSchedule* out) {
+  const int sms = device_sm_count();
+  if (sms <= 0) return false;
+  DecodeSchedule s = make_schedule(B, Q, H, topk, sms, (int)(flags & 0xFFFFu), (flags & NVFP4MLA_FLAG_CLUSTER) != 0);
+  if (s.cluster > 1) {
+    const int fit = max_active_clusters(H < kHeadsPerCta ? H : kHeadsPerCta, s.cluster);
+    if (fit < s.units) s = make_schedule(B, Q, H, topk, sms, (int)(flags & 0xFFFFu), false);
+  }
+  *out = s;
+  return true;
+}
+
 extern "C" {
 
 const char* nvfp4mla_status_string(int status) {
@@ -139,11 +171,20 @@ int mla_kv_pack(const void* latent, int64_t latent_row_stride, const void* rope,
   return err == cudaSuccess ? NVFP4MLA_OK : NVFP4MLA_ERR_CUDA;
 }
 
+int sparse_mla_decode_plan(int B, int Q, int H, int topk, uint32_t flags, int* ctas, int* cluster) {
+  if (!sizes_ok(B, Q, H, topk)) return NVFP4MLA_ERR_INVALID_ARG;
+  DecodeSchedule s;
+  if (!plan_on_device(B, Q, H, topk, flags, &s)) return NVFP4MLA_ERR_CUDA;
+  if (ctas != nullptr) *ctas = s.ctas;
+  if (cluster != nullptr) *cluster = s.cluster;
+  return NVFP4MLA_OK;
+}
+
 size_t sparse_mla_decode_workspace_size(int B, int Q, int H, int topk, int num_sms) {
   if (!sizes_ok(B, Q, H, topk)) return 0;
   if (num_sms <= 0) num_sms = device_sm_count();
   if (num_sms <= 0) return 0;
-  const DecodeSchedule s = make_schedule(B, Q, H, topk, num_sms, 0);
+  const DecodeSchedule s = make_schedule(B, Q, H, topk, num_sms, 0, false);
   if (s.total_tiles > (int64_t)INT32_MAX) return 0;
   return workspace_bytes_for(s, H);
 }
@@ -163,9 +204,8 @@ int sparse_mla_decode(const void* q, const void* kv_cache, int64_t num_pages, co
   if (!aligned(page_table, 4) || !aligned(topk_indices, 4) || !aligned(seq_lens, 4) || !aligned(lse, 4))
     return NVFP4MLA_ERR_ALIGNMENT;
   if (dev_status != nullptr && !aligned(dev_status, 4)) return NVFP4MLA_ERR_ALIGNMENT;
-  const int sms = device_sm_count();
-  if (sms <= 0) return NVFP4MLA_ERR_CUDA;
-  const DecodeSchedule s = make_schedule(B, Q, H, topk, sms, (int)(flags & 0xFFFFu));
+  DecodeSchedule s;
+  if (!plan_on_device(B, Q, H, topk, flags, &s)) return NVFP4MLA_ERR_CUDA;
   const size_t need = workspace_bytes_for(s, H);
   if (workspace == nullptr || workspace_bytes < need) return NVFP4MLA_ERR_WORKSPACE;
   if (!aligned(workspace, 256)) return NVFP4MLA_ERR_ALIGNMENT;
@@ -201,10 +241,11 @@ int sparse_mla_decode(const void* q, const void* kv_cache, int64_t num_pages, co
   p.total_tiles = s.total_tiles;
   p.tiles_per_unit = s.tiles_per_unit;
   p.ctas = s.ctas;
+  p.cluster = s.cluster;
   p.withhold = (flags & NVFP4MLA_FLAG_TEST_TIMEOUT) ? 1u : 0u;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (launch_decode(p, st) != cudaSuccess) return NVFP4MLA_ERR_CUDA;
-  if (launch_merge(p, st) != cudaSuccess) return NVFP4MLA_ERR_CUDA;
+  if (p.cluster == 0 && launch_merge(p, st) != cudaSuccess) return NVFP4MLA_ERR_CUDA;
   return NVFP4MLA_OK;
 }
 

@@ -83,6 +83,15 @@ struct alignas(16) Smem {
   alignas(16) float red[4][32];      // softmax group: per-warp partial reductions (float4 stores)
   int vote[4];                       // softmax group: does a warp see a score above max + kLazy
   int need_rescale;
+  float wmax[12];                    // cluster mode: per-warp |q| maxima of the in-kernel q conversion
+};
+
+// Cluster mode, end of the kernel: the partial (m, l) of this CTA and the merge's per-head values,
+// kept in the ring buffer (idle once the last tile has been converted).
+struct ClusterScratch {
+  float cm[32], cl[32];              // this CTA's partial running max and sum per head
+  float cw[8][32];                   // weight of each CTA's partial per head
+  float cinv[32], clse[32];          // 1 / combined sum, LSE per head
 };
 
 struct TileInfo {
@@ -135,6 +144,67 @@ __device__ __forceinline__ void split_unit(const DecodeParams& p, int64_t unit, 
   const int64_t u = unit / p.head_groups;
   b = (int)(u / p.Q);
   j = (int)(u - (int64_t)b * p.Q);
+}
+
+// ------------------------------------------------------------------ q image
+// q (bf16) of one (query, head group) -> FP16 scaled by 2^e so that max|q| * 2^e lies in
+// [2^14, 2^15), written as the exact shared-memory image the decode CTA uses as the UMMA B operand
+// (K-major, 128-byte swizzle: 9 atoms of NH rows x 128 B) at dst (global or shared memory).
+// Threads tid = 0..kNT-1 take part; the maximum goes through wmax[kNT / 32] and barrier kBar
+// (0: __syncthreads, else named barrier kBar over kNT threads). Every thread returns the unit's
+// qscale = softmax_scale * log2(e) * 2^-e. All loads are issued before any is used.
+template <int NH, int kNT, int kBar>
+__device__ __forceinline__ float q_image(const DecodeParams& p, int64_t unit, int tid, uint8_t* dst, float* wmax) {
+  int b, j, hg;
+  split_unit(p, unit, b, j, hg);
+  const uint16_t* src = p.q + (((int64_t)b * p.Q + j) * p.H + (int64_t)hg * NH) * kQK;
+  constexpr int kChunks = NH * (kQK / 8);           // 16-byte chunks of the unit's q block
+  constexpr int kPer = (kChunks + kNT - 1) / kNT;
+  uint4 v[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int c = tid + kNT * i;
+    v[i] = c < kChunks ? __ldg(reinterpret_cast<const uint4*>(src) + c) : make_uint4(0u, 0u, 0u, 0u);
+  }
+  float mx = 0.f;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+    for (int t = 0; t < 4; ++t)
+      mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(w[t] << 16)), fabsf(__uint_as_float(w[t] & 0xFFFF0000u))));
+  }
+#pragma unroll
+  for (int s = 16; s >= 1; s >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, s));
+  if ((tid & 31) == 0) wmax[tid >> 5] = mx;
+  if constexpr (kBar == 0) __syncthreads();
+  else asm volatile("bar.sync %0, %1;" ::"n"(kBar), "n"(kNT) : "memory");
+  mx = wmax[0];
+#pragma unroll
+  for (int i = 1; i < kNT / 32; ++i) mx = fmaxf(mx, wmax[i]);
+  int e = 0;
+  if (mx > 0.f && isfinite(mx)) {
+    int E;
+    frexpf(mx, &E);     // mx in [2^(E-1), 2^E)
+    e = 15 - E;
+  }
+  const float up = ldexpf(1.f, e);
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int c = tid + kNT * i;
+    if (c >= kChunks) break;
+    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+    uint32_t o[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const __half2 h = __floats2half2_rn(__uint_as_float(w[t] << 16) * up, __uint_as_float(w[t] & 0xFFFF0000u) * up);
+      o[t] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    const int h = c / (kQK / 8), cc = c % (kQK / 8);
+    const int atom = cc >> 3, ch = cc & 7;
+    *reinterpret_cast<uint4*>(dst + atom * (NH * 128) + h * 128 + ((ch ^ (h & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+  return p.scale_log2 * ldexpf(1.f, -e);
 }
 
 // ------------------------------------------------------------------ producer
@@ -483,13 +553,14 @@ struct MmaIssuer {
 // Each issuer polls (without suspending) and issues whichever of QK(kq) and PV(kp) is ready, so PV
 // of one tile never waits behind QK of the next. QK runs at most one tile ahead of PV; that bound
 // also keeps every polled barrier within one phase of the parity being tested.
-template <int NH>
+template <int NH, bool kCluster>
 __device__ void mma_loop(const DecodeParams& p, Smem* sm, uint8_t* vtile, uint8_t* qs, uint8_t* ps,
                          int64_t t_begin, int64_t t_end, int which) {
   MmaIssuer<NH> m(p, sm, vtile, qs, ps, t_begin, t_end, which);
   const int64_t n = t_end - t_begin;
-  int64_t kq = 0, kp = 0, q_copies = 0;
-  bool q_pending = false;
+  // cluster mode: q_full phase 0 is the unit's q image written in-kernel (no copy to request)
+  int64_t kq = 0, kp = 0, q_copies = kCluster ? 1 : 0;
+  bool q_pending = kCluster;
   TileInfo tq = tile_info(p, t_begin, t_begin, t_end), tp = tq;
   uint64_t t_idle = 0;
   uint32_t idle = 0;
@@ -532,7 +603,7 @@ __device__ void mma_loop(const DecodeParams& p, Smem* sm, uint8_t* vtile, uint8_
     }
   }
   // never leave with a q copy in flight (abort path)
-  if (q_copies > 0) mbar_wait(&sm->q_full[which], (uint32_t)((q_copies - 1) & 1), nullptr, kWaitTimeoutNs);
+  if (q_copies > (kCluster ? 1 : 0)) mbar_wait(&sm->q_full[which], (uint32_t)((q_copies - 1) & 1), nullptr, kWaitTimeoutNs);
   // drain: every UMMA of this thread has completed before TMEM is released
   umma_commit(&sm->drain);
   mbar_wait(&sm->drain, 0, nullptr, kWaitTimeoutNs);
@@ -590,9 +661,9 @@ __device__ __forceinline__ void load_scores(uint32_t taddr, bool valid, float qs
 // most tiles need one group vote instead of a max reduction (and rarely an O rescale), while
 // P = 2^(z - max) stays <= 2^15, inside the fp16 range.
 constexpr float kLazy = 15.f;
-template <int NH>
-__device__ void softmax_loop(const DecodeParams& p, Smem* sm, uint8_t* ps, int64_t t_begin, int64_t t_end,
-                             int64_t cta) {
+template <int NH, bool kCluster>
+__device__ void softmax_loop(const DecodeParams& p, Smem* sm, uint8_t* ps, uint8_t* vtile, ClusterScratch* cs,
+                             int64_t t_begin, int64_t t_end, int64_t cta, float qscale) {
   constexpr uint32_t kPBytes = 128 * NH * 2;
   const int t = threadIdx.x - 384;          // 0..127: tile row / TMEM lane
   const int w = t >> 5, lane = t & 31;
@@ -600,15 +671,14 @@ __device__ void softmax_loop(const DecodeParams& p, Smem* sm, uint8_t* ps, int64
   const uint32_t s_col = kTmemS, o_col = kTmemS + 2 * NH;
   const float kNegInf = __int_as_float(0xff800000);
   float l_part[32];
-  float qscale = 0.f;
   int64_t seg = 0;
   bool ok = true;
-  asm volatile("griddepcontrol.wait;" ::: "memory");   // qscale comes from the prep kernel
+  if constexpr (!kCluster) asm volatile("griddepcontrol.wait;" ::: "memory");   // qscale comes from the prep kernel
   for (int64_t g = t_begin; g < t_end && ok; ++g) {
     const int64_t k = g - t_begin;
     const TileInfo ti = tile_info(p, g, t_begin, t_end);
     if (ti.first) {
-      qscale = p.qscale[ti.unit];
+      if constexpr (!kCluster) qscale = p.qscale[ti.unit];
 #pragma unroll
       for (int h = 0; h < 32; ++h) l_part[h] = 0.f;
       if (t < 32) sm->m_used[t] = kNegInf;
@@ -739,7 +809,9 @@ __device__ void softmax_loop(const DecodeParams& p, Smem* sm, uint8_t* ps, int64
       }
       tc_fence_after();
       const int64_t slot = cta + ti.unit;
-      float* po = p.part_o + slot * (int64_t)NH * kLatent;
+      // stream-K: partial to the workspace; cluster mode: to this CTA's V tile (free now: the last
+      // PV is complete), read by the cluster's CTAs through distributed shared memory
+      float* po = kCluster ? reinterpret_cast<float*>(vtile) : p.part_o + slot * (int64_t)NH * kLatent;
       {
         float v[32];
 #pragma unroll
@@ -750,8 +822,13 @@ __device__ void softmax_loop(const DecodeParams& p, Smem* sm, uint8_t* ps, int64
       named_sync_softmax();
       if (t < NH) {
         const float lsum = sm->red[0][t] + sm->red[1][t] + sm->red[2][t] + sm->red[3][t];
-        p.part_ml[(slot * NH + t) * 2 + 0] = sm->m_used[t];
-        p.part_ml[(slot * NH + t) * 2 + 1] = lsum;
+        if constexpr (kCluster) {
+          cs->cm[t] = sm->m_used[t];
+          cs->cl[t] = lsum;
+        } else {
+          p.part_ml[(slot * NH + t) * 2 + 0] = sm->m_used[t];
+          p.part_ml[(slot * NH + t) * 2 + 1] = lsum;
+        }
       }
       __syncwarp();
 #pragma unroll 1
@@ -775,7 +852,96 @@ __device__ void softmax_loop(const DecodeParams& p, Smem* sm, uint8_t* ps, int64
   }
 }
 
+// ------------------------------------------------------------------ cluster merge
+// Cluster mode: the G CTAs of a cluster hold the partials (O [NH][512] fp32 in their V tiles,
+// running max m and sum l per head) of one unit. CTA r combines latent dims [512r/G, 512(r+1)/G)
+// (rounded to 64) of every head with the log-sum-exp rule (m* = max m_g, w_g = 2^(m_g - m*),
+// O = sum w_g O_g / sum w_g l_g), reading the other CTAs' partials through distributed shared
+// memory, and writes the bf16 output; CTA 0 writes the LSE (natural log).
 template <int NH>
+__device__ void cluster_merge(const DecodeParams& p, ClusterScratch* sm, uint8_t* vtile, int64_t unit, int rank,
+                              bool have) {
+  const int G = p.cluster;
+  const float kNegInf = __int_as_float(0xff800000);
+  if (!have && threadIdx.x < NH) {   // no tiles here: contribute nothing
+    sm->cm[threadIdx.x] = kNegInf;
+    sm->cl[threadIdx.x] = 0.f;
+  }
+  cluster_sync_all();
+  if (threadIdx.x < NH) {
+    const int h = threadIdx.x;
+    const uint32_t am = smem_u32(&sm->cm[h]), al = smem_u32(&sm->cl[h]);
+    float m[8], l[8];
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+      m[g] = g < G ? ld_dsmem_f32(map_shared_rank(am, (uint32_t)g)) : kNegInf;
+      l[g] = g < G ? ld_dsmem_f32(map_shared_rank(al, (uint32_t)g)) : 0.f;
+    }
+    float mstar = kNegInf;
+#pragma unroll
+    for (int g = 0; g < 8; ++g)
+      if (l[g] > 0.f) mstar = fmaxf(mstar, m[g]);
+    float lsum = 0.f;
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+      const float w = l[g] > 0.f ? exp2f(m[g] - mstar) : 0.f;
+      lsum += w * l[g];
+      sm->cw[g][h] = w;
+    }
+    sm->cinv[h] = lsum > 0.f ? 1.f / lsum : 0.f;
+    sm->clse[h] = lsum > 0.f ? (mstar + log2f(lsum)) * 0.69314718055994530942f : kNegInf;
+  }
+  __syncthreads();
+  int b, j, hg;
+  split_unit(p, unit, b, j, hg);
+  const int64_t row0 = ((int64_t)b * p.Q + j) * p.H + (int64_t)hg * NH;
+  if (rank == 0 && threadIdx.x < NH) p.lse[row0 + threadIdx.x] = sm->clse[threadIdx.x];
+  const int d_lo = (kLatent / 8) * ((rank * 8) / G), d_hi = (kLatent / 8) * (((rank + 1) * 8) / G);
+  const int span4 = (d_hi - d_lo) / 4;   // float4 items per head
+  const int total = NH * span4;
+  const uint32_t base = smem_u32(vtile);
+  constexpr int kBatch = 4;   // items per thread per round; every CTA's loads for them are issued together
+  for (int it0 = threadIdx.x; it0 < total; it0 += kThreads * kBatch) {
+    int hh[kBatch], dd[kBatch];
+    float4 acc[kBatch];
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      const int it = it0 + i * kThreads;
+      hh[i] = it < total ? it / span4 : 0;
+      dd[i] = it < total ? d_lo + 4 * (it - hh[i] * span4) : d_lo;
+      acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    for (int g = 0; g < G; ++g) {
+      float4 o[kBatch];
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i)
+        o[i] = ld_dsmem_f4(map_shared_rank(base + (uint32_t)(hh[i] * kLatent + dd[i]) * 4u, (uint32_t)g));
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) {
+        const float w = sm->cw[g][hh[i]];
+        acc[i].x += w * o[i].x;
+        acc[i].y += w * o[i].y;
+        acc[i].z += w * o[i].z;
+        acc[i].w += w * o[i].w;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      if (it0 + i * kThreads >= total) break;
+      const float inv = sm->cinv[hh[i]];
+      const __nv_bfloat162 lo = __floats2bfloat162_rn(acc[i].x * inv, acc[i].y * inv);
+      const __nv_bfloat162 hi = __floats2bfloat162_rn(acc[i].z * inv, acc[i].w * inv);
+      uint2 packed;
+      packed.x = *reinterpret_cast<const uint32_t*>(&lo);
+      packed.y = *reinterpret_cast<const uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(p.out + (row0 + hh[i]) * kLatent + dd[i]) = packed;
+    }
+  }
+  // no CTA leaves (and releases its shared memory) while another may still read it
+  cluster_sync_all();
+}
+
+template <int NH, bool kCluster>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ DecodeParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -788,11 +954,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
 
   const int warp = threadIdx.x >> 5;
   const int64_t cta = blockIdx.x;
-  // Every decode CTA is resident once all of them reach this point, so letting the
-  // merge grid be scheduled now cannot take resources a decode CTA still needs.
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int64_t t_begin = cta * p.total_tiles / p.ctas;
-  const int64_t t_end = (cta + 1) * p.total_tiles / p.ctas;
+  int64_t t_begin, t_end;
+  if constexpr (kCluster) {
+    // cluster u (CTAs uG .. uG+G-1) owns unit u; CTA rank r takes the r-th share of its tiles
+    const int64_t unit = cta / p.cluster, r = cta % p.cluster;
+    t_begin = unit * p.tiles_per_unit + r * p.tiles_per_unit / p.cluster;
+    t_end = unit * p.tiles_per_unit + (r + 1) * p.tiles_per_unit / p.cluster;
+  } else {
+    // Every decode CTA is resident once all of them reach this point, so letting the
+    // merge grid be scheduled now cannot take resources a decode CTA still needs.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    t_begin = cta * p.total_tiles / p.ctas;
+    t_end = (cta + 1) * p.total_tiles / p.ctas;
+  }
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kRingStages; ++i) {
@@ -814,8 +988,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     mbar_init(&sm->p_full[1], 128);
     mbar_init(&sm->o_done, 2);
     mbar_init(&sm->o_free, 128);
-    mbar_init(&sm->q_full[0], 1);
-    mbar_init(&sm->q_full[1], 1);
+    mbar_init(&sm->q_full[0], kCluster ? 384 : 1);   // cluster mode: the converting threads
+    mbar_init(&sm->q_full[1], kCluster ? 384 : 1);
     mbar_init(&sm->drain, 2);
     sm->abort = 0;
     fence_barrier_init();
@@ -828,15 +1002,28 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   __syncthreads();
   tc_fence_after();
 
+  float qscale = 0.f;
+  if constexpr (kCluster) {
+    // The dequant and softmax warps (idle until the first tile arrives) write the unit's q image
+    // straight into the q buffer; the UMMAs read it through the async proxy once every writer
+    // has arrived on q_full.
+    if (warp >= 4) {
+      qscale = q_image<NH, 384, 2>(p, cta / p.cluster, threadIdx.x - 128, qs, sm->wmax);
+      fence_proxy_async_smem();
+      mbar_arrive(&sm->q_full[0]);
+      mbar_arrive(&sm->q_full[1]);
+    }
+  }
   if (warp == 0 || warp == 3) {
     producer_loop(p, sm, t_begin, t_end, warp == 0 ? 0 : 1);
   } else if (warp == 1 || warp == 2) {
-    if ((threadIdx.x & 31) == 0) mma_loop<NH>(p, sm, vtile, qs, ps, t_begin, t_end, warp - 1);
+    if ((threadIdx.x & 31) == 0) mma_loop<NH, kCluster>(p, sm, vtile, qs, ps, t_begin, t_end, warp - 1);
     __syncwarp();
   } else if (warp >= 4 && warp < 12) {
     dequant_loop(p, sm, ring, vtile, t_begin, t_end, warp);
   } else if (warp >= 12) {
-    softmax_loop<NH>(p, sm, ps, t_begin, t_end, cta);
+    softmax_loop<NH, kCluster>(p, sm, ps, vtile, reinterpret_cast<ClusterScratch*>(ring), t_begin, t_end, cta,
+                               qscale);
   }
   tc_fence_before();
   __syncthreads();
@@ -844,13 +1031,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     tc_fence_after();
     tmem_dealloc(sm->tmem_base, kTmemCols);
   }
+  if constexpr (kCluster)
+    cluster_merge<NH>(p, reinterpret_cast<ClusterScratch*>(ring), vtile, cta / p.cluster, (int)(cta % p.cluster),
+                      t_begin < t_end);
 }
 
 // ------------------------------------------------------------------ q prep
-// One block per (query, head group): q (bf16) -> FP16 scaled by 2^e so that
-// max|q| * 2^e lies in [2^14, 2^15), written as the exact shared-memory image
-// the decode CTA uses as the UMMA B operand (K-major, 128-byte swizzle: 9 atoms
-// of NH rows x 128 B). qscale = softmax_scale * log2(e) * 2^-e.
+// Stream-K mode: one block per (query, head group) writes the unit's FP16 q image (see q_image)
+// and its qscale to the workspace, for the decode CTAs to copy.
 template <int NH>
 __global__ void __launch_bounds__(256) q_prep_kernel(const DecodeParams p) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -870,55 +1058,8 @@ __global__ void __launch_bounds__(256) q_prep_kernel(const DecodeParams p) {
       for (int64_t o = (int64_t)threadIdx.x * 128; o < pt_bytes; o += 256 * 128) prefetch_l2(pt + o);
     }
   }
-  const uint16_t* src = p.q + (((int64_t)b * p.Q + j) * p.H + (int64_t)hg * NH) * kQK;
-  uint8_t* dst = p.q16 + unit * (int64_t)(9 * NH * 128);
-  constexpr int kChunks = NH * (kQK / 8);           // 16-byte chunks of the unit's q block
-  constexpr int kPer = (kChunks + 255) / 256;
-  // every load is issued before any is used: one memory round trip, values kept in registers
-  uint4 v[kPer];
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    const int c = threadIdx.x + 256 * i;
-    v[i] = c < kChunks ? __ldg(reinterpret_cast<const uint4*>(src) + c) : make_uint4(0u, 0u, 0u, 0u);
-  }
-  float mx = 0.f;
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-#pragma unroll
-    for (int t = 0; t < 4; ++t)
-      mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(w[t] << 16)), fabsf(__uint_as_float(w[t] & 0xFFFF0000u))));
-  }
-#pragma unroll
-  for (int s = 16; s >= 1; s >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, s));
-  if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = mx;
-  __syncthreads();
-  mx = wmax[0];
-#pragma unroll
-  for (int i = 1; i < 8; ++i) mx = fmaxf(mx, wmax[i]);
-  int e = 0;
-  if (mx > 0.f && isfinite(mx)) {
-    int E;
-    frexpf(mx, &E);     // mx in [2^(E-1), 2^E)
-    e = 15 - E;
-  }
-  const float up = ldexpf(1.f, e);
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    const int c = threadIdx.x + 256 * i;
-    if (c >= kChunks) break;
-    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-    uint32_t o[4];
-#pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      const __half2 h = __floats2half2_rn(__uint_as_float(w[t] << 16) * up, __uint_as_float(w[t] & 0xFFFF0000u) * up);
-      o[t] = *reinterpret_cast<const uint32_t*>(&h);
-    }
-    const int h = c / (kQK / 8), cc = c % (kQK / 8);
-    const int atom = cc >> 3, ch = cc & 7;
-    *reinterpret_cast<uint4*>(dst + atom * (NH * 128) + h * 128 + ((ch ^ (h & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-  }
-  if (threadIdx.x == 0) p.qscale[unit] = p.scale_log2 * ldexpf(1.f, -e);
+  const float qscale = q_image<NH, 256, 0>(p, unit, threadIdx.x, p.q16 + unit * (int64_t)(9 * NH * 128), wmax);
+  if (threadIdx.x == 0) p.qscale[unit] = qscale;
 }
 
 // ------------------------------------------------------------------ merge
@@ -1025,12 +1166,14 @@ static cudaError_t set_attributes() {
     const cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess && result == cudaSuccess) result = e;
   }
-  cudaError_t e = cudaFuncSetAttribute((const void*)decode_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)decode_smem_bytes<32>());
-  if (e != cudaSuccess && result == cudaSuccess) result = e;
-  e = cudaFuncSetAttribute((const void*)decode_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)decode_smem_bytes<16>());
-  if (e != cudaSuccess && result == cudaSuccess) result = e;
+  const void* big[4] = {(const void*)decode_kernel<32, false>, (const void*)decode_kernel<32, true>,
+                        (const void*)decode_kernel<16, false>, (const void*)decode_kernel<16, true>};
+  const int bytes[4] = {(int)decode_smem_bytes<32>(), (int)decode_smem_bytes<32>(), (int)decode_smem_bytes<16>(),
+                        (int)decode_smem_bytes<16>()};
+  for (int i = 0; i < 4; ++i) {
+    const cudaError_t e = cudaFuncSetAttribute(big[i], cudaFuncAttributeMaxDynamicSharedMemorySize, bytes[i]);
+    if (e != cudaSuccess && result == cudaSuccess) result = e;
+  }
   return result;
 }
 
@@ -1049,12 +1192,34 @@ static cudaError_t set_attributes_once() {
   return err;
 }
 
-// q prep (ordinary launch) -> decode (PDL) -> merge (PDL): each dependent grid is
+static cudaLaunchAttribute cluster_attr(int g) {
+  cudaLaunchAttribute a;
+  a.id = cudaLaunchAttributeClusterDimension;
+  a.val.clusterDim.x = (unsigned)g;
+  a.val.clusterDim.y = 1;
+  a.val.clusterDim.z = 1;
+  return a;
+}
+
+// Stream-K: q prep (ordinary launch) -> decode (PDL) -> merge (PDL): each dependent grid is
 // launched early and waits with griddepcontrol.wait before reading its inputs.
+// Cluster mode: the decode grid alone (q converted in-kernel, partials merged on chip).
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream) {
   cudaError_t err = set_attributes_once();
   if (err != cudaSuccess) return err;
   const bool h32 = p.heads_per_cta == 32;
+  if (p.cluster > 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.ctas, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = h32 ? decode_smem_bytes<32>() : decode_smem_bytes<16>();
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1] = {cluster_attr(p.cluster)};
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (h32) return cudaLaunchKernelEx(&cfg, decode_kernel<32, true>, p);
+    return cudaLaunchKernelEx(&cfg, decode_kernel<16, true>, p);
+  }
   if (h32) q_prep_kernel<32><<<(unsigned)p.units, 256, 0, stream>>>(p);
   else q_prep_kernel<16><<<(unsigned)p.units, 256, 0, stream>>>(p);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
@@ -1067,8 +1232,36 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream) {
   cudaLaunchAttribute attr[1] = {pdl_attr()};
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (h32) return cudaLaunchKernelEx(&cfg, decode_kernel<32>, p);
-  return cudaLaunchKernelEx(&cfg, decode_kernel<16>, p);
+  if (h32) return cudaLaunchKernelEx(&cfg, decode_kernel<32, false>, p);
+  return cudaLaunchKernelEx(&cfg, decode_kernel<16, false>, p);
+}
+
+int max_active_clusters(int heads_per_cta, int cluster) {
+  if (set_attributes_once() != cudaSuccess) return 0;
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static int cache[kMaxDevices][2][9] = {};   // value + 1; 0 = not computed yet
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cluster < 1 || cluster > 8) return 0;
+  const int hi = heads_per_cta == 32 ? 1 : 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev >= 0 && dev < kMaxDevices && cache[dev][hi][cluster] > 0) return cache[dev][hi][cluster] - 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(cluster * 64), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = hi ? decode_smem_bytes<32>() : decode_smem_bytes<16>();
+  cudaLaunchAttribute attr[1] = {cluster_attr(cluster)};
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  const cudaError_t e = hi ? cudaOccupancyMaxActiveClusters(&n, decode_kernel<32, true>, &cfg)
+                           : cudaOccupancyMaxActiveClusters(&n, decode_kernel<16, true>, &cfg);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    n = 0;
+  }
+  if (dev >= 0 && dev < kMaxDevices) cache[dev][hi][cluster] = n + 1;
+  return n;
 }
 
 cudaError_t launch_merge(const DecodeParams& p, cudaStream_t stream) {

@@ -19,17 +19,20 @@ constexpr int kTileTokens = 128;      // tokens per decode tile (UMMA M)
 constexpr int kHeadsPerCta = 32;      // heads handled by one decode CTA (UMMA N <= 32)
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;   // bounded in-kernel waits: 2 s
 
-// Work split of the decode kernel: the tiles of all (unit, head-group) pairs
-// form one sequence, cut into `ctas` contiguous ranges (stream-K style).
+// Work split of the decode kernel. Stream-K (cluster == 0): the tiles of all (unit, head-group)
+// pairs form one sequence, cut into `ctas` contiguous ranges; the merge grid combines the partials.
+// Cluster (cluster == G >= 1): G CTAs (one thread-block cluster) per unit, each a contiguous share
+// of the unit's tiles, combined on chip through distributed shared memory.
 struct DecodeSchedule {
   int64_t units;           // B * Q * head_groups
   int tiles_per_unit;      // ceil(topk / 128)
   int64_t total_tiles;     // units * tiles_per_unit
   int ctas;                // grid size
-  int64_t partial_slots;   // ctas + units - 1
+  int64_t partial_slots;   // stream-K: ctas + units - 1
+  int cluster;             // 0 = stream-K, else CTAs per unit
 };
 
-DecodeSchedule make_schedule(int B, int Q, int H, int topk, int num_sms, int max_ctas);
+DecodeSchedule make_schedule(int B, int Q, int H, int topk, int num_sms, int max_ctas, bool allow_cluster);
 size_t workspace_bytes_for(const DecodeSchedule& s, int H);
 
 struct DecodeParams {
@@ -54,6 +57,7 @@ struct DecodeParams {
   int32_t* status;            // optional
   int64_t units, total_tiles;
   int tiles_per_unit, ctas;
+  int cluster;                // 0 = stream-K split, else CTAs per unit (one cluster per unit)
   uint32_t withhold;          // testing aid: 1 = the producers never publish tile 1's row table
 };
 
@@ -61,6 +65,7 @@ cudaError_t launch_pack(const uint16_t* latent, int64_t lstride, const uint16_t*
                         const int64_t* slots, int64_t n, uint8_t* cache, int64_t num_pages, int32_t* status,
                         cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);
+int max_active_clusters(int heads_per_cta, int cluster);   // clusters of the decode grid that fit at once
 cudaError_t launch_merge(const DecodeParams& p, cudaStream_t stream);
 
 int device_sm_count();

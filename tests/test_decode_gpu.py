@@ -60,6 +60,45 @@ def test_small_cases_match_oracle(spec, max_ctas):
     assert_close(out, lse, ref_out, ref_lse, f"{spec} max_ctas={max_ctas}")
 
 
+# Cases the cluster schedule (NVFP4MLA_FLAG_CLUSTER) takes on a 152-SM GB300 (expected G in the id): one CTA per
+# tile, several tiles per CTA, ragged tails, H=16 and several head groups, ranks whose tiles
+# hold only unused (-1) entries, invalid and duplicate entries.
+CLUSTER = [
+    (1, dict(B=1, Q=1, H=32, topk=100, L=(900,))),
+    (2, dict(B=1, Q=1, H=16, topk=256, L=(4096,))),
+    (3, dict(B=2, Q=2, H=64, topk=384, L=(1500, 1400))),
+    (3, dict(B=1, Q=1, H=16, topk=300, L=(100,))),                    # ranks 1, 2: only -1 entries
+    (4, dict(B=2, Q=1, H=32, topk=500, L=(3000, 2500), invalid_frac=0.25, dup=True)),
+    (5, dict(B=1, Q=1, H=32, topk=600, L=(5000,))),
+    (6, dict(B=3, Q=1, H=16, topk=700, L=(900, 1200, 800))),
+    (7, dict(B=1, Q=1, H=32, topk=833, L=(2000,))),
+    (8, dict(B=1, Q=1, H=32, topk=1024, L=(1500,))),
+    (8, dict(B=10, Q=1, H=32, topk=2048, L=(3000,) * 10)),          # two tiles per CTA
+]
+
+
+@pytest.mark.parametrize("G,spec", CLUSTER, ids=lambda x: x if isinstance(x, int) else
+                         "B{B}Q{Q}H{H}K{topk}".format(**x))
+def test_cluster_schedule_matches_oracle(G, spec):
+    ctas, cluster = m.sparse_mla_decode_plan(spec["B"], spec["Q"], spec["H"], spec["topk"], cluster=True)
+    assert m.sparse_mla_decode_plan(spec["B"], spec["Q"], spec["H"], spec["topk"])[1] == 0   # default: split
+    if torch.cuda.get_device_properties(0).multi_processor_count == 152:
+        assert cluster == G, (ctas, cluster)
+    else:
+        assert cluster >= 1, (ctas, cluster)
+    assert ctas == cluster * spec["B"] * spec["Q"] * max(1, spec["H"] // 32)
+    assert m.sparse_mla_decode_plan(spec["B"], spec["Q"], spec["H"], spec["topk"], max_ctas=152, cluster=True)[1] == 0
+    case = workloads.small_case(seed=300 + G + spec["topk"], **spec)
+    lat, rope, rows = _host_cache(case)
+    cache = _gpu_cache(lat, rope, case.num_pages)
+    ref_out, ref_lse = attention.sparse_decode(case.q_bits, rows, case.page_table, case.topk_indices,
+                                               case.seq_lens, case.softmax_scale)
+    out, lse = _decode(case, cache, cluster=True)
+    assert_close(out, lse, ref_out, ref_lse, f"cluster G={cluster} {spec}")
+    out2, lse2 = _decode(case, cache, cluster=True)        # deterministic across calls
+    assert torch.equal(out, out2) and torch.equal(lse, lse2)
+
+
 def test_all_entries_unused_gives_zero_and_neg_inf():
     case = workloads.small_case(B=2, Q=1, H=32, topk=300, L=(500, 600), seed=3)
     case.topk_indices[:] = -1

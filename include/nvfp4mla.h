@@ -12,7 +12,8 @@
  *
  * Common rules for every call:
  *   - All pointers except dev_status may be NULL only where stated. Data
- *     pointers are DEVICE pointers of the current CUDA device.
+ *     pointers are DEVICE pointers of the current CUDA device, except where a
+ *     call states that page-locked host memory is accepted.
  *   - The caller owns every buffer. The library never allocates, never frees
  *     and never synchronises; all work is enqueued on `stream` (a
  *     cudaStream_t; NULL = legacy default stream) and the call returns before
@@ -128,6 +129,17 @@ size_t sparse_mla_decode_workspace_size(int B, int Q, int H, int topk, int num_s
  * (causal within the Q new tokens), idx/64 < max_pages_per_seq and
  * 0 <= page_table[b, idx/64] < num_pages. Entries are counted as often as
  * listed. A query with no usable entry gets out = 0 and lse = -inf.
+ *
+ * Host buffers: q, page_table, topk_indices, seq_lens, out and lse may each be
+ * page-locked host memory mapped for the device at the same address
+ * (cudaMallocHost / cudaHostAlloc, or cudaHostRegister'd; on GB300 the GPU
+ * reaches it over NVLink-C2C). The kernels then read those inputs from, and
+ * write the results to, host memory themselves, in stream order, with results
+ * identical to device buffers; no separate copy is needed. kv_cache, workspace
+ * and dev_status must be device memory. Every pointer is checked with
+ * cudaPointerGetAttributes before anything is enqueued: pageable host memory,
+ * another device's memory or an unknown pointer returns
+ * NVFP4MLA_ERR_INVALID_ARG.
  *
  *   q                 bf16 [B, Q, H, 576] contiguous, 16-byte aligned
  *   kv_cache          uint8 [num_pages, 64, 352], 16-byte aligned

@@ -83,12 +83,15 @@ def _stream_ptr(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
-def _check(t, name, dtype, device=None, ndim=None, contiguous=True):
+def _check(t, name, dtype, device=None, ndim=None, contiguous=True, host_ok=False):
+    """device: the CUDA device the tensor must be on. host_ok: a page-locked (pinned) CPU tensor
+    is accepted too (the kernels read or write it over the host link)."""
     if t.dtype != dtype:
         raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
     if not t.is_cuda:
-        raise ValueError(f"{name}: must be a CUDA tensor")
-    if device is not None and t.device != device:
+        if not (host_ok and t.device.type == "cpu" and t.is_pinned()):
+            raise ValueError(f"{name}: must be a CUDA tensor" + (" or a pinned CPU tensor" if host_ok else ""))
+    elif device is not None and t.device != device:
         raise ValueError(f"{name}: on {t.device}, expected {device}")
     if ndim is not None and t.dim() != ndim:
         raise ValueError(f"{name}: expected {ndim} dims, got {t.dim()}")
@@ -140,14 +143,16 @@ def sparse_mla_decode(q, kv_cache, page_table, topk_indices, seq_lens, softmax_s
     page_table int32 [B,max_pages], topk_indices int32 [B,Q,K], seq_lens int32 [B].
     Returns (out bf16 [B,Q,H,512], lse fp32 [B,Q,H]). max_ctas and test_timeout are the
     testing aids NVFP4MLA_FLAG_MAX_CTAS and NVFP4MLA_FLAG_TEST_TIMEOUT; cluster=True sets
-    NVFP4MLA_FLAG_CLUSTER (allow the one-grid cluster schedule)."""
+    NVFP4MLA_FLAG_CLUSTER (allow the one-grid cluster schedule). q, page_table, topk_indices,
+    seq_lens, out and lse may be pinned CPU tensors: the kernels then read the inputs from and
+    write the results to host memory directly, inside the call's stream order."""
     import torch
-    _check(q, "q", torch.bfloat16, ndim=4)
-    dev = q.device
-    _check(kv_cache, "kv_cache", torch.uint8, dev, 3)
-    _check(page_table, "page_table", torch.int32, dev, 2)
-    _check(topk_indices, "topk_indices", torch.int32, dev, 3)
-    _check(seq_lens, "seq_lens", torch.int32, dev, 1)
+    _check(kv_cache, "kv_cache", torch.uint8, ndim=3)
+    dev = kv_cache.device
+    _check(q, "q", torch.bfloat16, dev, 4, host_ok=True)
+    _check(page_table, "page_table", torch.int32, dev, 2, host_ok=True)
+    _check(topk_indices, "topk_indices", torch.int32, dev, 3, host_ok=True)
+    _check(seq_lens, "seq_lens", torch.int32, dev, 1, host_ok=True)
     B, Q, H, D = q.shape
     K = topk_indices.shape[2]
     if D != QK_DIM or topk_indices.shape[:2] != (B, Q) or seq_lens.shape[0] != B or page_table.shape[0] != B:
@@ -156,8 +161,8 @@ def sparse_mla_decode(q, kv_cache, page_table, topk_indices, seq_lens, softmax_s
         out = torch.empty((B, Q, H, LATENT_DIM), dtype=torch.bfloat16, device=dev)
     if lse is None:
         lse = torch.empty((B, Q, H), dtype=torch.float32, device=dev)
-    _check(out, "out", torch.bfloat16, dev, 4)
-    _check(lse, "lse", torch.float32, dev, 3)
+    _check(out, "out", torch.bfloat16, dev, 4, host_ok=True)
+    _check(lse, "lse", torch.float32, dev, 3, host_ok=True)
     if workspace is None:
         nbytes = sparse_mla_decode_workspace_size(B, Q, H, K)
         workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)

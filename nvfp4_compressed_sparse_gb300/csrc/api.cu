@@ -87,6 +87,30 @@ static bool sizes_ok(int B, int Q, int H, int topk) {
 
 static inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Memory the decode kernels may read or write with this pointer: device or managed memory of the
+// current device, or page-locked host memory mapped for the device at the same address (the
+// kernels then move those bytes over the host link themselves; host_ok = false admits device or
+// managed memory only). Anything else (pageable host memory, another device's memory, an unknown
+// pointer) is rejected before any launch.
+static bool device_addressable(const void* p, bool host_ok = true) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return false;
+  }
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  switch (a.type) {
+    case cudaMemoryTypeDevice:
+    case cudaMemoryTypeManaged:
+      return a.device == dev;
+    case cudaMemoryTypeHost:
+      return host_ok && a.devicePointer == p;
+    default:
+      return false;
+  }
+}
+
 // cuTensorMapEncodeTiled, fetched once through the runtime (no link-time libcuda dependency).
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -204,11 +228,16 @@ int sparse_mla_decode(const void* q, const void* kv_cache, int64_t num_pages, co
   if (!aligned(page_table, 4) || !aligned(topk_indices, 4) || !aligned(seq_lens, 4) || !aligned(lse, 4))
     return NVFP4MLA_ERR_ALIGNMENT;
   if (dev_status != nullptr && !aligned(dev_status, 4)) return NVFP4MLA_ERR_ALIGNMENT;
+  if (!device_addressable(q) || !device_addressable(page_table) || !device_addressable(topk_indices) ||
+      !device_addressable(seq_lens) || !device_addressable(out) || !device_addressable(lse) ||
+      !device_addressable(kv_cache, false) || (dev_status != nullptr && !device_addressable(dev_status, false)))
+    return NVFP4MLA_ERR_INVALID_ARG;
   DecodeSchedule s;
   if (!plan_on_device(B, Q, H, topk, flags, &s)) return NVFP4MLA_ERR_CUDA;
   const size_t need = workspace_bytes_for(s, H);
   if (workspace == nullptr || workspace_bytes < need) return NVFP4MLA_ERR_WORKSPACE;
   if (!aligned(workspace, 256)) return NVFP4MLA_ERR_ALIGNMENT;
+  if (!device_addressable(workspace, false)) return NVFP4MLA_ERR_INVALID_ARG;
   if (num_pages * kPageTokens > (int64_t)INT32_MAX) return NVFP4MLA_ERR_UNSUPPORTED;   // int32 row coordinates
   if (s.total_tiles > (int64_t)INT32_MAX) return NVFP4MLA_ERR_UNSUPPORTED;               // int32 tile numbers
 

@@ -231,3 +231,49 @@ def test_full_size_case_sampled(cfg):
         assert_close(o[b, j], l[b, j], ro, rl, f"cfg {cfg} unit {(b, j)}")
     # every output finite; lse finite where the query has usable entries
     assert np.isfinite(o).all()
+
+
+@pytest.mark.parametrize("kw", [dict(), dict(max_ctas=1), dict(cluster=True)], ids=["split", "split-prep", "cluster"])
+def test_pinned_host_buffers_match_device_buffers(kw):
+    """q, page table, index lists, lengths, out and LSE in page-locked host memory (read and
+    written by the kernels over the host link) give bitwise the device-buffer results."""
+    case = workloads.small_case(B=3, Q=2, H=32, topk=300, L=(1500, 2000, 900), seed=21)
+    lat, rope, rows = _host_cache(case)
+    cache = _gpu_cache(lat, rope, case.num_pages)
+    q, pt, tk, sl = decode_inputs(case)
+    out_d, lse_d = m.sparse_mla_decode(q, cache, pt, tk, sl, case.softmax_scale, **kw)
+    hq, hpt, htk, hsl = (t.cpu().pin_memory() for t in (q, pt, tk, sl))
+    hout = torch.empty(tuple(out_d.shape), dtype=out_d.dtype).pin_memory()
+    hlse = torch.empty(tuple(lse_d.shape), dtype=lse_d.dtype).pin_memory()
+    m.sparse_mla_decode(hq, cache, hpt, htk, hsl, case.softmax_scale, out=hout, lse=hlse, **kw)
+    torch.cuda.synchronize()
+    assert torch.equal(out_d.cpu(), hout) and torch.equal(lse_d.cpu(), hlse)
+    ref_out, ref_lse = attention.sparse_decode(case.q_bits, rows, case.page_table, case.topk_indices,
+                                               case.seq_lens, case.softmax_scale)
+    assert_close(hout, hlse, ref_out, ref_lse, f"host buffers {kw}")
+
+
+def test_pageable_host_memory_is_rejected_before_launch():
+    import ctypes
+    case = workloads.small_case(B=1, Q=1, H=32, topk=128, L=(900,), seed=5)
+    lat, rope, rows = _host_cache(case)
+    cache = _gpu_cache(lat, rope, case.num_pages)
+    q, pt, tk, sl = decode_inputs(case)
+    pageable_q = q.cpu()
+    with pytest.raises(ValueError):
+        m.sparse_mla_decode(pageable_q, cache, pt, tk, sl, case.softmax_scale)
+    lib = m.load_library()
+    out = torch.full((1, 1, 32, 512), 7.0, dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((1, 1, 32), 7.0, dtype=torch.float32, device="cuda")
+    wsb = m.sparse_mla_decode_workspace_size(1, 1, 32, 128)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    P = lambda t: ctypes.c_void_p(t.data_ptr())
+    for name in ("q", "out", "cache"):
+        args = dict(q=q, out=out, cache=cache)
+        args[name] = args[name].cpu()               # pageable copy
+        rc = lib.sparse_mla_decode(P(args["q"]), P(args["cache"]), case.num_pages, P(pt), pt.shape[1], P(tk), P(sl),
+                                   1, 1, 32, 128, ctypes.c_float(case.softmax_scale), P(args["out"]), P(lse), P(ws),
+                                   wsb, None, 0, None)
+        assert rc == 1, (name, rc)
+    torch.cuda.synchronize()
+    assert bool((out == 7.0).all()) and bool((lse == 7.0).all())   # nothing was launched

@@ -3,6 +3,8 @@
 // synchronisation; everything is enqueued on the caller's stream.
 #include <cuda_runtime.h>
 
+#include <atomic>
+#include <chrono>
 #include <cstdint>
 #include <mutex>
 
@@ -63,9 +65,10 @@ DecodeSchedule make_schedule(int B, int Q, int H, int topk, int num_sms, int max
 static inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Workspace: partial O [slots, nh, 512] f32 | partial (max, sum) [slots, nh, 2] f32 |
-// FP16 q images [units, 9 * nh * 128] | q scales [units] f32; each part 256-byte aligned.
+// FP16 q images [units, 9 * nh * 128] | q scales [units] f32 | partial-ready flags [slots] u64;
+// each part 256-byte aligned.
 struct WorkspaceLayout {
-  size_t o, ml, q16, qscale, total;
+  size_t o, ml, q16, qscale, flag, total;
 };
 static WorkspaceLayout layout_for(const DecodeSchedule& s, int H) {
   const int nh = H < kHeadsPerCta ? H : kHeadsPerCta;
@@ -74,7 +77,8 @@ static WorkspaceLayout layout_for(const DecodeSchedule& s, int H) {
   w.ml = w.o + align256((size_t)s.partial_slots * nh * kLatent * sizeof(float));
   w.q16 = w.ml + align256((size_t)s.partial_slots * nh * 2 * sizeof(float));
   w.qscale = w.q16 + align256((size_t)s.units * 9 * nh * 128);
-  w.total = w.qscale + align256((size_t)s.units * sizeof(float));
+  w.flag = w.qscale + align256((size_t)s.units * sizeof(float));
+  w.total = w.flag + align256((size_t)s.partial_slots * sizeof(uint64_t));
   return w;
 }
 
@@ -89,25 +93,25 @@ static inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cas
 
 // Memory the decode kernels may read or write with this pointer: device or managed memory of the
 // current device, or page-locked host memory mapped for the device at the same address (the
-// kernels then move those bytes over the host link themselves; host_ok = false admits device or
-// managed memory only). Anything else (pageable host memory, another device's memory, an unknown
-// pointer) is rejected before any launch.
-static bool device_addressable(const void* p, bool host_ok = true) {
+// kernels then move those bytes over the host link themselves). Anything else (pageable host
+// memory, another device's memory, an unknown pointer) is invalid and rejected before any launch.
+enum PtrKind { kPtrInvalid, kPtrDevice, kPtrHost };
+static PtrKind pointer_kind(const void* p) {
   cudaPointerAttributes a;
   if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
     (void)cudaGetLastError();
-    return false;
+    return kPtrInvalid;
   }
   int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  if (cudaGetDevice(&dev) != cudaSuccess) return kPtrInvalid;
   switch (a.type) {
     case cudaMemoryTypeDevice:
     case cudaMemoryTypeManaged:
-      return a.device == dev;
+      return a.device == dev ? kPtrDevice : kPtrInvalid;
     case cudaMemoryTypeHost:
-      return host_ok && a.devicePointer == p;
+      return a.devicePointer == p ? kPtrHost : kPtrInvalid;
     default:
-      return false;
+      return kPtrInvalid;
   }
 }
 
@@ -145,6 +149,17 @@ static bool encode_cache_map(CUtensorMap* map, const void* cache, int64_t num_pa
 }  // namespace nvfp4mla
 
 using namespace nvfp4mla;
+
+// A tag no earlier call of this process used (odd, so never 0): the merge grid recognises the
+// partials of this call by it, so the workspace needs no clearing between calls.
+static uint64_t next_call_tag() {
+  static std::atomic<uint64_t> counter{0};
+  static const uint64_t seed = (uint64_t)std::chrono::steady_clock::now().time_since_epoch().count();
+  uint64_t z = seed + 0x9E3779B97F4A7C15ull * (counter.fetch_add(1, std::memory_order_relaxed) + 1);
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;   // splitmix64 finaliser
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return (z ^ (z >> 31)) | 1ull;
+}
 
 // The decode grid for these sizes on the current device: with NVFP4MLA_FLAG_CLUSTER, the cluster
 // schedule when make_schedule picks it and all its clusters can be resident at once (each CTA takes
@@ -228,16 +243,18 @@ int sparse_mla_decode(const void* q, const void* kv_cache, int64_t num_pages, co
   if (!aligned(page_table, 4) || !aligned(topk_indices, 4) || !aligned(seq_lens, 4) || !aligned(lse, 4))
     return NVFP4MLA_ERR_ALIGNMENT;
   if (dev_status != nullptr && !aligned(dev_status, 4)) return NVFP4MLA_ERR_ALIGNMENT;
-  if (!device_addressable(q) || !device_addressable(page_table) || !device_addressable(topk_indices) ||
-      !device_addressable(seq_lens) || !device_addressable(out) || !device_addressable(lse) ||
-      !device_addressable(kv_cache, false) || (dev_status != nullptr && !device_addressable(dev_status, false)))
+  const PtrKind k_out = pointer_kind(out), k_lse = pointer_kind(lse);
+  if (pointer_kind(q) == kPtrInvalid || pointer_kind(page_table) == kPtrInvalid ||
+      pointer_kind(topk_indices) == kPtrInvalid || pointer_kind(seq_lens) == kPtrInvalid || k_out == kPtrInvalid ||
+      k_lse == kPtrInvalid || pointer_kind(kv_cache) != kPtrDevice ||
+      (dev_status != nullptr && pointer_kind(dev_status) != kPtrDevice))
     return NVFP4MLA_ERR_INVALID_ARG;
   DecodeSchedule s;
   if (!plan_on_device(B, Q, H, topk, flags, &s)) return NVFP4MLA_ERR_CUDA;
   const size_t need = workspace_bytes_for(s, H);
   if (workspace == nullptr || workspace_bytes < need) return NVFP4MLA_ERR_WORKSPACE;
   if (!aligned(workspace, 256)) return NVFP4MLA_ERR_ALIGNMENT;
-  if (!device_addressable(workspace, false)) return NVFP4MLA_ERR_INVALID_ARG;
+  if (pointer_kind(workspace) != kPtrDevice) return NVFP4MLA_ERR_INVALID_ARG;
   if (num_pages * kPageTokens > (int64_t)INT32_MAX) return NVFP4MLA_ERR_UNSUPPORTED;   // int32 row coordinates
   if (s.total_tiles > (int64_t)INT32_MAX) return NVFP4MLA_ERR_UNSUPPORTED;               // int32 tile numbers
 
@@ -265,6 +282,9 @@ int sparse_mla_decode(const void* q, const void* kv_cache, int64_t num_pages, co
   p.part_ml = reinterpret_cast<float*>(wsb + wl.ml);
   p.q16 = wsb + wl.q16;
   p.qscale = reinterpret_cast<float*>(wsb + wl.qscale);
+  p.part_flag = reinterpret_cast<uint64_t*>(wsb + wl.flag);
+  p.tag = next_call_tag();
+  p.merge_poll = (k_out == kPtrHost || k_lse == kPtrHost) ? 1 : 0;
   p.status = dev_status;
   p.units = s.units;
   p.total_tiles = s.total_tiles;

@@ -661,8 +661,9 @@ __device__ __forceinline__ void load_scores(uint32_t taddr, bool valid, float qs
 // most tiles need one group vote instead of a max reduction (and rarely an O rescale), while
 // P = 2^(z - max) stays <= 2^15, inside the fp16 range.
 constexpr float kLazy = 15.f;
+// Returns false when the group gave up (abort); every thread of the group returns the same value.
 template <int NH, bool kCluster>
-__device__ void softmax_loop(const DecodeParams& p, Smem* sm, uint8_t* ps, uint8_t* vtile, ClusterScratch* cs,
+__device__ bool softmax_loop(const DecodeParams& p, Smem* sm, uint8_t* ps, uint8_t* vtile, ClusterScratch* cs,
                              int64_t t_begin, int64_t t_end, int64_t cta, float qscale) {
   constexpr uint32_t kPBytes = 128 * NH * 2;
   const int t = threadIdx.x - 384;          // 0..127: tile row / TMEM lane
@@ -850,6 +851,7 @@ __device__ void softmax_loop(const DecodeParams& p, Smem* sm, uint8_t* ps, uint8
       ++seg;
     }
   }
+  return ok;
 }
 
 // ------------------------------------------------------------------ cluster merge
@@ -941,7 +943,10 @@ __device__ void cluster_merge(const DecodeParams& p, ClusterScratch* sm, uint8_t
   cluster_sync_all();
 }
 
-template <int NH, bool kCluster>
+// kCluster: the cluster schedule (in-kernel q, DSMEM merge). kPublish: the split schedule with a
+// polling merge grid (results in host memory): each CTA tags its partial slots when done. The
+// tagging is a separate instance because its mere presence slowed the other split kernel by ~2 %.
+template <int NH, bool kCluster, bool kPublish>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ DecodeParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1022,8 +1027,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   } else if (warp >= 4 && warp < 12) {
     dequant_loop(p, sm, ring, vtile, t_begin, t_end, warp);
   } else if (warp >= 12) {
-    softmax_loop<NH, kCluster>(p, sm, ps, vtile, reinterpret_cast<ClusterScratch*>(ring), t_begin, t_end, cta,
-                               qscale);
+    const bool ok = softmax_loop<NH, kCluster>(p, sm, ps, vtile, reinterpret_cast<ClusterScratch*>(ring), t_begin,
+                                               t_end, cta, qscale);
+    if constexpr (kPublish) {
+      // Polling merge (results in host memory): publish this CTA's partials. Every writer fences
+      // its stores at GPU scope, then one thread tags the CTA's slots, which the merge grid polls
+      // instead of waiting for the whole decode grid.
+      if (ok && t_begin < t_end) {
+        __threadfence();
+        named_sync_softmax();
+        if (threadIdx.x == 384) {
+          const int64_t u0 = t_begin / p.tiles_per_unit, u1 = (t_end - 1) / p.tiles_per_unit;
+          for (int64_t u = u0; u <= u1; ++u) st_relaxed_gpu_u64(p.part_flag + cta + u, p.tag);
+        }
+      }
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -1063,14 +1081,26 @@ __global__ void __launch_bounds__(256) q_prep_kernel(const DecodeParams p) {
 }
 
 // ------------------------------------------------------------------ merge
-// Block (virtual unit, group of 8 heads), 512 threads: 64 threads per head, 8 latent dims each,
-// so the whole grid fits on the GPU at once. Combines the partials of the CTAs that covered the
+// Block (virtual unit, group of 8 heads), 512 threads: 64 threads per head, 8 latent dims each.
+// Combines the partials of the CTAs that covered the
 // unit with the log-sum-exp rule (m* = max m_s, w_s = 2^(m_s - m*), O = sum w_s O_s / sum w_s l_s);
 // writes bf16 out and fp32 LSE (natural log). For units covered by up to kMax CTAs every load is
-// issued before any is used (one memory round trip).
-template <int NH>
+// issued before any is used (one memory round trip). The grid is launched early (programmatic
+// dependent launch). When out and LSE live in host memory (merge_poll), each block starts as soon
+// as its unit's partials are tagged, so most of the results cross the host link while the last
+// decode CTAs still run; otherwise the block waits for the decode grid, which costs less than
+// the tags' fences when the results stay on the device.
+// Partial loads: L2 only when polling (a slot is rewritten by every call, and only thread 0 of the
+// block performed the acquire); plain loads after the grid-completion wait.
+template <bool kPoll, class T>
+__device__ __forceinline__ T ld_partial(const T* ptr) {
+  if constexpr (kPoll) return __ldcg(ptr);
+  else return *ptr;
+}
+
+template <int NH, bool kPoll>
 __global__ void __launch_bounds__(512) merge_kernel(const DecodeParams p) {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if constexpr (!kPoll) asm volatile("griddepcontrol.wait;" ::: "memory");
   const int64_t unit = blockIdx.x;
   const int h = blockIdx.y * 8 + (threadIdx.x >> 6);
   const int d8 = threadIdx.x & 63;                 // dims 8*d8 .. 8*d8+7
@@ -1079,6 +1109,33 @@ __global__ void __launch_bounds__(512) merge_kernel(const DecodeParams p) {
   const int64_t c_hi = ((g1 + 1) * p.ctas - 1) / p.total_tiles;
   const int n = (int)(c_hi - c_lo + 1);   // CTAs (partial slots) that covered the unit
   const float kNegInf = __int_as_float(0xff800000);
+  if constexpr (kPoll) {
+    // Polling mode: the unit's partials are complete once every covering CTA has tagged its slot
+    // with this call's tag (bounded wait; the barrier passes thread 0's acquire on to the block).
+    __shared__ int ready;
+    if (threadIdx.x == 0) {
+      bool ok = true;
+      uint64_t t0 = 0;
+      for (int i = 0; i < n && ok; ++i) {
+        const uint64_t* f = p.part_flag + c_lo + unit + i;
+        for (uint32_t it = 0; ld_acquire_gpu_u64(f) != p.tag; ++it) {
+          __nanosleep(128);
+          if ((it & 63u) == 63u) {
+            const uint64_t now = globaltimer_ns();
+            if (t0 == 0) t0 = now;
+            else if (now - t0 > kWaitTimeoutNs) {
+              ok = false;
+              break;
+            }
+          }
+        }
+      }
+      if (!ok && p.status != nullptr) atomicAdd(p.status + 2, 1);
+      ready = ok ? 1 : 0;
+    }
+    __syncthreads();
+    if (!ready) return;
+  }
   const float2* ml_base = reinterpret_cast<const float2*>(p.part_ml) + (c_lo + unit) * NH + h;
   const float4* o_base = reinterpret_cast<const float4*>(p.part_o + ((c_lo + unit) * NH + h) * (int64_t)kLatent) + 2 * d8;
   constexpr int64_t kSlotO = (int64_t)NH * kLatent / 4;   // float4 stride between slots
@@ -1091,9 +1148,9 @@ __global__ void __launch_bounds__(512) merge_kernel(const DecodeParams p) {
 #pragma unroll
     for (int i = 0; i < kMax; ++i) {
       const bool in = i < n;
-      ml[i] = in ? ml_base[(int64_t)i * NH] : make_float2(kNegInf, 0.f);
-      o0[i] = in ? o_base[(int64_t)i * kSlotO] : make_float4(0.f, 0.f, 0.f, 0.f);
-      o1[i] = in ? o_base[(int64_t)i * kSlotO + 1] : make_float4(0.f, 0.f, 0.f, 0.f);
+      ml[i] = in ? ld_partial<kPoll>(ml_base + (int64_t)i * NH) : make_float2(kNegInf, 0.f);
+      o0[i] = in ? ld_partial<kPoll>(o_base + (int64_t)i * kSlotO) : make_float4(0.f, 0.f, 0.f, 0.f);
+      o1[i] = in ? ld_partial<kPoll>(o_base + (int64_t)i * kSlotO + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
     for (int i = 0; i < kMax; ++i)
@@ -1110,16 +1167,17 @@ __global__ void __launch_bounds__(512) merge_kernel(const DecodeParams p) {
     }
   } else {
     for (int i = 0; i < n; ++i) {
-      const float2 ml = ml_base[(int64_t)i * NH];
+      const float2 ml = ld_partial<kPoll>(ml_base + (int64_t)i * NH);
       if (ml.y > 0.f) mstar = fmaxf(mstar, ml.x);
     }
     if (mstar != kNegInf) {
       for (int i = 0; i < n; ++i) {
-        const float2 ml = ml_base[(int64_t)i * NH];
+        const float2 ml = ld_partial<kPoll>(ml_base + (int64_t)i * NH);
         if (!(ml.y > 0.f)) continue;
         const float w = exp2f(ml.x - mstar);
         lsum += w * ml.y;
-        const float4 o0 = o_base[(int64_t)i * kSlotO], o1 = o_base[(int64_t)i * kSlotO + 1];
+        const float4 o0 = ld_partial<kPoll>(o_base + (int64_t)i * kSlotO);
+        const float4 o1 = ld_partial<kPoll>(o_base + (int64_t)i * kSlotO + 1);
         a0.x += w * o0.x; a0.y += w * o0.y; a0.z += w * o0.z; a0.w += w * o0.w;
         a1.x += w * o1.x; a1.y += w * o1.y; a1.z += w * o1.z; a1.w += w * o1.w;
       }
@@ -1158,19 +1216,22 @@ static cudaLaunchAttribute pdl_attr() {
 // decode launch would keep the decode grid from starting while the prep grid runs).
 static cudaError_t set_attributes() {
   cudaError_t result = cudaSuccess;
-  const void* small[4] = {(const void*)q_prep_kernel<32>, (const void*)q_prep_kernel<16>,
-                          (const void*)merge_kernel<32>, (const void*)merge_kernel<16>};
+  const void* small[6] = {(const void*)q_prep_kernel<32>,        (const void*)q_prep_kernel<16>,
+                          (const void*)merge_kernel<32, false>, (const void*)merge_kernel<16, false>,
+                          (const void*)merge_kernel<32, true>,  (const void*)merge_kernel<16, true>};
   // The prep and merge grids ask for the same (maximum) shared-memory carveout as the decode grid,
   // so an SM does not have to be reconfigured between the three kernels.
   for (const void* f : small) {
     const cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess && result == cudaSuccess) result = e;
   }
-  const void* big[4] = {(const void*)decode_kernel<32, false>, (const void*)decode_kernel<32, true>,
-                        (const void*)decode_kernel<16, false>, (const void*)decode_kernel<16, true>};
-  const int bytes[4] = {(int)decode_smem_bytes<32>(), (int)decode_smem_bytes<32>(), (int)decode_smem_bytes<16>(),
-                        (int)decode_smem_bytes<16>()};
-  for (int i = 0; i < 4; ++i) {
+  const void* big[6] = {(const void*)decode_kernel<32, false, false>, (const void*)decode_kernel<32, false, true>,
+                        (const void*)decode_kernel<32, true, false>,  (const void*)decode_kernel<16, false, false>,
+                        (const void*)decode_kernel<16, false, true>,  (const void*)decode_kernel<16, true, false>};
+  const int bytes[6] = {(int)decode_smem_bytes<32>(), (int)decode_smem_bytes<32>(), (int)decode_smem_bytes<32>(),
+                        (int)decode_smem_bytes<16>(), (int)decode_smem_bytes<16>(), (int)decode_smem_bytes<16>()};
+  static_assert(sizeof(big) / sizeof(big[0]) == sizeof(bytes) / sizeof(bytes[0]), "one size per decode instance");
+  for (int i = 0; i < 6; ++i) {
     const cudaError_t e = cudaFuncSetAttribute(big[i], cudaFuncAttributeMaxDynamicSharedMemorySize, bytes[i]);
     if (e != cudaSuccess && result == cudaSuccess) result = e;
   }
@@ -1217,8 +1278,8 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream) {
     cudaLaunchAttribute attr[1] = {cluster_attr(p.cluster)};
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (h32) return cudaLaunchKernelEx(&cfg, decode_kernel<32, true>, p);
-    return cudaLaunchKernelEx(&cfg, decode_kernel<16, true>, p);
+    if (h32) return cudaLaunchKernelEx(&cfg, decode_kernel<32, true, false>, p);
+    return cudaLaunchKernelEx(&cfg, decode_kernel<16, true, false>, p);
   }
   if (h32) q_prep_kernel<32><<<(unsigned)p.units, 256, 0, stream>>>(p);
   else q_prep_kernel<16><<<(unsigned)p.units, 256, 0, stream>>>(p);
@@ -1232,8 +1293,12 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream) {
   cudaLaunchAttribute attr[1] = {pdl_attr()};
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (h32) return cudaLaunchKernelEx(&cfg, decode_kernel<32, false>, p);
-  return cudaLaunchKernelEx(&cfg, decode_kernel<16, false>, p);
+  if (p.merge_poll) {
+    if (h32) return cudaLaunchKernelEx(&cfg, decode_kernel<32, false, true>, p);
+    return cudaLaunchKernelEx(&cfg, decode_kernel<16, false, true>, p);
+  }
+  if (h32) return cudaLaunchKernelEx(&cfg, decode_kernel<32, false, false>, p);
+  return cudaLaunchKernelEx(&cfg, decode_kernel<16, false, false>, p);
 }
 
 int max_active_clusters(int heads_per_cta, int cluster) {
@@ -1254,8 +1319,8 @@ int max_active_clusters(int heads_per_cta, int cluster) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  const cudaError_t e = hi ? cudaOccupancyMaxActiveClusters(&n, decode_kernel<32, true>, &cfg)
-                           : cudaOccupancyMaxActiveClusters(&n, decode_kernel<16, true>, &cfg);
+  const cudaError_t e = hi ? cudaOccupancyMaxActiveClusters(&n, decode_kernel<32, true, false>, &cfg)
+                           : cudaOccupancyMaxActiveClusters(&n, decode_kernel<16, true, false>, &cfg);
   if (e != cudaSuccess) {
     (void)cudaGetLastError();
     n = 0;
@@ -1273,8 +1338,12 @@ cudaError_t launch_merge(const DecodeParams& p, cudaStream_t stream) {
   cudaLaunchAttribute attr[1] = {pdl_attr()};
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (p.heads_per_cta == 32) return cudaLaunchKernelEx(&cfg, merge_kernel<32>, p);
-  return cudaLaunchKernelEx(&cfg, merge_kernel<16>, p);
+  if (p.merge_poll) {
+    if (p.heads_per_cta == 32) return cudaLaunchKernelEx(&cfg, merge_kernel<32, true>, p);
+    return cudaLaunchKernelEx(&cfg, merge_kernel<16, true>, p);
+  }
+  if (p.heads_per_cta == 32) return cudaLaunchKernelEx(&cfg, merge_kernel<32, false>, p);
+  return cudaLaunchKernelEx(&cfg, merge_kernel<16, false>, p);
 }
 
 }  // namespace nvfp4mla

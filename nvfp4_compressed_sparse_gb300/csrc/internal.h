@@ -54,6 +54,9 @@ struct DecodeParams {
   float* part_ml;             // [slots, heads_per_cta, 2]  (running max in log2 units, sum)
   uint8_t* q16;               // [units, 9 * heads_per_cta * 128]: FP16 q image in UMMA B layout
   float* qscale;              // [units]: softmax_scale * log2(e) * 2^-e for the unit's q scaling
+  uint64_t* part_flag;        // [slots]: tag of the call whose partial the slot holds (stream-K)
+  uint64_t tag;               // this call's tag (unique per call in the process)
+  int merge_poll;             // 1 = the merge polls part_flag (results in host memory), else waits for the grid
   int32_t* status;            // optional
   int64_t units, total_tiles;
   int tiles_per_unit, ctas;

@@ -42,7 +42,7 @@ def test_status_strings(lib):
 
 def _ws(slots, units, nh):
     r = lambda x: (x + 255) // 256 * 256
-    return r(slots * nh * 512 * 4) + r(slots * nh * 2 * 4) + r(units * 9 * nh * 128) + r(units * 4)
+    return r(slots * nh * 512 * 4) + r(slots * nh * 2 * 4) + r(units * 9 * nh * 128) + r(units * 4) + r(slots * 8)
 
 
 def test_workspace_size_formula(lib):

@@ -1090,6 +1090,8 @@ __global__ void __launch_bounds__(256) q_prep_kernel(const DecodeParams p) {
 // as its unit's partials are tagged, so most of the results cross the host link while the last
 // decode CTAs still run; otherwise the block waits for the decode grid, which costs less than
 // the tags' fences when the results stay on the device.
+constexpr int kMergeThreads = 128;   // 64 threads per head; small blocks keep the grid in one wave
+
 // Partial loads: L2 only when polling (a slot is rewritten by every call, and only thread 0 of the
 // block performed the acquire); plain loads after the grid-completion wait.
 template <bool kPoll, class T>
@@ -1099,10 +1101,10 @@ __device__ __forceinline__ T ld_partial(const T* ptr) {
 }
 
 template <int NH, bool kPoll>
-__global__ void __launch_bounds__(512) merge_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeParams p) {
   if constexpr (!kPoll) asm volatile("griddepcontrol.wait;" ::: "memory");
   const int64_t unit = blockIdx.x;
-  const int h = blockIdx.y * 8 + (threadIdx.x >> 6);
+  const int h = blockIdx.y * (kMergeThreads / 64) + (threadIdx.x >> 6);
   const int d8 = threadIdx.x & 63;                 // dims 8*d8 .. 8*d8+7
   const int64_t g0 = unit * p.tiles_per_unit, g1 = g0 + p.tiles_per_unit - 1;
   const int64_t c_lo = ((g0 + 1) * p.ctas - 1) / p.total_tiles;
@@ -1331,8 +1333,8 @@ int max_active_clusters(int heads_per_cta, int cluster) {
 
 cudaError_t launch_merge(const DecodeParams& p, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)p.units, (unsigned)(p.heads_per_cta / 8), 1);
-  cfg.blockDim = dim3(512, 1, 1);
+  cfg.gridDim = dim3((unsigned)p.units, (unsigned)(p.heads_per_cta / (kMergeThreads / 64)), 1);
+  cfg.blockDim = dim3(kMergeThreads, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1] = {pdl_attr()};

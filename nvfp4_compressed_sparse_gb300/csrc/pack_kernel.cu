@@ -6,11 +6,15 @@
 // nibble of byte i), 32 E4M3 block scales (one per 16 latent values), 64 E4M3
 // rope bytes.
 //
-// One warp per row. Lane l loads latent elements 8l..8l+7 and 256+8l..256+8l+7
-// (two 16-byte loads; the warp reads the 1 KB latent row fully coalesced) and
-// rope elements 2l, 2l+1. A 16-value block spans a lane pair, so one shuffle
-// gives the block amax. The row is assembled in shared memory and written with
-// 22 coalesced 16-byte stores.
+// One warp per row, two rows per warp in flight: every load of both rows (slot,
+// latent, rope) is issued before any is used, so a row costs one memory round
+// trip, not a slot load followed by the data loads. Lane l loads latent
+// elements 8l..8l+7 and 256+8l..256+8l+7 (two 16-byte loads; the warp reads
+// the 1 KB latent row fully coalesced) and rope elements 2l, 2l+1. A 16-value
+// block spans a lane pair, so one shuffle gives the block amax. The row is
+// assembled in shared memory and written with 22 coalesced 16-byte stores.
+// Inputs and the cache rows are streamed (read or written once).
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include "internal.h"
@@ -29,6 +33,9 @@ __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 
 // without dividing: |x|/s vs a midpoint m is |x| vs m*s, and m*s is exact in
 // fp32 (m has <= 3 significant bits, s <= 4). Ties at 0.25, 1.25, 2.5, 5 go
 // down (even codes 0, 2, 4, 6); ties at 0.75, 1.75, 3.5 go up (codes 2, 4, 6).
+// The thresholds increase and each crossing test is monotonic in |x|, so the
+// code (the number of thresholds crossed) is found by binary search: three
+// compares instead of seven. NaN magnitudes cross none (code 0).
 struct Thresholds {
   float t0, t1, t2, t3, t4, t5, t6;
 };
@@ -38,13 +45,17 @@ __device__ __forceinline__ Thresholds make_thresholds(float s) {
     t.t0 = 0.25f * s; t.t1 = 0.75f * s; t.t2 = 1.25f * s; t.t3 = 1.75f * s;
     t.t4 = 2.5f * s;  t.t5 = 3.5f * s;  t.t6 = 5.0f * s;
   } else {
-    t.t0 = t.t1 = t.t2 = t.t3 = t.t4 = t.t5 = t.t6 = __int_as_float(0x7f800000);  // all magnitudes code 0
+    t.t0 = t.t1 = t.t2 = t.t3 = t.t4 = t.t5 = t.t6 = __int_as_float(0x7f800000);  // all finite magnitudes code 0
   }
   return t;
 }
 __device__ __forceinline__ uint32_t e2m1_code(float x, const Thresholds& t) {
   const float a = fabsf(x);
-  uint32_t c = (a > t.t0) + (a >= t.t1) + (a > t.t2) + (a >= t.t3) + (a > t.t4) + (a >= t.t5) + (a > t.t6);
+  const bool b2 = a >= t.t3;                        // codes 4..7
+  const bool b1 = a >= (b2 ? t.t5 : t.t1);          // codes 6..7 / 2..3
+  const float tb = b2 ? (b1 ? t.t6 : t.t4) : (b1 ? t.t2 : t.t0);
+  const bool b0 = a > tb;
+  const uint32_t c = (b2 ? 4u : 0u) | (b1 ? 2u : 0u) | (b0 ? 1u : 0u);
   return c | ((__float_as_uint(x) >> 28) & 8u);
 }
 // 8 bf16 (one uint4) -> 8 nibbles (one 32-bit word), element 0 in bits 0..3.
@@ -58,17 +69,21 @@ __device__ __forceinline__ uint32_t encode8(const uint4& v, const Thresholds& t)
   }
   return out;
 }
+// max |x| of 8 bf16 (exact: bf16 abs and max, two lanes per instruction; a NaN loses to the other
+// operand, as with fmaxf)
 __device__ __forceinline__ float amax8(const uint4& v) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  float m = 0.f;
+  __nv_bfloat162 m = __habs2(*reinterpret_cast<const __nv_bfloat162*>(&w[0]));
 #pragma unroll
-  for (int i = 0; i < 4; ++i) m = fmaxf(m, fmaxf(fabsf(bf_lo(w[i])), fabsf(bf_hi(w[i]))));
-  return m;
+  for (int i = 1; i < 4; ++i) m = __hmax2(m, __habs2(*reinterpret_cast<const __nv_bfloat162*>(&w[i])));
+  return fmaxf(fmaxf(__low2float(m), __high2float(m)), 0.f);
 }
 __device__ __forceinline__ float e4m3_to_f32(uint32_t byte) {
   const uint32_t h2 = ptx::e4m3x2_to_f16x2(byte & 0xFFu);
   return __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
 }
+
+constexpr int kRowsPerWarp = 2;
 
 __global__ void __launch_bounds__(kWarpsPerBlock * 32) pack_kernel(
     const uint16_t* __restrict__ latent, int64_t lstride, const uint16_t* __restrict__ rope, int64_t rstride,
@@ -78,42 +93,56 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) pack_kernel(
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint8_t* srow = stage[warp];
   const int64_t nslots = num_pages * kPageTokens;
-  for (int64_t row = (int64_t)blockIdx.x * kWarpsPerBlock + warp; row < n;
-       row += (int64_t)gridDim.x * kWarpsPerBlock) {
-    const int64_t slot = __ldg(slots + row);
-    if (slot < 0 || slot >= nslots) {
-      if (slot != -1 && lane == 0 && status != nullptr) atomicAdd(status + 3, 1);
-      continue;
+  for (int64_t row0 = ((int64_t)blockIdx.x * kWarpsPerBlock + warp) * kRowsPerWarp; row0 < n;
+       row0 += (int64_t)gridDim.x * kWarpsPerBlock * kRowsPerWarp) {
+    int64_t slot_v[kRowsPerWarp];
+    uint4 a_v[kRowsPerWarp], b_v[kRowsPerWarp];
+    uint32_t r_v[kRowsPerWarp];
+#pragma unroll
+    for (int i = 0; i < kRowsPerWarp; ++i) {
+      const int64_t row = row0 + i;
+      const bool in = row < n;
+      const uint16_t* lp = latent + (in ? row : 0) * lstride;
+      slot_v[i] = in ? __ldcs(slots + row) : -1;
+      a_v[i] = in ? __ldcs(reinterpret_cast<const uint4*>(lp) + lane) : make_uint4(0u, 0u, 0u, 0u);         // 8l..8l+7
+      b_v[i] = in ? __ldcs(reinterpret_cast<const uint4*>(lp + 256) + lane) : make_uint4(0u, 0u, 0u, 0u);   // 256+8l..
+      r_v[i] = in ? __ldcs(reinterpret_cast<const unsigned int*>(rope + row * rstride) + lane) : 0u;
     }
-    const uint16_t* lp = latent + row * lstride;
-    const uint4 a = __ldg(reinterpret_cast<const uint4*>(lp) + lane);         // elements 8l..8l+7
-    const uint4 b = __ldg(reinterpret_cast<const uint4*>(lp + 256) + lane);   // elements 256+8l..
-    const uint32_t r = __ldg(reinterpret_cast<const uint32_t*>(rope + row * rstride) + lane);
+#pragma unroll
+    for (int i = 0; i < kRowsPerWarp; ++i) {
+      const int64_t slot = slot_v[i];
+      if (slot < 0 || slot >= nslots) {
+        if (slot != -1 && lane == 0 && status != nullptr) atomicAdd(status + 3, 1);
+        continue;
+      }
+      const uint4 a = a_v[i], b = b_v[i];
+      const uint32_t r = r_v[i];
 
-    // block amax: blocks (l>>1) and 16+(l>>1) span lanes 2m, 2m+1
-    float ma = amax8(a), mb = amax8(b);
-    ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, 1));
-    mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
-    // scale = E4M3_rn_sat(amax / 6); IEEE division, then one rounding to E4M3
-    const uint32_t sc = ptx::f32x2_to_e4m3x2(__fdiv_rn(ma, 6.0f), __fdiv_rn(mb, 6.0f));
-    const Thresholds ta = make_thresholds(e4m3_to_f32(sc & 0xFFu));
-    const Thresholds tb = make_thresholds(e4m3_to_f32(sc >> 8));
-    const uint32_t wa = encode8(a, ta), wb = encode8(b, tb);
-    const uint32_t rr = ptx::f32x2_to_e4m3x2(bf_lo(r), bf_hi(r));
+      // block amax: blocks (l>>1) and 16+(l>>1) span lanes 2m, 2m+1
+      float ma = amax8(a), mb = amax8(b);
+      ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, 1));
+      mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
+      // scale = E4M3_rn_sat(amax / 6); IEEE division, then one rounding to E4M3
+      const uint32_t sc = ptx::f32x2_to_e4m3x2(__fdiv_rn(ma, 6.0f), __fdiv_rn(mb, 6.0f));
+      const Thresholds ta = make_thresholds(e4m3_to_f32(sc & 0xFFu));
+      const Thresholds tb = make_thresholds(e4m3_to_f32(sc >> 8));
+      const uint32_t wa = encode8(a, ta), wb = encode8(b, tb);
+      const uint32_t rr = ptx::f32x2_to_e4m3x2(bf_lo(r), bf_hi(r));
 
-    *reinterpret_cast<uint32_t*>(srow + 4 * lane) = wa;
-    *reinterpret_cast<uint32_t*>(srow + 128 + 4 * lane) = wb;
-    if ((lane & 1) == 0) {
-      srow[kScaleOff + (lane >> 1)] = (uint8_t)(sc & 0xFFu);
-      srow[kScaleOff + 16 + (lane >> 1)] = (uint8_t)(sc >> 8);
+      *reinterpret_cast<uint32_t*>(srow + 4 * lane) = wa;
+      *reinterpret_cast<uint32_t*>(srow + 128 + 4 * lane) = wb;
+      if ((lane & 1) == 0) {
+        srow[kScaleOff + (lane >> 1)] = (uint8_t)(sc & 0xFFu);
+        srow[kScaleOff + 16 + (lane >> 1)] = (uint8_t)(sc >> 8);
+      }
+      *reinterpret_cast<uint16_t*>(srow + kRopeOff + 2 * lane) = (uint16_t)rr;
+      __syncwarp();
+      if (lane < kRowBytes / 16) {
+        const uint4 v = *reinterpret_cast<const uint4*>(srow + 16 * lane);
+        __stcs(reinterpret_cast<uint4*>(cache + slot * kRowBytes + 16 * lane), v);
+      }
+      __syncwarp();
     }
-    *reinterpret_cast<uint16_t*>(srow + kRopeOff + 2 * lane) = (uint16_t)rr;
-    __syncwarp();
-    if (lane < kRowBytes / 16) {
-      const uint4 v = *reinterpret_cast<const uint4*>(srow + 16 * lane);
-      *reinterpret_cast<uint4*>(cache + slot * kRowBytes + 16 * lane) = v;
-    }
-    __syncwarp();
   }
 }
 
@@ -123,8 +152,18 @@ cudaError_t launch_pack(const uint16_t* latent, int64_t lstride, const uint16_t*
                         const int64_t* slots, int64_t n, uint8_t* cache, int64_t num_pages, int32_t* status,
                         cudaStream_t stream) {
   const int sms = device_sm_count();
-  const int64_t want = (n + kWarpsPerBlock - 1) / kWarpsPerBlock;
-  const int64_t cap = (int64_t)(sms > 0 ? sms : 148) * 8;   // 8 blocks of 8 warps per SM
+  // one resident wave of blocks, each striding over the rows
+  static int per_sm = 0;
+  if (per_sm == 0) {
+    int b = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, pack_kernel, kWarpsPerBlock * 32, 0) != cudaSuccess || b < 1) {
+      (void)cudaGetLastError();
+      b = 2;
+    }
+    per_sm = b;
+  }
+  const int64_t want = (n + kWarpsPerBlock * kRowsPerWarp - 1) / (kWarpsPerBlock * kRowsPerWarp);
+  const int64_t cap = (int64_t)(sms > 0 ? sms : 148) * per_sm;
   const int grid = (int)(want < cap ? want : cap);
   pack_kernel<<<grid, kWarpsPerBlock * 32, 0, stream>>>(latent, lstride, rope, rstride, slots, n, cache,
                                                          num_pages, status);

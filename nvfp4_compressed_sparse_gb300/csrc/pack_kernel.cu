@@ -17,6 +17,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <atomic>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -152,15 +154,17 @@ cudaError_t launch_pack(const uint16_t* latent, int64_t lstride, const uint16_t*
                         const int64_t* slots, int64_t n, uint8_t* cache, int64_t num_pages, int32_t* status,
                         cudaStream_t stream) {
   const int sms = device_sm_count();
-  // one resident wave of blocks, each striding over the rows
-  static int per_sm = 0;
+  // one resident wave of blocks, each striding over the rows (the occupancy is the same on every
+  // device of this build's architecture; concurrent first calls store the same value)
+  static std::atomic<int> cached_per_sm{0};
+  int per_sm = cached_per_sm.load(std::memory_order_relaxed);
   if (per_sm == 0) {
-    int b = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, pack_kernel, kWarpsPerBlock * 32, 0) != cudaSuccess || b < 1) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pack_kernel, kWarpsPerBlock * 32, 0) != cudaSuccess ||
+        per_sm < 1) {
       (void)cudaGetLastError();
-      b = 2;
+      per_sm = 2;
     }
-    per_sm = b;
+    cached_per_sm.store(per_sm, std::memory_order_relaxed);
   }
   const int64_t want = (n + kWarpsPerBlock * kRowsPerWarp - 1) / (kWarpsPerBlock * kRowsPerWarp);
   const int64_t cap = (int64_t)(sms > 0 ? sms : 148) * per_sm;

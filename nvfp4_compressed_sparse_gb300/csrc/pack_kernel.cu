@@ -37,39 +37,45 @@ __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 
 // down (even codes 0, 2, 4, 6); ties at 0.75, 1.75, 3.5 go up (codes 2, 4, 6).
 // The thresholds increase and each crossing test is monotonic in |x|, so the
 // code (the number of thresholds crossed) is found by binary search: three
-// compares instead of seven. NaN magnitudes cross none (code 0).
+// compares instead of seven. The search runs on bf16 pairs (two values per
+// instruction): x is bf16 and every threshold m*s has at most 7 significant
+// bits (s >= 2^-9), so it is exact in bf16 and the comparisons are exact. NaN
+// magnitudes cross none (code 0).
 struct Thresholds {
-  float t0, t1, t2, t3, t4, t5, t6;
+  uint32_t t0, t1, t2, t3, t4, t5, t6;   // m*s as a bf16 pair (both halves equal)
 };
+__device__ __forceinline__ uint32_t bf16_pair(float f) {
+  const uint32_t b = __float_as_uint(f) >> 16;   // exact: the low 16 bits of m*s are zero
+  return b | (b << 16);
+}
 __device__ __forceinline__ Thresholds make_thresholds(float s) {
   Thresholds t;
   if (s > 0.f) {
-    t.t0 = 0.25f * s; t.t1 = 0.75f * s; t.t2 = 1.25f * s; t.t3 = 1.75f * s;
-    t.t4 = 2.5f * s;  t.t5 = 3.5f * s;  t.t6 = 5.0f * s;
+    t.t0 = bf16_pair(0.25f * s); t.t1 = bf16_pair(0.75f * s); t.t2 = bf16_pair(1.25f * s);
+    t.t3 = bf16_pair(1.75f * s); t.t4 = bf16_pair(2.5f * s);  t.t5 = bf16_pair(3.5f * s);
+    t.t6 = bf16_pair(5.0f * s);
   } else {
-    t.t0 = t.t1 = t.t2 = t.t3 = t.t4 = t.t5 = t.t6 = __int_as_float(0x7f800000);  // all finite magnitudes code 0
+    t.t0 = t.t1 = t.t2 = t.t3 = t.t4 = t.t5 = t.t6 = 0x7F807F80u;   // +inf: all finite magnitudes code 0
   }
   return t;
 }
-__device__ __forceinline__ uint32_t e2m1_code(float x, const Thresholds& t) {
-  const float a = fabsf(x);
-  const bool b2 = a >= t.t3;                        // codes 4..7
-  const bool b1 = a >= (b2 ? t.t5 : t.t1);          // codes 6..7 / 2..3
-  const float tb = b2 ? (b1 ? t.t6 : t.t4) : (b1 ? t.t2 : t.t0);
-  const bool b0 = a > tb;
-  const uint32_t c = (b2 ? 4u : 0u) | (b1 ? 2u : 0u) | (b0 ? 1u : 0u);
-  return c | ((__float_as_uint(x) >> 28) & 8u);
+__device__ __forceinline__ __nv_bfloat162 as_bf2(uint32_t u) { return *reinterpret_cast<const __nv_bfloat162*>(&u); }
+__device__ __forceinline__ uint32_t pick(uint32_t mask, uint32_t if_set, uint32_t if_clear) {
+  return (mask & if_set) | (~mask & if_clear);
+}
+// e2m1 codes of the bf16 pair w (element in bits 0..15 -> nibble 0, bits 16..31 -> nibble 1)
+__device__ __forceinline__ uint32_t e2m1_pair(uint32_t w, const Thresholds& t) {
+  const __nv_bfloat162 a = as_bf2(w & 0x7FFF7FFFu);
+  const uint32_t b2 = __hge2_mask(a, as_bf2(t.t3));                       // codes 4..7
+  const uint32_t b1 = __hge2_mask(a, as_bf2(pick(b2, t.t5, t.t1)));      // 6..7 / 2..3
+  const uint32_t tb = pick(b2, pick(b1, t.t6, t.t4), pick(b1, t.t2, t.t0));
+  const uint32_t b0 = __hgt2_mask(a, as_bf2(tb));
+  const uint32_t c = (b2 & 0x00040004u) | (b1 & 0x00020002u) | (b0 & 0x00010001u);   // per half
+  return (c & 0x7u) | ((c >> 12) & 0x70u) | ((w >> 12) & 0x8u) | ((w >> 24) & 0x80u);   // + sign bits
 }
 // 8 bf16 (one uint4) -> 8 nibbles (one 32-bit word), element 0 in bits 0..3.
 __device__ __forceinline__ uint32_t encode8(const uint4& v, const Thresholds& t) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  uint32_t out = 0;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    out |= e2m1_code(bf_lo(w[i]), t) << (8 * i);
-    out |= e2m1_code(bf_hi(w[i]), t) << (8 * i + 4);
-  }
-  return out;
+  return e2m1_pair(v.x, t) | (e2m1_pair(v.y, t) << 8) | (e2m1_pair(v.z, t) << 16) | (e2m1_pair(v.w, t) << 24);
 }
 // max |x| of 8 bf16 (exact: bf16 abs and max, two lanes per instruction; a NaN loses to the other
 // operand, as with fmaxf)
@@ -87,7 +93,7 @@ __device__ __forceinline__ float e4m3_to_f32(uint32_t byte) {
 
 constexpr int kRowsPerWarp = 2;
 
-__global__ void __launch_bounds__(kWarpsPerBlock * 32) pack_kernel(
+__global__ void __launch_bounds__(kWarpsPerBlock * 32, 4) pack_kernel(
     const uint16_t* __restrict__ latent, int64_t lstride, const uint16_t* __restrict__ rope, int64_t rstride,
     const int64_t* __restrict__ slots, int64_t n, uint8_t* __restrict__ cache, int64_t num_pages,
     int32_t* __restrict__ status) {

@@ -207,15 +207,15 @@ def barrier(world):
 def run_reference(args, world, rank):
     if rank != 0:
         return None
-    import numpy as np
     steps, warm = args.steps, args.warmup
     # bounded sample per step: one query token (2,048 rows), scaled to the 64-token step
     per_step_units = 1
-    tot = cpu_baseline_sample(max(1, warm)) if warm > 0 else None  # warm-up (imports, caches)
+    if warm > 0:
+        cpu_baseline_sample(warm)   # warm-up (imports, caches)
     t = cpu_baseline_sample(steps * per_step_units)
     value = t["value"]
     return {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "us/step", "n_gpus": args.gpus,
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "us/step", "n_gpus": world,
         "steps": steps, "warmup": warm, "ms_per_step": value / 1000.0, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": WORKLOAD, "sample": "one query token per step"},

@@ -1100,6 +1100,48 @@ __device__ __forceinline__ T ld_partial(const T* ptr) {
   else return *ptr;
 }
 
+// Fold partial slots base .. base+3 (those below n) of one (unit, head) into the running
+// (max, sum, O) of the merge: max and sum in log2 units, O unnormalised.
+constexpr int kMergeChunk = 4;
+template <int NH, bool kPoll>
+__device__ __forceinline__ void merge_chunk(const float2* ml_base, const float4* o_base, int base, int n, float& mstar,
+                                            float& lsum, float4& a0, float4& a1) {
+  constexpr int64_t kSlotO = (int64_t)NH * kLatent / 4;   // float4 stride between slots
+  const float kNegInf = __int_as_float(0xff800000);
+  float2 ml[kMergeChunk];
+  float4 o0[kMergeChunk], o1[kMergeChunk];
+#pragma unroll
+  for (int i = 0; i < kMergeChunk; ++i) {
+    const bool in = base + i < n;
+    const int64_t s = base + i;
+    ml[i] = in ? ld_partial<kPoll>(ml_base + s * NH) : make_float2(kNegInf, 0.f);
+    o0[i] = in ? ld_partial<kPoll>(o_base + s * kSlotO) : make_float4(0.f, 0.f, 0.f, 0.f);
+    o1[i] = in ? ld_partial<kPoll>(o_base + s * kSlotO + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  float cmax = kNegInf;
+#pragma unroll
+  for (int i = 0; i < kMergeChunk; ++i)
+    if (ml[i].y > 0.f) cmax = fmaxf(cmax, ml[i].x);
+  if (cmax == kNegInf) return;
+  if (cmax > mstar) {
+    if (mstar != kNegInf) {
+      const float r = exp2f(mstar - cmax);
+      lsum *= r;
+      a0.x *= r; a0.y *= r; a0.z *= r; a0.w *= r;
+      a1.x *= r; a1.y *= r; a1.z *= r; a1.w *= r;
+    }
+    mstar = cmax;
+  }
+#pragma unroll
+  for (int i = 0; i < kMergeChunk; ++i) {
+    if (!(ml[i].y > 0.f)) continue;
+    const float w = exp2f(ml[i].x - mstar);
+    lsum += w * ml[i].y;
+    a0.x += w * o0[i].x; a0.y += w * o0[i].y; a0.z += w * o0[i].z; a0.w += w * o0[i].w;
+    a1.x += w * o1[i].x; a1.y += w * o1[i].y; a1.z += w * o1[i].z; a1.w += w * o1[i].w;
+  }
+}
+
 template <int NH, bool kPoll>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeParams p) {
   if constexpr (!kPoll) asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -1140,51 +1182,15 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeParams
   }
   const float2* ml_base = reinterpret_cast<const float2*>(p.part_ml) + (c_lo + unit) * NH + h;
   const float4* o_base = reinterpret_cast<const float4*>(p.part_o + ((c_lo + unit) * NH + h) * (int64_t)kLatent) + 2 * d8;
-  constexpr int64_t kSlotO = (int64_t)NH * kLatent / 4;   // float4 stride between slots
   float mstar = kNegInf, lsum = 0.f;
   float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
-  constexpr int kMax = 4;
-  if (n <= kMax) {
-    float2 ml[kMax];
-    float4 o0[kMax], o1[kMax];
-#pragma unroll
-    for (int i = 0; i < kMax; ++i) {
-      const bool in = i < n;
-      ml[i] = in ? ld_partial<kPoll>(ml_base + (int64_t)i * NH) : make_float2(kNegInf, 0.f);
-      o0[i] = in ? ld_partial<kPoll>(o_base + (int64_t)i * kSlotO) : make_float4(0.f, 0.f, 0.f, 0.f);
-      o1[i] = in ? ld_partial<kPoll>(o_base + (int64_t)i * kSlotO + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-#pragma unroll
-    for (int i = 0; i < kMax; ++i)
-      if (ml[i].y > 0.f) mstar = fmaxf(mstar, ml[i].x);
-    if (mstar != kNegInf) {
-#pragma unroll
-      for (int i = 0; i < kMax; ++i) {
-        if (!(ml[i].y > 0.f)) continue;
-        const float w = exp2f(ml[i].x - mstar);
-        lsum += w * ml[i].y;
-        a0.x += w * o0[i].x; a0.y += w * o0[i].y; a0.z += w * o0[i].z; a0.w += w * o0[i].w;
-        a1.x += w * o1[i].x; a1.y += w * o1[i].y; a1.z += w * o1[i].z; a1.w += w * o1[i].w;
-      }
-    }
-  } else {
-    for (int i = 0; i < n; ++i) {
-      const float2 ml = ld_partial<kPoll>(ml_base + (int64_t)i * NH);
-      if (ml.y > 0.f) mstar = fmaxf(mstar, ml.x);
-    }
-    if (mstar != kNegInf) {
-      for (int i = 0; i < n; ++i) {
-        const float2 ml = ld_partial<kPoll>(ml_base + (int64_t)i * NH);
-        if (!(ml.y > 0.f)) continue;
-        const float w = exp2f(ml.x - mstar);
-        lsum += w * ml.y;
-        const float4 o0 = ld_partial<kPoll>(o_base + (int64_t)i * kSlotO);
-        const float4 o1 = ld_partial<kPoll>(o_base + (int64_t)i * kSlotO + 1);
-        a0.x += w * o0.x; a0.y += w * o0.y; a0.z += w * o0.z; a0.w += w * o0.w;
-        a1.x += w * o1.x; a1.y += w * o1.y; a1.z += w * o1.z; a1.w += w * o1.w;
-      }
-    }
-  }
+  // Slots in chunks of four, every load of a chunk issued before any is used; the running sums are
+  // rescaled when a later chunk raises the maximum, so a unit split over many CTAs costs one L2
+  // round trip per chunk instead of one per slot. (One chunk, the usual case, is its own copy:
+  // with the chunk base fixed at 0 the loads and their predicates are set up ahead.)
+  if (n <= kMergeChunk) merge_chunk<NH, kPoll>(ml_base, o_base, 0, n, mstar, lsum, a0, a1);
+  else
+    for (int base = 0; base < n; base += kMergeChunk) merge_chunk<NH, kPoll>(ml_base, o_base, base, n, mstar, lsum, a0, a1);
   int b, j, hg;
   split_unit(p, unit, b, j, hg);
   const int64_t row = ((int64_t)b * p.Q + j) * p.H + (int64_t)hg * NH + h;

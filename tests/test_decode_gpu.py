@@ -253,6 +253,24 @@ def test_pinned_host_buffers_match_device_buffers(kw):
     assert_close(hout, hlse, ref_out, ref_lse, f"host buffers {kw}")
 
 
+@pytest.mark.parametrize("H", [16, 128])
+def test_host_q_alone_matches_device_q(H):
+    """q in page-locked host memory alone (its prep grid then splits every unit over a cluster of
+    CTAs that share the unit's maximum): bitwise the device-q result, for one and several head
+    groups."""
+    case = workloads.small_case(B=2, Q=3, H=H, topk=260, L=(1300, 2100), seed=40 + H)
+    lat, rope, rows = _host_cache(case)
+    cache = _gpu_cache(lat, rope, case.num_pages)
+    q, pt, tk, sl = decode_inputs(case)
+    out_d, lse_d = m.sparse_mla_decode(q, cache, pt, tk, sl, case.softmax_scale)
+    out_h, lse_h = m.sparse_mla_decode(q.cpu().pin_memory(), cache, pt, tk, sl, case.softmax_scale)
+    torch.cuda.synchronize()
+    assert torch.equal(out_d, out_h) and torch.equal(lse_d, lse_h)
+    ref_out, ref_lse = attention.sparse_decode(case.q_bits, rows, case.page_table, case.topk_indices,
+                                               case.seq_lens, case.softmax_scale)
+    assert_close(out_h, lse_h, ref_out, ref_lse, f"host q H={H}")
+
+
 def test_pageable_host_memory_is_rejected_before_launch():
     import ctypes
     case = workloads.small_case(B=1, Q=1, H=32, topk=128, L=(900,), seed=5)

@@ -97,9 +97,8 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, 4) pack_kernel(
     const uint16_t* __restrict__ latent, int64_t lstride, const uint16_t* __restrict__ rope, int64_t rstride,
     const int64_t* __restrict__ slots, int64_t n, uint8_t* __restrict__ cache, int64_t num_pages,
     int32_t* __restrict__ status) {
-  __shared__ __align__(16) uint8_t stage[kWarpsPerBlock][kRowBytes];
+  __shared__ __align__(16) uint8_t stage[kWarpsPerBlock][kRowsPerWarp][kRowBytes];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  uint8_t* srow = stage[warp];
   const int64_t nslots = num_pages * kPageTokens;
   for (int64_t row0 = ((int64_t)blockIdx.x * kWarpsPerBlock + warp) * kRowsPerWarp; row0 < n;
        row0 += (int64_t)gridDim.x * kWarpsPerBlock * kRowsPerWarp) {
@@ -116,13 +115,11 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, 4) pack_kernel(
       b_v[i] = in ? __ldcs(reinterpret_cast<const uint4*>(lp + 256) + lane) : make_uint4(0u, 0u, 0u, 0u);   // 256+8l..
       r_v[i] = in ? __ldcs(reinterpret_cast<const unsigned int*>(rope + row * rstride) + lane) : 0u;
     }
+    // Both rows are encoded as straight-line code (a row whose slot is skipped is encoded too
+    // and not stored), so the two rows' arithmetic can interleave.
 #pragma unroll
     for (int i = 0; i < kRowsPerWarp; ++i) {
-      const int64_t slot = slot_v[i];
-      if (slot < 0 || slot >= nslots) {
-        if (slot != -1 && lane == 0 && status != nullptr) atomicAdd(status + 3, 1);
-        continue;
-      }
+      uint8_t* srow = stage[warp][i];
       const uint4 a = a_v[i], b = b_v[i];
       const uint32_t r = r_v[i];
 
@@ -144,13 +141,21 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, 4) pack_kernel(
         srow[kScaleOff + 16 + (lane >> 1)] = (uint8_t)(sc >> 8);
       }
       *reinterpret_cast<uint16_t*>(srow + kRopeOff + 2 * lane) = (uint16_t)rr;
-      __syncwarp();
+    }
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < kRowsPerWarp; ++i) {
+      const int64_t slot = slot_v[i];
+      if (slot < 0 || slot >= nslots) {
+        if (slot != -1 && lane == 0 && status != nullptr) atomicAdd(status + 3, 1);
+        continue;
+      }
       if (lane < kRowBytes / 16) {
-        const uint4 v = *reinterpret_cast<const uint4*>(srow + 16 * lane);
+        const uint4 v = *reinterpret_cast<const uint4*>(stage[warp][i] + 16 * lane);
         __stcs(reinterpret_cast<uint4*>(cache + slot * kRowBytes + 16 * lane), v);
       }
-      __syncwarp();
     }
+    __syncwarp();
   }
 }
 

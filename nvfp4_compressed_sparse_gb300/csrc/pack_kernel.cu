@@ -45,21 +45,23 @@ struct Thresholds {
   uint32_t t0, t1, t2, t3, t4, t5, t6;   // m*s as a bf16 pair (both halves equal)
 };
 __device__ __forceinline__ uint32_t bf16_pair(float f) {
-  const uint32_t b = __float_as_uint(f) >> 16;   // exact: the low 16 bits of m*s are zero
+  const uint32_t b = __float_as_uint(f) >> 16;   // exact for E4M3 values: their low 16 bits are zero
   return b | (b << 16);
 }
+__device__ __forceinline__ __nv_bfloat162 as_bf2(uint32_t u) { return *reinterpret_cast<const __nv_bfloat162*>(&u); }
+__device__ __forceinline__ uint32_t as_u32(__nv_bfloat162 v) { return *reinterpret_cast<const uint32_t*>(&v); }
+// m*s for the seven midpoints m, two lanes per bf16 multiply: s (an E4M3 value, <= 4 significant
+// bits) is exact in bf16 and so is every product (<= 7 bits, within [2^-11, 2240]). A zero scale
+// becomes +inf, so every finite magnitude codes 0.
 __device__ __forceinline__ Thresholds make_thresholds(float s) {
-  Thresholds t;
-  if (s > 0.f) {
-    t.t0 = bf16_pair(0.25f * s); t.t1 = bf16_pair(0.75f * s); t.t2 = bf16_pair(1.25f * s);
-    t.t3 = bf16_pair(1.75f * s); t.t4 = bf16_pair(2.5f * s);  t.t5 = bf16_pair(3.5f * s);
-    t.t6 = bf16_pair(5.0f * s);
-  } else {
-    t.t0 = t.t1 = t.t2 = t.t3 = t.t4 = t.t5 = t.t6 = 0x7F807F80u;   // +inf: all finite magnitudes code 0
-  }
+  const __nv_bfloat162 s2 = as_bf2(s > 0.f ? bf16_pair(s) : 0x7F807F80u);
+  Thresholds t;   // midpoints 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5 as bf16 pairs
+  t.t0 = as_u32(__hmul2(s2, as_bf2(0x3E803E80u))); t.t1 = as_u32(__hmul2(s2, as_bf2(0x3F403F40u)));
+  t.t2 = as_u32(__hmul2(s2, as_bf2(0x3FA03FA0u))); t.t3 = as_u32(__hmul2(s2, as_bf2(0x3FE03FE0u)));
+  t.t4 = as_u32(__hmul2(s2, as_bf2(0x40204020u))); t.t5 = as_u32(__hmul2(s2, as_bf2(0x40604060u)));
+  t.t6 = as_u32(__hmul2(s2, as_bf2(0x40A040A0u)));
   return t;
 }
-__device__ __forceinline__ __nv_bfloat162 as_bf2(uint32_t u) { return *reinterpret_cast<const __nv_bfloat162*>(&u); }
 __device__ __forceinline__ uint32_t pick(uint32_t mask, uint32_t if_set, uint32_t if_clear) {
   return (mask & if_set) | (~mask & if_clear);
 }

@@ -65,19 +65,22 @@ __device__ __forceinline__ Thresholds make_thresholds(float s) {
 __device__ __forceinline__ uint32_t pick(uint32_t mask, uint32_t if_set, uint32_t if_clear) {
   return (mask & if_set) | (~mask & if_clear);
 }
-// e2m1 codes of the bf16 pair w (element in bits 0..15 -> nibble 0, bits 16..31 -> nibble 1)
+// e2m1 codes (with sign bits) of the bf16 pair w, one per half: the element in bits 0..15 gives
+// the nibble in bits 0..3, the element in bits 16..31 the nibble in bits 16..19.
 __device__ __forceinline__ uint32_t e2m1_pair(uint32_t w, const Thresholds& t) {
   const __nv_bfloat162 a = as_bf2(w & 0x7FFF7FFFu);
   const uint32_t b2 = __hge2_mask(a, as_bf2(t.t3));                       // codes 4..7
   const uint32_t b1 = __hge2_mask(a, as_bf2(pick(b2, t.t5, t.t1)));      // 6..7 / 2..3
-  const uint32_t tb = pick(b2, pick(b1, t.t6, t.t4), pick(b1, t.t2, t.t0));
+  const uint32_t tb = pick(b1, pick(b2, t.t6, t.t2), pick(b2, t.t4, t.t0));
   const uint32_t b0 = __hgt2_mask(a, as_bf2(tb));
-  const uint32_t c = (b2 & 0x00040004u) | (b1 & 0x00020002u) | (b0 & 0x00010001u);   // per half
-  return (c & 0x7u) | ((c >> 12) & 0x70u) | ((w >> 12) & 0x8u) | ((w >> 24) & 0x80u);   // + sign bits
+  return (b2 & 0x00040004u) | (b1 & 0x00020002u) | (b0 & 0x00010001u) | ((w >> 12) & 0x00080008u);
 }
-// 8 bf16 (one uint4) -> 8 nibbles (one 32-bit word), element 0 in bits 0..3.
+// 8 bf16 (one uint4) -> 8 nibbles (one 32-bit word), element 0 in bits 0..3: each pair folds its
+// two nibbles into its low byte (c | c >> 12), and byte permutes gather the four bytes.
 __device__ __forceinline__ uint32_t encode8(const uint4& v, const Thresholds& t) {
-  return e2m1_pair(v.x, t) | (e2m1_pair(v.y, t) << 8) | (e2m1_pair(v.z, t) << 16) | (e2m1_pair(v.w, t) << 24);
+  const uint32_t c0 = e2m1_pair(v.x, t), c1 = e2m1_pair(v.y, t), c2 = e2m1_pair(v.z, t), c3 = e2m1_pair(v.w, t);
+  const uint32_t x0 = c0 | (c0 >> 12), x1 = c1 | (c1 >> 12), x2 = c2 | (c2 >> 12), x3 = c3 | (c3 >> 12);
+  return __byte_perm(__byte_perm(x0, x1, 0x0040), __byte_perm(x2, x3, 0x0040), 0x5410);
 }
 // max |x| of 8 bf16 (exact: bf16 abs and max, two lanes per instruction; a NaN loses to the other
 // operand, as with fmaxf)

@@ -98,6 +98,14 @@ __device__ __forceinline__ float e4m3_to_f32(uint32_t byte) {
 
 constexpr int kRowsPerWarp = 2;
 
+// RN32(1/6) = (1/6)(1 + 2^-25). For a bf16 amax, amax * RN32(1/6) rounds to the same E4M3 value as
+// the exact amax/6: where amax/6 is an E4M3 rounding midpoint (at most 5 significant bits) the
+// product is within 2^-25 relative of it, less than half an fp32 ulp, so it rounds onto the
+// midpoint and the E4M3 rounding breaks the tie as for the exact quotient; every other amax/6 is
+// at least ~2^-8 relative away from a midpoint. (Checked against the exact quotient for every
+// non-negative bf16, +inf included.)
+constexpr float kRcp6 = 0.16666667163372040f;   // 0x3E2AAAAB
+
 __global__ void __launch_bounds__(kWarpsPerBlock * 32, 4) pack_kernel(
     const uint16_t* __restrict__ latent, int64_t lstride, const uint16_t* __restrict__ rope, int64_t rstride,
     const int64_t* __restrict__ slots, int64_t n, uint8_t* __restrict__ cache, int64_t num_pages,
@@ -132,8 +140,8 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, 4) pack_kernel(
       float ma = amax8(a), mb = amax8(b);
       ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, 1));
       mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
-      // scale = E4M3_rn_sat(amax / 6); IEEE division, then one rounding to E4M3
-      const uint32_t sc = ptx::f32x2_to_e4m3x2(__fdiv_rn(ma, 6.0f), __fdiv_rn(mb, 6.0f));
+      // scale = E4M3_rn_sat(amax / 6), amax/6 formed as amax * RN32(1/6) (see kRcp6)
+      const uint32_t sc = ptx::f32x2_to_e4m3x2(__fmul_rn(ma, kRcp6), __fmul_rn(mb, kRcp6));
       const Thresholds ta = make_thresholds(e4m3_to_f32(sc & 0xFFu));
       const Thresholds tb = make_thresholds(e4m3_to_f32(sc >> 8));
       const uint32_t wa = encode8(a, ta), wb = encode8(b, tb);

@@ -91,9 +91,10 @@ __device__ __forceinline__ float amax8(const uint4& v) {
   for (int i = 1; i < 4; ++i) m = __hmax2(m, __habs2(*reinterpret_cast<const __nv_bfloat162*>(&w[i])));
   return fmaxf(fmaxf(__low2float(m), __high2float(m)), 0.f);
 }
-__device__ __forceinline__ float e4m3_to_f32(uint32_t byte) {
-  const uint32_t h2 = ptx::e4m3x2_to_f16x2(byte & 0xFFu);
-  return __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
+// The two E4M3 scale bytes of sc (byte 0, byte 1) as floats, one conversion for both.
+__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t sc) {
+  const uint32_t h2 = ptx::e4m3x2_to_f16x2(sc & 0xFFFFu);
+  return __half22float2(*reinterpret_cast<const __half2*>(&h2));
 }
 
 constexpr int kRowsPerWarp = 2;
@@ -142,8 +143,9 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, 4) pack_kernel(
       mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
       // scale = E4M3_rn_sat(amax / 6), amax/6 formed as amax * RN32(1/6) (see kRcp6)
       const uint32_t sc = ptx::f32x2_to_e4m3x2(__fmul_rn(ma, kRcp6), __fmul_rn(mb, kRcp6));
-      const Thresholds ta = make_thresholds(e4m3_to_f32(sc & 0xFFu));
-      const Thresholds tb = make_thresholds(e4m3_to_f32(sc >> 8));
+      const float2 s = e4m3x2_to_f32x2(sc);
+      const Thresholds ta = make_thresholds(s.x);
+      const Thresholds tb = make_thresholds(s.y);
       const uint32_t wa = encode8(a, ta), wb = encode8(b, tb);
       const uint32_t rr = ptx::f32x2_to_e4m3x2(bf_lo(r), bf_hi(r));
 

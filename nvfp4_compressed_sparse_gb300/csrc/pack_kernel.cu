@@ -32,8 +32,7 @@ __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 
 
 // e2m1 code of x for a block whose decoded scale is s: nearest grid point of
 // |x|/s, ties to the even code, saturating at 6, sign bit kept. Decided
-// without dividing: |x|/s vs a midpoint m is |x| vs m*s, and m*s is exact in
-// fp32 (m has <= 3 significant bits, s <= 4). Ties at 0.25, 1.25, 2.5, 5 go
+// without dividing: |x|/s vs a midpoint m is |x| vs m*s. Ties at 0.25, 1.25, 2.5, 5 go
 // down (even codes 0, 2, 4, 6); ties at 0.75, 1.75, 3.5 go up (codes 2, 4, 6).
 // The thresholds increase and each crossing test is monotonic in |x|, so the
 // code (the number of thresholds crossed) is found by binary search: three
@@ -42,7 +41,8 @@ __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 
 // bits (s >= 2^-9), so it is exact in bf16 and the comparisons are exact. NaN
 // magnitudes cross none (code 0).
 struct Thresholds {
-  uint32_t t0, t1, t2, t3, t4, t5, t6;   // m*s as a bf16 pair (both halves equal)
+  uint32_t t0, t1, t2, t3;               // m*s for m = 0.25, 0.75, 1.25, 1.75, as bf16 pairs
+  uint32_t d51, d40, d62;                // t5 - t1, t4 - t0, t6 - t2 (0 when s = 0)
 };
 __device__ __forceinline__ uint32_t bf16_pair(float f) {
   const uint32_t b = __float_as_uint(f) >> 16;   // exact for E4M3 values: their low 16 bits are zero
@@ -50,30 +50,35 @@ __device__ __forceinline__ uint32_t bf16_pair(float f) {
 }
 __device__ __forceinline__ __nv_bfloat162 as_bf2(uint32_t u) { return *reinterpret_cast<const __nv_bfloat162*>(&u); }
 __device__ __forceinline__ uint32_t as_u32(__nv_bfloat162 v) { return *reinterpret_cast<const uint32_t*>(&v); }
-// m*s for the seven midpoints m, two lanes per bf16 multiply: s (an E4M3 value, <= 4 significant
-// bits) is exact in bf16 and so is every product (<= 7 bits, within [2^-11, 2240]). A zero scale
-// becomes +inf, so every finite magnitude codes 0.
+// Thresholds m*s and the differences between the ones a search level chooses from, two lanes per
+// bf16 multiply: s (an E4M3 value, <= 4 significant bits) is exact in bf16 and so is every product
+// (m and the differences 2.75, 2.25, 3.75 have <= 4 bits; products within [2^-11, 2240]). A zero
+// scale makes the thresholds +inf (every finite magnitude codes 0) and the differences 0.
 __device__ __forceinline__ Thresholds make_thresholds(float s) {
   const __nv_bfloat162 s2 = as_bf2(s > 0.f ? bf16_pair(s) : 0x7F807F80u);
-  Thresholds t;   // midpoints 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5 as bf16 pairs
+  const __nv_bfloat162 sd = as_bf2(s > 0.f ? bf16_pair(s) : 0u);
+  Thresholds t;   // bf16 pairs of 0.25, 0.75, 1.25, 1.75 and of 2.75, 2.25, 3.75
   t.t0 = as_u32(__hmul2(s2, as_bf2(0x3E803E80u))); t.t1 = as_u32(__hmul2(s2, as_bf2(0x3F403F40u)));
   t.t2 = as_u32(__hmul2(s2, as_bf2(0x3FA03FA0u))); t.t3 = as_u32(__hmul2(s2, as_bf2(0x3FE03FE0u)));
-  t.t4 = as_u32(__hmul2(s2, as_bf2(0x40204020u))); t.t5 = as_u32(__hmul2(s2, as_bf2(0x40604060u)));
-  t.t6 = as_u32(__hmul2(s2, as_bf2(0x40A040A0u)));
+  t.d51 = as_u32(__hmul2(sd, as_bf2(0x40304030u))); t.d40 = as_u32(__hmul2(sd, as_bf2(0x40104010u)));
+  t.d62 = as_u32(__hmul2(sd, as_bf2(0x40704070u)));
   return t;
 }
-__device__ __forceinline__ uint32_t pick(uint32_t mask, uint32_t if_set, uint32_t if_clear) {
-  return (mask & if_set) | (~mask & if_clear);
-}
 // e2m1 codes (with sign bits) of the bf16 pair w, one per half: the element in bits 0..15 gives
-// the nibble in bits 0..3, the element in bits 16..31 the nibble in bits 16..19.
+// the nibble in bits 0..3, the element in bits 16..31 the nibble in bits 16..19. The search runs
+// in bf16 arithmetic (the fused multiply-add pipe): each test gives 1.0 or 0.0 per half, a level's
+// threshold is chosen as t_lo + g * (t_hi - t_lo) (exact: one of the two exact values), and the
+// code is summed onto 128 (bf16 128 + c has c in its low mantissa bits, so c = bits ^ 0x4300).
 __device__ __forceinline__ uint32_t e2m1_pair(uint32_t w, const Thresholds& t) {
   const __nv_bfloat162 a = as_bf2(w & 0x7FFF7FFFu);
-  const uint32_t b2 = __hge2_mask(a, as_bf2(t.t3));                       // codes 4..7
-  const uint32_t b1 = __hge2_mask(a, as_bf2(pick(b2, t.t5, t.t1)));      // 6..7 / 2..3
-  const uint32_t tb = pick(b1, pick(b2, t.t6, t.t2), pick(b2, t.t4, t.t0));
-  const uint32_t b0 = __hgt2_mask(a, as_bf2(tb));
-  return (b2 & 0x00040004u) | (b1 & 0x00020002u) | (b0 & 0x00010001u) | ((w >> 12) & 0x00080008u);
+  const __nv_bfloat162 g2 = __hge2(a, as_bf2(t.t3));                                   // codes 4..7
+  const __nv_bfloat162 g1 = __hge2(a, __hfma2(g2, as_bf2(t.d51), as_bf2(t.t1)));       // t5 / t1
+  const __nv_bfloat162 u = __hfma2(g2, as_bf2(t.d40), as_bf2(t.t0));                  // t4 / t0
+  const __nv_bfloat162 v = __hfma2(g2, as_bf2(t.d62), as_bf2(t.t2));                  // t6 / t2
+  const __nv_bfloat162 g0 = __hgt2(a, __hfma2(g1, __hsub2(v, u), u));
+  const __nv_bfloat162 c = __hfma2(g2, as_bf2(0x40804080u), __hfma2(g1, as_bf2(0x40004000u),
+                                                                     __hadd2(g0, as_bf2(0x43004300u))));
+  return (as_u32(c) ^ 0x43004300u) | ((w >> 12) & 0x00080008u);
 }
 // 8 bf16 (one uint4) -> 8 nibbles (one 32-bit word), element 0 in bits 0..3: each pair folds its
 // two nibbles into its low byte (c | c >> 12), and byte permutes gather the four bytes.

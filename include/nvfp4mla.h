@@ -81,6 +81,11 @@ enum {
  * (nearest-even, saturating at 6, sign kept; all magnitudes 0 when s_k = 0).
  * Row bytes: [0,256) nibbles, element 2i in the low nibble of byte i;
  * [256,288) the 32 scales; [288,352) E4M3(rope[d]).
+ * Non-finite inputs (the pages are silent; this library's rule): a NaN
+ * latent value takes no part in its block's amax and is stored with
+ * magnitude 0 (sign kept); an infinity saturates its block scale to 448 and
+ * is stored as +-6; a NaN rope value is stored as E4M3 NaN (0x7F or 0xFF,
+ * sign kept), an infinite one as +-448.
  *
  *   latent            bf16 [num_tokens, 512], row stride latent_row_stride
  *                     ELEMENTS; base 16-byte aligned, stride a multiple of 8

@@ -67,9 +67,17 @@ def _nearest_even(mag: np.ndarray, grid: np.ndarray) -> np.ndarray:
 
 
 def e4m3_encode(x: np.ndarray) -> np.ndarray:
-    """Round float64 values to E4M3 bytes: nearest, ties to even, saturating."""
+    """Round float64 values to E4M3 bytes: nearest, ties to even, saturating.
+
+    Non-finite inputs (a reading; the pages say nothing about them): +-inf
+    saturates to +-448 like any value past the largest finite magnitude, and
+    NaN becomes the E4M3 NaN pattern 0x7F with the input's sign bit kept
+    (0x7F or 0xFF).
+    """
     x = np.asarray(x, dtype=np.float64)
-    idx = _nearest_even(np.abs(x), E4M3_GRID)
+    nan = np.isnan(x)
+    idx = _nearest_even(np.where(nan, 0.0, np.abs(x)), E4M3_GRID)
+    idx = np.where(nan, 0x7F, idx)
     sign = np.signbit(x).astype(np.int64) << 7
     return (idx | sign).astype(np.uint8)
 
@@ -81,8 +89,13 @@ def e2m1_decode(code: np.ndarray) -> np.ndarray:
 
 
 def e2m1_encode(v: np.ndarray) -> np.ndarray:
-    """Round float64 values to e2m1 codes (0..15): nearest, ties to even, saturating at 6."""
+    """Round float64 values to e2m1 codes (0..15): nearest, ties to even, saturating at 6.
+
+    e2m1 has no NaN or infinity. Reading for non-finite inputs: +-inf
+    saturates to +-6 (code 7 with the sign bit), and NaN gets magnitude code 0
+    with its sign bit kept.
+    """
     v = np.asarray(v, dtype=np.float64)
-    idx = _nearest_even(np.abs(v), E2M1_GRID)
+    idx = _nearest_even(np.where(np.isnan(v), 0.0, np.abs(v)), E2M1_GRID)
     sign = np.signbit(v).astype(np.int64) << 3
     return (idx | sign).astype(np.uint8)

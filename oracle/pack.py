@@ -18,6 +18,10 @@ Readings where the pages are silent (each is listed in the design notes):
   * byte layout: bytes [0,256) hold element 2i in the low nibble and 2i+1 in
     the high nibble of byte i; bytes [256,288) hold the 32 block scales in
     order; bytes [288,352) hold the 64 rope bytes;
+  * non-finite inputs: a NaN latent value takes no part in its block's
+    maximum and is coded with magnitude 0 (its sign bit kept); an infinity
+    takes part, so its block scale saturates to 448 and it codes as +-6; a
+    rope NaN becomes E4M3 NaN (0x7F, sign kept) and a rope infinity +-448;
   * the cache is uint8 [num_pages, 64, 352]; a slot s addresses page s // 64,
     row s % 64; slot -1 means "skip this token"; any other slot outside
     [0, num_pages*64) is also skipped (and counted as a bad slot).
@@ -52,7 +56,10 @@ def block_scale_codes(latent: np.ndarray) -> np.ndarray:
     as rounding the exact quotient.
     """
     x = np.asarray(latent, dtype=np.float64).reshape(-1, N_BLOCKS, BLOCK)
-    amax = np.abs(x).max(axis=2)
+    # Reading for non-finite values: a NaN takes no part in its block's maximum
+    # (a block of NaNs and zeros has amax 0); an infinity does, and amax/6 =
+    # inf then saturates the scale to 448.
+    amax = np.where(np.isnan(x), 0.0, np.abs(x)).max(axis=2)
     return codec.e4m3_encode(amax / 6.0)
 
 

@@ -38,9 +38,10 @@ def assert_close(out, lse, ref_out, ref_lse, what=""):
 
 def oracle_units_from_device_rows(case, units, lat_dev, rope_dev):
     """Oracle outputs for (b, j) units, encoding the selected rows from their bf16
-    inputs (gathered from the device input tensors by physical slot)."""
-    q = codec.bf16_bits_to_f64(case.q_bits)
-    res = {}
+    inputs (gathered from the device input tensors by physical slot). The CPU work
+    runs in a pool of spawned worker processes."""
+    from tests import oracle_pool
+    keys, jobs = [], []
     for b, j in units:
         L = int(case.seq_lens[b])
         idx = case.topk_indices[b, j].astype(np.int64)
@@ -48,7 +49,6 @@ def oracle_units_from_device_rows(case, units, lat_dev, rope_dev):
         sel = idx[ok]
         slots = case.page_table[b][sel // 64].astype(np.int64) * 64 + sel % 64
         st = torch.from_numpy(slots).to(lat_dev.device)
-        rows = pack.encode_rows(bits_of(lat_dev[st]), bits_of(rope_dev[st]))
-        c = attention.dequant_rows(rows)
-        res[(b, j)] = attention.attend(q[b, j], c, case.softmax_scale)
-    return res
+        jobs.append((case.q_bits[b, j], bits_of(lat_dev[st]), bits_of(rope_dev[st]), case.softmax_scale))
+        keys.append((b, j))
+    return dict(zip(keys, oracle_pool.attend_units(jobs)))

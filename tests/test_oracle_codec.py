@@ -228,3 +228,41 @@ def test_write_cache_slots():
     touched = np.zeros((3, 64), bool)
     touched[0, 5] = touched[2, 2] = True
     assert (cache[~touched] == 0xCD).all()
+
+
+def test_bf16_bits_to_f64_matches_torch_on_every_pattern():
+    """The bf16 decode every other pin builds on, against torch's own bfloat16 on all
+    65,536 bit patterns (NaN patterns compare as NaN)."""
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    ours = codec.bf16_bits_to_f64(bits)
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).double().numpy()
+    np.testing.assert_array_equal(np.isnan(ours), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    np.testing.assert_array_equal(ours[ok], ref[ok])
+    np.testing.assert_array_equal(np.signbit(ours[ok]), np.signbit(ref[ok]))
+
+
+def test_non_finite_inputs_follow_the_stated_reading():
+    """NaN and infinity: a NaN latent value is left out of the block maximum and codes to
+    magnitude 0 with its sign; an infinity saturates the scale to 448 and codes to +-6; rope
+    NaN is E4M3 NaN with its sign, rope infinity +-448. Expected bytes written out by hand."""
+    lat = np.zeros((1, 512), np.uint16)
+    rope = np.zeros((1, 64), np.uint16)
+    lat[0, 0:2] = [0x7FC0, 0x3F80]      # block 0: NaN, 1.0      -> scale E4M3(1/6) = 0x23 (0.171875)
+    lat[0, 16:18] = [0x7F80, 0x3F80]    # block 1: +inf, 1.0     -> scale 448 (0x7E)
+    lat[0, 32:34] = [0xFF80, 0x3F80]    # block 2: -inf, 1.0     -> scale 448
+    lat[0, 48] = 0xFFC0                 # block 3: -NaN alone    -> amax 0, scale 0
+    lat[0, 64:66] = [0x7FC1, 0xFFC0]    # block 4: NaNs only     -> scale 0
+    rope[0, 0:4] = [0x7FC0, 0x7F80, 0xFF80, 0xFFC0]
+    with np.errstate(all="ignore"):
+        row = pack.encode_rows(lat, rope)[0]
+    assert list(row[256:261]) == [0x23, 0x7E, 0x7E, 0x00, 0x00]
+    # element codes (low nibble = even element): 1.0 / 0.171875 = 5.82 -> code 7 (6); NaN -> 0;
+    # +inf -> 7 and 1/448 -> 0; -inf -> 0xF; -NaN -> 0x8; NaN -> 0 and -NaN -> 0x8
+    assert row[0] == 0x70 and row[8] == 0x07 and row[16] == 0x0F and row[24] == 0x08 and row[32] == 0x80
+    assert list(row[288:292]) == [0x7F, 0x7E, 0xFE, 0xFF]
+    # the NaN-free elements of a block are coded as if the NaN were absent
+    clean = lat.copy()
+    clean[0, 0] = 0
+    with np.errstate(all="ignore"):
+        assert pack.encode_rows(clean, np.zeros((1, 64), np.uint16))[0][256] == 0x23

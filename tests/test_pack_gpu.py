@@ -136,3 +136,24 @@ def test_spec_verify_append_full_size_sampled():
     written = torch.zeros(flat.shape[0], dtype=torch.bool, device="cuda")
     written[slots] = True
     assert bool((flat[~written] == 0xCD).all())
+
+
+def test_non_finite_latent_and_rope_bit_exact():
+    """NaN (both signs, several payloads) and +-inf in latent blocks and rope values: the kernel's
+    bytes equal the oracle's under the stated reading (NaN out of the block maximum, coded as a
+    signed zero; infinity saturating; rope NaN -> E4M3 NaN with sign, rope inf -> +-448)."""
+    rng = np.random.default_rng(11)
+    specials = np.array([0x7FC0, 0xFFC0, 0x7F81, 0xFFFF, 0x7F80, 0xFF80], np.uint16)
+    n = 256
+    lat = workloads.f32_to_bf16_bits(rng.standard_normal((n, 512), dtype=np.float32))
+    rope = workloads.f32_to_bf16_bits(rng.standard_normal((n, 64), dtype=np.float32))
+    # each row gets specials in a few random positions; some blocks are all NaN
+    for r in range(n):
+        k = int(rng.integers(1, 6))
+        lat[r, rng.integers(0, 512, size=k)] = specials[rng.integers(0, specials.size, size=k)]
+        rope[r, rng.integers(0, 64, size=2)] = specials[rng.integers(0, specials.size, size=2)]
+    lat[0, 0:16] = 0x7FC0
+    lat[1, 16:32] = np.where(np.arange(16) % 2 == 0, 0xFFC0, 0)
+    lat[2, 32:48] = 0x7F80
+    with np.errstate(all="ignore"):
+        _check_rows(lat, rope)

@@ -497,12 +497,6 @@ struct MmaIssuer {
     pd0 = sdesc(smem_u32(ps), 4096, kPSbo, kPSw);
   }
 
-  // QK(k) of this half may be issued once the half is in TMEM and the softmax group has read S of
-  // tile k-1.
-  __device__ __forceinline__ bool qk_ready(int64_t k) {
-    return mbar_test(&sm->kv_ready[which], (uint32_t)(k & 1)) &&
-           (k == 0 || mbar_test(&sm->s_free, (uint32_t)((k - 1) & 1)));
-  }
   __device__ __forceinline__ void qk_step(int ks, uint32_t acc) {
     const uint64_t b = qd + (uint64_t)((((ks >> 2) * NH * 128) + (ks & 3) * 32) >> 4);
     umma_ts(s_col, tmem + kTmemK + 8 * ks, b, kIdQK, acc);
@@ -520,12 +514,6 @@ struct MmaIssuer {
     umma_commit(&sm->s_full);
   }
 
-  // PV(k) may be issued once P(k) and the V rows of tile k are in shared memory and, when tile k
-  // starts a new unit, the epilogue of the previous unit has read O.
-  __device__ __forceinline__ bool pv_ready(int64_t k, const TileInfo& ti) {
-    return mbar_test(&sm->p_full[k & 1], (uint32_t)((k >> 1) & 1)) && mbar_test(&sm->v_ready[which], (uint32_t)(k & 1)) &&
-           !(ti.first && k > 0 && !mbar_test(&sm->o_free, (uint32_t)(ofree_waits & 1)));
-  }
   __device__ __forceinline__ void pv(int64_t k, const TileInfo& ti) {
     if (ti.first && k > 0) ++ofree_waits;
     tc_fence_after();
@@ -550,57 +538,48 @@ struct MmaIssuer {
   }
 };
 
-// Each issuer polls (without suspending) and issues whichever of QK(kq) and PV(kp) is ready, so PV
-// of one tile never waits behind QK of the next. QK runs at most one tile ahead of PV; that bound
-// also keeps every polled barrier within one phase of the parity being tested.
+// Each issuer runs its half's UMMAs in the pipeline's order QK(0), PV(0), QK(1), PV(1), ..., and
+// sleeps in hardware on the barrier it needs next (a polling issuer takes issue slots from the
+// warps on its scheduler). PV(k) is ready before QK(k+1): both follow pass B(k) on the dequant
+// warps, and QK(k+1) also needs pass A(k+1), which those warps run after pass B(k). When the next
+// tile starts a new unit, its q image is requested as soon as QK(k) has completed (the q buffer is
+// free then), before the wait for P(k). Every wait below is on a barrier at most one phase ahead
+// of the parity it tests (each is released by a step that needs this thread's previous issue).
 template <int NH, bool kCluster>
 __device__ void mma_loop(const DecodeParams& p, Smem* sm, uint8_t* vtile, uint8_t* qs, uint8_t* ps,
                          int64_t t_begin, int64_t t_end, int which) {
   MmaIssuer<NH> m(p, sm, vtile, qs, ps, t_begin, t_end, which);
   const int64_t n = t_end - t_begin;
   // cluster mode: q_full phase 0 is the unit's q image written in-kernel (no copy to request)
-  int64_t kq = 0, kp = 0, q_copies = kCluster ? 1 : 0;
-  bool q_pending = kCluster;
-  TileInfo tq = tile_info(p, t_begin, t_begin, t_end), tp = tq;
-  uint64_t t_idle = 0;
-  uint32_t idle = 0;
-  while (kp < n) {
-    // A new unit's q overwrites the q buffer once this half's QK of the previous tile is complete
-    // (this thread issued that QK last, so its kfree phase is the newest one possible).
-    if (kq < n && kq <= kp + 1 && tq.first && !q_pending &&
-        (kq == 0 || mbar_test(&sm->kfree[which], (uint32_t)((kq - 1) & 1)))) {
-      if (q_copies == 0) asm volatile("griddepcontrol.wait;" ::: "memory");   // q16 comes from the prep grid
-      m.request_q(tq.unit);
-      ++q_copies;
-      q_pending = true;
-    }
-    if (kq < n && kq <= kp + 1 &&
-        (!tq.first || (q_pending && mbar_test(&sm->q_full[which], (uint32_t)((q_copies - 1) & 1)))) &&
-        m.qk_ready(kq)) {
-      if (tq.first) q_pending = false;
-      m.qk(kq);
-      if (++kq < n) tq = tile_info(p, t_begin + kq, t_begin, t_end);
-      idle = 0;
-      continue;
-    }
-    if (kp < kq && m.pv_ready(kp, tp)) {
-      m.pv(kp, tp);
-      if (++kp < n) tp = tile_info(p, t_begin + kp, t_begin, t_end);
-      idle = 0;
-      continue;
-    }
-    // Nothing ready: back off briefly so the polling thread leaves issue slots to the warps that
-    // share its scheduler, and give up (flagging a timeout) after kWaitTimeoutNs.
-    __nanosleep(20);
-    if ((++idle & 255u) == 0) {
-      if (sm->abort) break;
-      const uint64_t t = globaltimer_ns();
-      if (idle == 256) t_idle = t;
-      else if (t - t_idle > kWaitTimeoutNs) {
-        fail(sm, p.status);
-        break;
+  int64_t q_copies = kCluster ? 1 : 0;
+  if (!kCluster && n > 0) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // q16 comes from the prep grid
+    m.request_q(tile_info(p, t_begin, t_begin, t_end).unit);
+    q_copies = 1;
+  }
+  for (int64_t k = 0; k < n; ++k) {
+    const TileInfo ti = tile_info(p, t_begin + k, t_begin, t_end);
+    // ---- QK(k)
+    bool ok = true;
+    if (ti.first) ok = wait(sm, &sm->q_full[which], (uint32_t)((q_copies - 1) & 1), p.status);
+    if (ok) ok = wait(sm, &sm->kv_ready[which], (uint32_t)(k & 1), p.status);
+    if (ok && k > 0) ok = wait(sm, &sm->s_free, (uint32_t)((k - 1) & 1), p.status);
+    if (!ok) break;
+    m.qk(k);
+    if (k + 1 < n) {
+      const TileInfo tn = tile_info(p, t_begin + k + 1, t_begin, t_end);
+      if (tn.first) {
+        if (!wait(sm, &sm->kfree[which], (uint32_t)(k & 1), p.status)) break;
+        m.request_q(tn.unit);
+        ++q_copies;
       }
     }
+    // ---- PV(k)
+    ok = wait(sm, &sm->p_full[k & 1], (uint32_t)((k >> 1) & 1), p.status);
+    if (ok) ok = wait(sm, &sm->v_ready[which], (uint32_t)(k & 1), p.status);
+    if (ok && ti.first && k > 0) ok = wait(sm, &sm->o_free, (uint32_t)(m.ofree_waits & 1), p.status);
+    if (!ok) break;
+    m.pv(k, ti);
   }
   // never leave with a q copy in flight (abort path)
   if (q_copies > (kCluster ? 1 : 0)) mbar_wait(&sm->q_full[which], (uint32_t)((q_copies - 1) & 1), nullptr, kWaitTimeoutNs);
@@ -659,13 +638,12 @@ __device__ __forceinline__ void load_scores(uint32_t taddr, bool valid, float qs
 // Softmax group: thread t owns tile row t (a token) and all heads. The reference m of each head
 // (the "running max") is kept lazily: it is raised only when a score exceeds it by more than
 // kLazy = 15 (log2 units), so most tiles need one group vote instead of a max reduction, and
-// P = 2^(z - m) stays <= 2^15, inside the fp16 range. When it is raised, it is set kHeadroom = 8
-// above the tile's maximum: later tiles then need a raise (which must wait for PV of the previous
-// tile to finish before O can be rescaled) only for scores 23 above that maximum instead of 15
-// (with outlier-heavy keys, 7 % of tiles instead of 22 %). P of the maximum itself is 2^-8; fp16
-// keeps scores down to 17 below it, whose weights (< 2^-17 of the maximum's) are all that is lost.
+// P = 2^(z - m) stays <= 2^15, inside the fp16 range. When raised it is set to the tile's maximum
+// (no headroom), so P keeps fp16's whole range below it: weights down to 2^-24 of the maximum's
+// are represented, and the mass lost below that is at most topk * 2^-25 of the total. (A reference
+// set above the maximum would cut the raises but move the underflow threshold up with it: with 8
+// units of headroom, 2,047 tokens 17 units below a dominant one lost 1.5 % of the mass.)
 constexpr float kLazy = 15.f;
-constexpr float kHeadroom = 8.f;
 // Returns false when the group gave up (abort); every thread of the group returns the same value.
 template <int NH, bool kCluster>
 __device__ bool softmax_loop(const DecodeParams& p, Smem* sm, uint8_t* ps, uint8_t* vtile, ClusterScratch* cs,
@@ -734,7 +712,7 @@ __device__ bool softmax_loop(const DecodeParams& p, Smem* sm, uint8_t* ps, uint8
         const float mold = sm->m_used[lane];
         float mnew = mold, alpha = 1.f;
         if (tmax > mold + kLazy) {
-          mnew = tmax + kHeadroom;
+          mnew = tmax;
           alpha = (mold == kNegInf) ? 0.f : ex2_approx(mold - mnew);
         }
         sm->m_used[lane] = mnew;
@@ -747,30 +725,6 @@ __device__ bool softmax_loop(const DecodeParams& p, Smem* sm, uint8_t* ps, uint8
       for (int h = 0; h < 32; h += 4) {
         const float4 av = *reinterpret_cast<const float4*>(&sm->alpha[h]);
         l_part[h] *= av.x; l_part[h + 1] *= av.y; l_part[h + 2] *= av.z; l_part[h + 3] *= av.w;
-      }
-      if (sm->need_rescale && !ti.first) {
-        // O^T[dim, h] *= alpha[h], after PV of the previous tile has finished accumulating into O
-        if (lane == 0 && wait(sm, &sm->vfree[0][3], (uint32_t)((k - 1) & 1), p.status))
-          wait(sm, &sm->vfree[1][3], (uint32_t)((k - 1) & 1), p.status);
-        __syncwarp();
-        tc_fence_after();
-#pragma unroll 1
-        for (int mb = 0; mb < 4; ++mb) {
-          uint32_t r[32];
-          if (NH == 32) {
-            tmem_ld32(tmem_lane + o_col + mb * NH, r);
-          } else {
-            tmem_ld16(tmem_lane + o_col + mb * NH, *reinterpret_cast<uint32_t(*)[16]>(r));
-          }
-          tmem_wait_ld();
-#pragma unroll
-          for (int h = 0; h < NH; ++h) r[h] = __float_as_uint(__uint_as_float(r[h]) * sm->alpha[h]);
-          if (NH == 32) tmem_st32(tmem_lane + o_col + mb * NH, r);
-          else tmem_st16(tmem_lane + o_col + mb * NH, *reinterpret_cast<uint32_t(*)[16]>(r));
-        }
-        tmem_wait_st();
-        // z was not kept across the rescale (register pressure): reload this tile's scores
-        load_scores<NH>(tmem_lane + s_col, valid, qscale, z);
       }
     }
     tc_fence_before();
@@ -804,6 +758,30 @@ __device__ bool softmax_loop(const DecodeParams& p, Smem* sm, uint8_t* ps, uint8
         *reinterpret_cast<uint4*>(pbuf + t * 32 + ((c ^ ((t >> 2) & 1)) << 4)) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
     }
     fence_proxy_async_smem();
+    // ---- a raised reference: O^T[dim, h] *= alpha[h] before PV(k) adds to it, once PV(k-1) has
+    // finished accumulating (P above did not have to wait for this)
+    if (raise && sm->need_rescale && !ti.first) {
+      if (lane == 0 && wait(sm, &sm->vfree[0][3], (uint32_t)((k - 1) & 1), p.status))
+        wait(sm, &sm->vfree[1][3], (uint32_t)((k - 1) & 1), p.status);
+      __syncwarp();
+      tc_fence_after();
+#pragma unroll 1
+      for (int mb = 0; mb < 4; ++mb) {
+        uint32_t r[32];
+        if (NH == 32) {
+          tmem_ld32(tmem_lane + o_col + mb * NH, r);
+        } else {
+          tmem_ld16(tmem_lane + o_col + mb * NH, *reinterpret_cast<uint32_t(*)[16]>(r));
+        }
+        tmem_wait_ld();
+#pragma unroll
+        for (int h = 0; h < NH; ++h) r[h] = __float_as_uint(__uint_as_float(r[h]) * sm->alpha[h]);
+        if (NH == 32) tmem_st32(tmem_lane + o_col + mb * NH, r);
+        else tmem_st16(tmem_lane + o_col + mb * NH, *reinterpret_cast<uint32_t(*)[16]>(r));
+      }
+      tmem_wait_st();
+      tc_fence_before();
+    }
     mbar_arrive(&sm->p_full[k & 1]);
 
     if (ti.last) {

@@ -7,23 +7,27 @@ one shared permuted pool, top-k = 2,048 positions per query. Synthetic seeded
 data (workloads.make_case(2)); the cache (~2.6 GB) is packed on the device by
 mla_kv_pack from device-drawn bf16 rows before timing.
 
-A step is one sparse_mla_decode call (decode kernel + merge kernel). L2 is
+A step is one sparse_mla_decode call (q-prep, decode and merge kernels). L2 is
 flushed (256 MiB write) before every timed step; each step is timed with CUDA
 events on the launching stream. The JSON line also carries:
-  roofline     decode bytes at measured HBM bandwidth (the path is HBM-bound)
+  roofline     decode bytes at the measured HBM bandwidth (the path is HBM-bound),
+               and the same against the nominal 8 TB/s
   e2e          the same step through the public call with pinned host buffers:
                the kernels read q / index lists / page table / lengths from host
                memory and write out + LSE back over NVLink-C2C, inside the timed
                region (the KV cache stays resident in HBM, as in serving)
-  cpu_baseline the fp64 CPU oracle on a bounded sample of the same workload
+  cpu_baseline the fp64 CPU oracle on query tokens of the same workload (its own
+               rows and index lists): one thread, and one process per host core
+  configs      the decode-shard (B=16), spec-verify (192K-row pack + Q=4 decode in
+               one step) and capacity (1.63M-token pool) cases, device-timed
+  schedules    split vs cluster schedule for B = 1, 4, 16, 64 (headline requests)
   pack         mla_kv_pack of one 1M-row chunk of the cache fill (mean of 10 calls,
                L2 flushed before each), for context
---impl reference times the CPU oracle as the reference arm.
+--impl reference times the CPU oracle as the reference arm: every step runs all 64
+query tokens of the headline case through the oracle, one process per host core.
 Multi-GPU (torchrun): every rank runs an independent replica (the path shards
 by request with no exchange); the slowest rank's time is reported.
 """
-from __future__ import annotations
-
 import argparse
 import hashlib
 import json
@@ -34,12 +38,15 @@ import subprocess
 import sys
 import time
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "sparse MLA decode µs/step & achieved HBM GB/s (% roofline), B=64, top-k 2048"
 WORKLOAD = "mixed agent batch: B=64, Q=1, H=32, contexts U[70K,160K], 64-token pages, top-k 2048"
 FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS = 6800.0, 1900.0
+NOMINAL_HBM_GBS = 8000.0
 
 
 def peaks():
@@ -139,39 +146,36 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def cpu_baseline_sample(units: int, seed: int = 0) -> dict:
-    """Time the fp64 oracle (single thread) on `units` query tokens shaped like the
-    headline workload (2,048 selected rows each, H=32); scaled to us per 64-token step."""
-    code = r"""
-import os, sys, time, json
-sys.path.insert(0, %r)
-import numpy as np
-import workloads
-from oracle import attention, pack
-rng = np.random.default_rng(%d)
-K, H, U = 2048, 32, %d
-lat = workloads.f32_to_bf16_bits(rng.standard_normal((K, 512), dtype=np.float32))
-rope = workloads.f32_to_bf16_bits(rng.standard_normal((K, 64), dtype=np.float32))
-cache = pack.encode_rows(lat, rope).reshape(K // 64, 64, 352)
-q = workloads.f32_to_bf16_bits(rng.standard_normal((1, 1, H, 576), dtype=np.float32))
-pt = np.arange(K // 64, dtype=np.int32)[None]
-sl = np.array([K], np.int32)
-tks = [rng.permutation(K).astype(np.int32)[None, None] for _ in range(4)]
-t0 = time.perf_counter()
-for u in range(U):
-    attention.sparse_decode(q, cache, pt, tks[u %% 4], sl, workloads.SOFTMAX_SCALE)
-dt = time.perf_counter() - t0
-print(json.dumps({"seconds": dt, "units": U}))
-""" % (ROOT, seed, units)
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
-    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=1800)
-    if r.returncode != 0:
-        raise RuntimeError(r.stderr[-2000:])
-    d = json.loads(r.stdout.strip().splitlines()[-1])
-    per_unit = d["seconds"] / d["units"]
-    return {"value": per_unit * 64 * 1e6, "unit": "us/step", "cores": 1, "kind": "oracle",
-            "sample": f"{d['units']} query tokens of the headline shape (2048 rows, H=32) through the fp64 "
-                      f"oracle, single thread, scaled to one 64-token step; {d['seconds']:.1f} s of CPU work"}
+def oracle_pool(case, units, workers):
+    """Spawned oracle workers holding the prepared query tokens `units` of `case`."""
+    from oracle import timing
+    return timing.OraclePool(case, units, workers)
+
+
+def cpu_baseline(case, sample_units: int = 16, single_units: int = 2) -> dict:
+    """The fp64 oracle on `sample_units` query tokens of the case (its own rows and index lists):
+    all of them over one process per host core, and `single_units` of them in one thread; both
+    scaled to one step of the case (B*Q query tokens)."""
+    from oracle import timing
+    cores = os.cpu_count() or 1
+    rng = np.random.default_rng(7)
+    units_all = [(b, j) for b in range(case.B) for j in range(case.Q)]
+    pick = sorted(rng.choice(len(units_all), size=min(sample_units, len(units_all)), replace=False))
+    pool = oracle_pool(case, [units_all[i] for i in pick], cores)
+    try:
+        pool.step()                                   # warm-up
+        par = min(pool.step() for _ in range(2))
+        one = pool.step_single_thread(single_units)
+    finally:
+        pool.close()
+    n = len(pick)
+    scale = len(units_all)
+    return {"value": par / n * scale * 1e6, "unit": "us/step", "cores": cores, "kind": "oracle",
+            "cpu_model": timing.cpu_model(), "os_cpu_count": cores,
+            "single_thread_us_per_step": one / single_units * scale * 1e6,
+            "sample": f"{n} of the {scale} query tokens of this workload (own rows and index lists) through the "
+                      f"fp64 oracle, one process per core ({cores}), scaled to one {scale}-token step; the single-"
+                      f"thread figure runs {single_units} of them in one process"}
 
 
 def dist_setup():
@@ -206,27 +210,180 @@ def barrier(world):
 
 
 def run_reference(args, world, rank):
+    """The CPU oracle as the reference arm: each step runs all B*Q query tokens of the headline case
+    (its own rows and index lists) through the fp64 oracle, one process per host core."""
     if rank != 0:
         return None
-    steps, warm = args.steps, args.warmup
-    # bounded sample per step: one query token (2,048 rows), scaled to the 64-token step
-    per_step_units = 1
-    if warm > 0:
-        cpu_baseline_sample(warm)   # warm-up (imports, caches)
-    t = cpu_baseline_sample(steps * per_step_units)
-    value = t["value"]
+    import workloads
+    from oracle import timing
+    case = workloads.make_case(2)
+    cores = os.cpu_count() or 1
+    units = [(b, j) for b in range(case.B) for j in range(case.Q)]
+    full = len(units)
+    if 0 < args.ref_units < full:
+        units = units[:args.ref_units]
+    pool = oracle_pool(case, units, cores)
+    try:
+        for _ in range(args.warmup):
+            pool.step()
+        wall0 = time.perf_counter()
+        times = [pool.step() for _ in range(args.steps)]
+        wall = time.perf_counter() - wall0
+    finally:
+        pool.close()
+    mean_s = statistics.fmean(times) * full / len(units)
+    value = mean_s * 1e6
+    if len(units) == full:
+        sample = (f"all {full} query tokens of the headline case per step (own rows and index lists), "
+                  f"fp64 oracle, one process per core ({cores})")
+    else:
+        sample = (f"{len(units)} of the {full} query tokens per step, scaled to the full step, fp64 oracle, "
+                  f"one process per core ({cores})")
     return {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "us/step", "n_gpus": world,
-        "steps": steps, "warmup": warm, "ms_per_step": value / 1000.0, "higher_is_better": False,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_s * 1e3, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "sample": "one query token per step"},
-        "cpu_baseline": {"value": value, "unit": "us/step", "cores": 1, "kind": "oracle", "sample": t["sample"]},
+        "config": {"workload": WORKLOAD, "B": case.B, "Q": case.Q, "H": case.H, "topk": case.topk},
+        "cpu_baseline": {"value": value, "unit": "us/step", "cores": cores, "kind": "oracle",
+                         "cpu_model": timing.cpu_model(), "os_cpu_count": cores, "sample": sample},
         "e2e": {"value": value, "unit": "us/step", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "wall_s_timed_region": wall,
     }
 
 
+def fill_cache(m, workloads, case, dev, timed_pack=None):
+    """Pack the case's whole cache on the device (1M-row chunks of device-drawn bf16 rows). With
+    timed_pack = (stream, flush), the pack of the first chunk is also timed (mean of 10 calls, L2
+    flushed before each) and (ms, rows) is returned with the cache."""
+    import torch
+    rows_total = case.num_pages * 64
+    cache = torch.empty((case.num_pages, 64, 352), dtype=torch.uint8, device=dev)
+    chunk = 1 << 20
+    pack_ms, pack_rows = None, 0
+    for ci, s0 in enumerate(range(0, rows_total, chunk)):
+        n = min(chunk, rows_total - s0)
+        lat, rope = workloads.device_rows(case, n, dev, seed_offset=ci)
+        slots = torch.arange(s0, s0 + n, device=dev)
+        m.mla_kv_pack(lat, rope, slots, cache)
+        if ci == 0 and timed_pack is not None:
+            stream, flush = timed_pack
+            torch.cuda.synchronize(dev)
+            times = []
+            for _ in range(10):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                m.mla_kv_pack(lat, rope, slots, cache)
+                e1.record(stream)
+                times.append((e0, e1))
+            torch.cuda.synchronize(dev)
+            pack_ms, pack_rows = statistics.fmean(a.elapsed_time(b) for a, b in times), n
+        del lat, rope, slots
+    torch.cuda.synchronize(dev)
+    return cache, pack_ms, pack_rows
+
+
+def device_inputs(case, dev):
+    import torch
+    q = torch.from_numpy(case.q_bits.view(np.int16)).to(dev).view(torch.bfloat16)
+    return (q, torch.from_numpy(case.page_table).to(dev), torch.from_numpy(case.topk_indices).to(dev),
+            torch.from_numpy(case.seq_lens).to(dev))
+
+
+def time_decode(m, case, cache, inputs, stream, flush, steps, warmup, cluster=False, pre=None):
+    """Mean device time (ms) of one decode call (plus `pre`, a callable enqueued before it, timed
+    separately), L2 flushed before each step. Returns (decode ms, pre ms or None)."""
+    import torch
+    q, pt, tk, sl = inputs
+    out = torch.empty((case.B, case.Q, case.H, 512), dtype=torch.bfloat16, device=cache.device)
+    lse = torch.empty((case.B, case.Q, case.H), dtype=torch.float32, device=cache.device)
+    ws = torch.empty(max(1, m.sparse_mla_decode_workspace_size(case.B, case.Q, case.H, case.topk)),
+                     dtype=torch.uint8, device=cache.device)
+    ev = []
+    for i in range(warmup + steps):
+        flush.zero_()
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        e[0].record(stream)
+        if pre is not None:
+            pre()
+        e[1].record(stream)
+        m.sparse_mla_decode(q, cache, pt, tk, sl, case.softmax_scale, out=out, lse=lse, workspace=ws,
+                            stream=stream, cluster=cluster)
+        e[2].record(stream)
+        if i >= warmup:
+            ev.append(e)
+    torch.cuda.synchronize(cache.device)
+    dec = statistics.fmean(e[1].elapsed_time(e[2]) for e in ev)
+    pre_ms = statistics.fmean(e[0].elapsed_time(e[1]) for e in ev) if pre is not None else None
+    return dec, pre_ms
+
+
+def roofline_entry(nbytes, flops, ms, hbm):
+    t = ms * 1e-3
+    return {"us": ms * 1e3, "algorithmic_bytes": nbytes, "achieved_gbs": nbytes / t / 1e9,
+            "frac_of_measured_hbm": nbytes / t / 1e9 / hbm, "frac_of_nominal_hbm": nbytes / t / 1e9 / NOMINAL_HBM_GBS,
+            "algorithmic_flops": flops}
+
+
+def extra_configs(m, workloads, dev, stream, flush, hbm, steps):
+    """Device-timed µs and roofline fractions of the decode-shard, spec-verify and capacity cases."""
+    import torch
+    res = {}
+    for cfg in (1, 3, 4):
+        case = workloads.make_case(cfg)
+        cache, _, _ = fill_cache(m, workloads, case, dev)
+        inputs = device_inputs(case, dev)
+        nbytes, flops = algorithmic_cost(case)
+        entry = {"name": workloads.CONFIG_NAMES[cfg], "B": case.B, "Q": case.Q, "H": case.H, "topk": case.topk}
+        if cfg == 3:
+            # the step also packs the 6,000 new rows of every request (192K rows) into fresh pages
+            n_new = case.new_slots.size
+            lat, rope = workloads.device_rows(case, n_new, dev, seed_offset=99)
+            slots = torch.from_numpy(case.new_slots).to(dev)
+            pre = lambda: m.mla_kv_pack(lat, rope, slots, cache, stream=stream)
+            dec_ms, pack_ms = time_decode(m, case, cache, inputs, stream, flush, steps, 5, pre=pre)
+            pack_bytes = n_new * (1024 + 128 + 352 + 8)
+            entry["decode"] = roofline_entry(nbytes, flops, dec_ms, hbm)
+            entry["pack"] = {"rows": n_new, "us": pack_ms * 1e3, "algorithmic_bytes": pack_bytes,
+                             "achieved_gbs": pack_bytes / (pack_ms * 1e-3) / 1e9,
+                             "frac_of_measured_hbm": pack_bytes / (pack_ms * 1e-3) / 1e9 / hbm}
+            entry["step_us"] = (dec_ms + pack_ms) * 1e3
+            del lat, rope, slots
+        else:
+            dec_ms, _ = time_decode(m, case, cache, inputs, stream, flush, steps, 5)
+            entry["decode"] = roofline_entry(nbytes, flops, dec_ms, hbm)
+        if cfg == 4:
+            entry["aliased_page_fraction"] = case.notes.get("aliased_fraction")
+        res[str(cfg)] = entry
+        del cache, inputs
+        torch.cuda.empty_cache()
+    return res
+
+
+def schedule_table(m, workloads, case, cache, dev, stream, flush, steps):
+    """Split vs cluster schedule (forced wherever one wave of clusters fits) for the first B requests
+    of the headline case; cluster_size 0 = no wave of clusters fits."""
+    import copy
+    res = []
+    for B in (1, 4, 16, 64):
+        c = copy.copy(case)
+        c.B = B
+        c.seq_lens, c.page_table, c.topk_indices, c.q_bits = (case.seq_lens[:B], case.page_table[:B],
+                                                             case.topk_indices[:B], case.q_bits[:B])
+        inputs = device_inputs(c, dev)
+        split_ms, _ = time_decode(m, c, cache, inputs, stream, flush, steps, 5)
+        ctas, g = m.sparse_mla_decode_plan(c.B, c.Q, c.H, c.topk, cluster="any")
+        row = {"B": B, "split_us": split_ms * 1e3, "split_ctas": m.sparse_mla_decode_plan(c.B, c.Q, c.H, c.topk)[0],
+               "cluster_size": g}
+        if g > 0:
+            cl_ms, _ = time_decode(m, c, cache, inputs, stream, flush, steps, 5, cluster="any")
+            row["cluster_us"] = cl_ms * 1e3
+            row["cluster_ctas"] = ctas
+        res.append(row)
+    return res
+
+
 def run_gpu(args, world, rank, local):
-    import numpy as np
     import torch
 
     import nvfp4_compressed_sparse_gb300 as m
@@ -236,49 +393,18 @@ def run_gpu(args, world, rank, local):
     torch.cuda.set_device(dev)
     m.load_library()
     case = workloads.make_case(2)
-    rows_total = case.num_pages * 64
-    cache = torch.empty((case.num_pages, 64, 352), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-
-    # ---- fill the cache through mla_kv_pack in 1M-row chunks (device memory stays ~3 GB);
-    # the pack of one chunk is timed for context (not the headline)
-    chunk = 1 << 20
-    pack_ms, pack_rows = None, 0
-    for ci, s0 in enumerate(range(0, rows_total, chunk)):
-        n = min(chunk, rows_total - s0)
-        lat, rope = workloads.device_rows(case, n, dev, seed_offset=ci)
-        slots = torch.arange(s0, s0 + n, device=dev)
-        m.mla_kv_pack(lat, rope, slots, cache)
-        if ci == 0:
-            # mean of 10 calls on this chunk, L2 flushed (256 MiB write) before each
-            flush0 = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-            torch.cuda.synchronize(dev)
-            times = []
-            for _ in range(10):
-                flush0.zero_()
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                m.mla_kv_pack(lat, rope, slots, cache)
-                e1.record(stream)
-                times.append((e0, e1))
-            torch.cuda.synchronize(dev)
-            pack_ms, pack_rows = statistics.fmean(a.elapsed_time(b) for a, b in times), n
-            del flush0
-        del lat, rope, slots
-    torch.cuda.synchronize(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    cache, pack_ms, pack_rows = fill_cache(m, workloads, case, dev, timed_pack=(stream, flush))
     pack_bytes = pack_rows * (1024 + 128 + 352 + 8)
     torch.cuda.empty_cache()
 
-    q = torch.from_numpy(case.q_bits.view(np.int16)).to(dev).view(torch.bfloat16)
-    pt = torch.from_numpy(case.page_table).to(dev)
-    tk = torch.from_numpy(case.topk_indices).to(dev)
-    sl = torch.from_numpy(case.seq_lens).to(dev)
+    q, pt, tk, sl = device_inputs(case, dev)
     out = torch.empty((case.B, case.Q, case.H, 512), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((case.B, case.Q, case.H), dtype=torch.float32, device=dev)
     ws = torch.empty(max(1, m.sparse_mla_decode_workspace_size(case.B, case.Q, case.H, case.topk)),
                      dtype=torch.uint8, device=dev)
     status = torch.zeros(4, dtype=torch.int32, device=dev)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
     plan_ctas, plan_cluster = m.sparse_mla_decode_plan(case.B, case.Q, case.H, case.topk)
     launches_per_step = 1 if plan_cluster > 0 else 3
@@ -366,7 +492,8 @@ def run_gpu(args, world, rank, local):
         "median_us_per_step": statistics.median(times_ms) * 1000.0,
         "roofline": {"bound": "hbm" if roof_hbm_us >= roof_tc_us else "tensor", "achieved": achieved, "peak": hbm,
                      "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic_from_profile(),
-                     "peak_kind": peak_kind, "algorithmic_bytes": nbytes, "algorithmic_flops": flops,
+                     "peak_kind": peak_kind, "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
+                     "algorithmic_bytes": nbytes, "algorithmic_flops": flops,
                      "roofline_us": max(roof_hbm_us, roof_tc_us), "tensor_roofline_us": roof_tc_us,
                      "timed_unit": timed_unit, "decode_ctas": plan_ctas, "cluster": plan_cluster},
         "e2e": {"value": e2e_ms * 1000.0, "unit": "us/step", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -380,8 +507,13 @@ def run_gpu(args, world, rank, local):
         "dev_status": st,
         "wall_s_timed_region": wall,
     }
+    if not args.no_extra and world == 1:
+        result["schedules"] = schedule_table(m, workloads, case, cache, dev, stream, flush, min(K, 200))
+        del cache, hq, hpt, htk, hsl, hout, hlse, ws
+        torch.cuda.empty_cache()
+        result["configs"] = extra_configs(m, workloads, dev, stream, flush, hbm, min(K, 200))
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline_sample(args.cpu_units)
+        result["cpu_baseline"] = cpu_baseline(case)
     return result
 
 
@@ -391,8 +523,10 @@ def main():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--cpu-units", type=int, default=320)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true", help="skip the extra cases and the schedule table")
+    ap.add_argument("--ref-units", type=int, default=0,
+                    help="reference arm: query tokens per step (0 = all of the headline case)")
     args = ap.parse_args()
     world, rank, local = dist_setup()
     if args.impl == "reference":

@@ -100,6 +100,10 @@ enum {
  *   num_pages         >= 1
  *   dev_status        optional int32[NVFP4MLA_STATUS_WORDS] (may be NULL)
  *   stream            cudaStream_t
+ * All pointers must be device memory of the current device: each is checked
+ * with cudaPointerGetAttributes first, and host memory (pageable or
+ * page-locked), another device's memory or an unknown pointer returns
+ * NVFP4MLA_ERR_INVALID_ARG with nothing enqueued.
  * Two tokens mapped to the same slot race; the caller must not do that.
  */
 int mla_kv_pack(const void* latent, int64_t latent_row_stride, const void* rope, int64_t rope_row_stride,
@@ -167,7 +171,11 @@ size_t sparse_mla_decode_workspace_size(int B, int Q, int H, int topk, int num_s
  *                     decode CTAs at n (testing aid; 0 = no cap; a cap also
  *                     selects the split schedule), optionally or-ed with
  *                     NVFP4MLA_FLAG_CLUSTER (allow the cluster schedule, see
- *                     sparse_mla_decode_plan), optionally
+ *                     sparse_mla_decode_plan) and, with it,
+ *                     NVFP4MLA_FLAG_CLUSTER_ANY (tuning aid: take the cluster
+ *                     schedule whenever one wave of clusters fits, even when
+ *                     a CTA then runs more tiles than under the split
+ *                     schedule), optionally
  *                     or-ed with NVFP4MLA_FLAG_TEST_TIMEOUT (testing aid: the
  *                     decode grid withholds one internal signal, so its
  *                     bounded waits expire after about 2 s; the grid then
@@ -180,6 +188,7 @@ size_t sparse_mla_decode_workspace_size(int B, int Q, int H, int topk, int num_s
 #define NVFP4MLA_FLAG_MAX_CTAS(n) ((uint32_t)(n) & 0xFFFFu)
 #define NVFP4MLA_FLAG_TEST_TIMEOUT (1u << 31)
 #define NVFP4MLA_FLAG_CLUSTER (1u << 30)
+#define NVFP4MLA_FLAG_CLUSTER_ANY (1u << 29)
 int sparse_mla_decode(const void* q, const void* kv_cache, int64_t num_pages, const int32_t* page_table,
                       int64_t max_pages_per_seq, const int32_t* topk_indices, const int32_t* seq_lens, int B,
                       int Q, int H, int topk, float softmax_scale, void* out, float* lse, void* workspace,
@@ -233,9 +242,10 @@ int sparse_mla_decode_plan(int B, int Q, int H, int topk, uint32_t flags, int* c
  *   - All calls on a device share the region: calls whose work overlaps on the
  *     GPU race. Order them on one stream (or with events).
  *   - The region needs no initialisation; each call writes what it reads.
- *   - Returns NVFP4MLA_ERR_WORKSPACE, before enqueuing anything, when the sizes
- *     need more scratch than the region holds (see
- *     sparse_mla_decode_workspace_size); otherwise as sparse_mla_decode.
+ *   - Returns NVFP4MLA_ERR_WORKSPACE, before enqueuing anything, when the call
+ *     (these sizes and flags, on the current device) needs more scratch than
+ *     the region holds; otherwise as sparse_mla_decode (same size checks and
+ *     return codes).
  */
 #define NVFP4MLA_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
 int sparse_mla_decode_noalloc(const void* q, const void* kv_cache, int64_t num_pages, const int32_t* page_table,

@@ -22,6 +22,7 @@ ROPE_DIM = 64
 QK_DIM = 576
 FLAG_TEST_TIMEOUT = 1 << 31   # NVFP4MLA_FLAG_TEST_TIMEOUT
 FLAG_CLUSTER = 1 << 30        # NVFP4MLA_FLAG_CLUSTER
+FLAG_CLUSTER_ANY = 1 << 29    # NVFP4MLA_FLAG_CLUSTER_ANY
 STATUS_WORDS = 4
 STAT_BAD_INDEX, STAT_BAD_PAGE, STAT_TIMEOUT, STAT_BAD_SLOT = 0, 1, 2, 3
 
@@ -125,10 +126,18 @@ def sparse_mla_decode_workspace_size(B: int, Q: int, H: int, topk: int, num_sms:
     return int(load_library().sparse_mla_decode_workspace_size(B, Q, H, topk, num_sms))
 
 
+def _cluster_flags(cluster) -> int:
+    # cluster: False, True (allow the cluster schedule where it is as balanced as the split one) or
+    # "any" (take it whenever one wave of clusters fits; a tuning aid)
+    if not cluster:
+        return 0
+    return FLAG_CLUSTER | (FLAG_CLUSTER_ANY if cluster == "any" else 0)
+
+
 def sparse_mla_decode_plan(B: int, Q: int, H: int, topk: int, max_ctas: int = 0,
-                           cluster: bool = False) -> tuple[int, int]:
+                           cluster=False) -> tuple[int, int]:
     """(decode CTAs, cluster size G; 0 = split schedule) that sparse_mla_decode launches on the current device."""
-    flags = (max_ctas & 0xFFFF) | (FLAG_CLUSTER if cluster else 0)
+    flags = (max_ctas & 0xFFFF) | _cluster_flags(cluster)
     ctas, g = ctypes.c_int(0), ctypes.c_int(0)
     rc = load_library().sparse_mla_decode_plan(B, Q, H, topk, flags, ctypes.byref(ctas), ctypes.byref(g))
     if rc != 0:
@@ -138,12 +147,13 @@ def sparse_mla_decode_plan(B: int, Q: int, H: int, topk: int, max_ctas: int = 0,
 
 def sparse_mla_decode(q, kv_cache, page_table, topk_indices, seq_lens, softmax_scale, out=None, lse=None,
                       workspace=None, dev_status=None, max_ctas: int = 0, stream=None,
-                      test_timeout: bool = False, cluster: bool = False):
+                      test_timeout: bool = False, cluster=False):
     """One sparse MLA decode step. q bf16 [B,Q,H,576], kv_cache uint8 [P,64,352],
     page_table int32 [B,max_pages], topk_indices int32 [B,Q,K], seq_lens int32 [B].
     Returns (out bf16 [B,Q,H,512], lse fp32 [B,Q,H]). max_ctas and test_timeout are the
     testing aids NVFP4MLA_FLAG_MAX_CTAS and NVFP4MLA_FLAG_TEST_TIMEOUT; cluster=True sets
-    NVFP4MLA_FLAG_CLUSTER (allow the one-grid cluster schedule). q, page_table, topk_indices,
+    NVFP4MLA_FLAG_CLUSTER (allow the one-grid cluster schedule; cluster="any" also sets
+    NVFP4MLA_FLAG_CLUSTER_ANY). q, page_table, topk_indices,
     seq_lens, out and lse may be pinned CPU tensors: the kernels then read the inputs from and
     write the results to host memory directly, inside the call's stream order."""
     import torch
@@ -172,7 +182,7 @@ def sparse_mla_decode(q, kv_cache, page_table, topk_indices, seq_lens, softmax_s
         _ptr(q), _ptr(kv_cache), kv_cache.shape[0], _ptr(page_table), page_table.shape[1], _ptr(topk_indices),
         _ptr(seq_lens), B, Q, H, K, float(softmax_scale), _ptr(out), _ptr(lse), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(dev_status),
-        (int(max_ctas) & 0xFFFF) | (FLAG_TEST_TIMEOUT if test_timeout else 0) | (FLAG_CLUSTER if cluster else 0),
+        (int(max_ctas) & 0xFFFF) | (FLAG_TEST_TIMEOUT if test_timeout else 0) | _cluster_flags(cluster),
         _stream_ptr(stream))
     if rc != 0:
         raise NvFp4MlaError(rc, "sparse_mla_decode")

@@ -31,7 +31,8 @@ int device_sm_count() {
   return cached[dev];
 }
 
-DecodeSchedule make_schedule(int B, int Q, int H, int topk, int num_sms, int max_ctas, bool allow_cluster) {
+DecodeSchedule make_schedule(int B, int Q, int H, int topk, int num_sms, int max_ctas, bool allow_cluster,
+                             bool any_balance) {
   DecodeSchedule s{};
   const int nh = H < kHeadsPerCta ? H : kHeadsPerCta;
   s.units = (int64_t)B * Q * (H / nh);
@@ -45,7 +46,8 @@ DecodeSchedule make_schedule(int B, int Q, int H, int topk, int num_sms, int max
   s.cluster = 0;
   // Cluster mode when one wave of G CTAs per unit is as balanced as the stream-K split:
   // G = min(8, SMs / units, tiles per unit). A cluster CTA that runs one tile more than the
-  // busiest stream-K CTA loses more than the separate q-prep and merge launches cost.
+  // busiest stream-K CTA loses more than the separate q-prep and merge launches cost
+  // (any_balance: take it whenever G >= 1, to measure the two schedules against each other).
   if (allow_cluster && max_ctas == 0 && num_sms > 0) {
     int64_t c = num_sms / s.units;
     if (c > 8) c = 8;
@@ -53,7 +55,7 @@ DecodeSchedule make_schedule(int B, int Q, int H, int topk, int num_sms, int max
     if (c >= 1) {
       const int64_t per_cta_cluster = (s.tiles_per_unit + c - 1) / c;
       const int64_t per_cta_split = (s.total_tiles + s.ctas - 1) / s.ctas;
-      if (per_cta_cluster <= per_cta_split) {
+      if (any_balance || per_cta_cluster <= per_cta_split) {
         s.cluster = (int)c;
         s.ctas = (int)(s.units * c);
       }
@@ -167,14 +169,28 @@ static uint64_t next_call_tag() {
 static bool plan_on_device(int B, int Q, int H, int topk, uint32_t flags, DecodeSchedule* out) {
   const int sms = device_sm_count();
   if (sms <= 0) return false;
-  DecodeSchedule s = make_schedule(B, Q, H, topk, sms, (int)(flags & 0xFFFFu), (flags & NVFP4MLA_FLAG_CLUSTER) != 0);
+  const bool any = (flags & NVFP4MLA_FLAG_CLUSTER_ANY) != 0;
+  DecodeSchedule s = make_schedule(B, Q, H, topk, sms, (int)(flags & 0xFFFFu), (flags & NVFP4MLA_FLAG_CLUSTER) != 0, any);
   if (s.cluster > 1) {
     const int fit = max_active_clusters(H < kHeadsPerCta ? H : kHeadsPerCta, s.cluster);
-    if (fit < s.units) s = make_schedule(B, Q, H, topk, sms, (int)(flags & 0xFFFFu), false);
+    if (fit < s.units) s = make_schedule(B, Q, H, topk, sms, (int)(flags & 0xFFFFu), false, false);
   }
   *out = s;
   return true;
 }
+
+namespace nvfp4mla {
+// Workspace bytes sparse_mla_decode needs for these sizes and flags on the current device, with the
+// same checks and return codes as the call itself (OK, INVALID_ARG, UNSUPPORTED, CUDA).
+int decode_workspace_need(int B, int Q, int H, int topk, uint32_t flags, size_t* need) {
+  if (!sizes_ok(B, Q, H, topk)) return NVFP4MLA_ERR_INVALID_ARG;
+  DecodeSchedule s;
+  if (!plan_on_device(B, Q, H, topk, flags, &s)) return NVFP4MLA_ERR_CUDA;
+  if (s.total_tiles > (int64_t)INT32_MAX) return NVFP4MLA_ERR_UNSUPPORTED;
+  *need = workspace_bytes_for(s, H);
+  return NVFP4MLA_OK;
+}
+}  // namespace nvfp4mla
 
 extern "C" {
 
@@ -203,6 +219,12 @@ int mla_kv_pack(const void* latent, int64_t latent_row_stride, const void* rope,
   if (!aligned(rope, 4) || (rope_row_stride % 2) != 0) return NVFP4MLA_ERR_ALIGNMENT;
   if (!aligned(kv_cache, 16) || !aligned(slot_mapping, 8)) return NVFP4MLA_ERR_ALIGNMENT;
   if (dev_status != nullptr && !aligned(dev_status, 4)) return NVFP4MLA_ERR_ALIGNMENT;
+  // The pack kernel reads and writes device memory only: pageable or page-locked host memory,
+  // another device's memory or an unknown pointer is rejected before anything is enqueued.
+  if (pointer_kind(latent) != kPtrDevice || pointer_kind(rope) != kPtrDevice ||
+      pointer_kind(slot_mapping) != kPtrDevice || pointer_kind(kv_cache) != kPtrDevice ||
+      (dev_status != nullptr && pointer_kind(dev_status) != kPtrDevice))
+    return NVFP4MLA_ERR_INVALID_ARG;
   const cudaError_t err = launch_pack(static_cast<const uint16_t*>(latent), latent_row_stride,
                                       static_cast<const uint16_t*>(rope), rope_row_stride, slot_mapping,
                                       num_tokens, static_cast<uint8_t*>(kv_cache), num_pages, dev_status,
@@ -223,7 +245,7 @@ size_t sparse_mla_decode_workspace_size(int B, int Q, int H, int topk, int num_s
   if (!sizes_ok(B, Q, H, topk)) return 0;
   if (num_sms <= 0) num_sms = device_sm_count();
   if (num_sms <= 0) return 0;
-  const DecodeSchedule s = make_schedule(B, Q, H, topk, num_sms, 0, false);
+  const DecodeSchedule s = make_schedule(B, Q, H, topk, num_sms, 0, false, false);
   if (s.total_tiles > (int64_t)INT32_MAX) return 0;
   return workspace_bytes_for(s, H);
 }

@@ -32,7 +32,8 @@ struct DecodeSchedule {
   int cluster;             // 0 = stream-K, else CTAs per unit
 };
 
-DecodeSchedule make_schedule(int B, int Q, int H, int topk, int num_sms, int max_ctas, bool allow_cluster);
+DecodeSchedule make_schedule(int B, int Q, int H, int topk, int num_sms, int max_ctas, bool allow_cluster,
+                             bool any_balance);
 size_t workspace_bytes_for(const DecodeSchedule& s, int H);
 
 struct DecodeParams {
@@ -72,5 +73,8 @@ int max_active_clusters(int heads_per_cta, int cluster);   // clusters of the de
 cudaError_t launch_merge(const DecodeParams& p, cudaStream_t stream);
 
 int device_sm_count();
+// Workspace bytes sparse_mla_decode needs for these sizes and flags on the current device (same
+// checks and return codes as the call).
+int decode_workspace_need(int B, int Q, int H, int topk, uint32_t flags, size_t* need);
 
 }  // namespace nvfp4mla

@@ -65,9 +65,11 @@ extern "C" int sparse_mla_decode_noalloc(const void* q, const void* kv_cache, in
                                          int topk, float softmax_scale, void* out, float* lse, int32_t* dev_status,
                                          uint32_t flags, void* stream) {
   using namespace nvfp4mla;
-  if (sparse_mla_decode_workspace_size(B, Q, H, topk, 1) == 0) return NVFP4MLA_ERR_INVALID_ARG;   // bad sizes
-  const size_t need = sparse_mla_decode_workspace_size(B, Q, H, topk, 0);
-  if (need == 0) return NVFP4MLA_ERR_CUDA;                                                         // no device
+  // The scratch this call's own schedule needs (the flags can change the grid), with the same
+  // size checks and return codes as sparse_mla_decode.
+  size_t need = 0;
+  const int rc = decode_workspace_need(B, Q, H, topk, flags, &need);
+  if (rc != NVFP4MLA_OK) return rc;
   if (need > kScratchBytes) return NVFP4MLA_ERR_WORKSPACE;
   void* scratch = nullptr;
   if (scratch_for_current_device(&scratch) != cudaSuccess) return NVFP4MLA_ERR_CUDA;

@@ -24,6 +24,9 @@ Modules:
   codec      bf16 / FP8-E4M3 / FP4-e2m1 value codecs
   pack       NVFP4 row encoding and the paged cache write
   attention  dequantisation and sparse / dense MLA decode in fp64
+  timing     runs the oracle on query tokens of a workload over spawned worker
+             processes (the benchmark's CPU baseline and reference arm); it
+             adds no arithmetic of its own
 
 Pins: every function here is checked by tests/test_oracle_*.py against facts
 that do not come from this package (the pages' row arithmetic, torch's

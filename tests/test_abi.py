@@ -82,6 +82,20 @@ def test_pack_host_checks(lib):
     assert _pack(lib, A, rope=A, slots=A, cache=A + 8) == 2
 
 
+def test_pack_rejects_host_memory_before_launch(lib):
+    """Real host buffers (pageable numpy memory), correctly sized and aligned: the pack call
+    classifies its pointers first and returns INVALID_ARG without touching the cache."""
+    import numpy as np
+    lat = np.zeros((4, 512), np.uint16)
+    rope = np.zeros((4, 64), np.uint16)
+    slots = np.arange(4, dtype=np.int64)
+    cache = np.full((1, 64, 352), 0xAB, np.uint8)
+    P = lambda a: V(a.ctypes.data)
+    rc = lib.mla_kv_pack(P(lat), 512, P(rope), 64, P(slots), 4, P(cache), 1, None, None)
+    assert rc == 1
+    assert (cache == 0xAB).all()
+
+
 def _dec(lib, q=1 << 20, cache=1 << 20, pages=10, pt=1 << 20, maxp=4, idx=1 << 20, sl=1 << 20, B=1, Q=1, H=32,
          K=128, scale=0.07, out=1 << 20, lse=1 << 20, ws=1 << 20, wsb=1 << 30, status=None, flags=0):
     return lib.sparse_mla_decode(V(q), V(cache), pages, V(pt), maxp, V(idx), V(sl), B, Q, H, K, ctypes.c_float(scale),

@@ -292,3 +292,21 @@ def test_pageable_host_memory_is_rejected_before_launch():
         assert rc == 1, (name, rc)
     torch.cuda.synchronize()
     assert bool((out == 7.0).all()) and bool((lse == 7.0).all())   # nothing was launched
+
+
+@pytest.mark.parametrize("spec", [dict(B=1, Q=1, H=32, topk=2048, L=(5000,)), dict(B=4, Q=1, H=32, topk=2048, L=(4000,) * 4),
+                                  dict(B=3, Q=1, H=16, topk=1000, L=(3000, 1200, 2500))],
+                         ids=lambda s: "B{B}H{H}K{topk}".format(**s))
+def test_cluster_any_schedule_matches_oracle(spec):
+    """NVFP4MLA_FLAG_CLUSTER_ANY: the cluster schedule wherever one wave of clusters fits, including
+    shapes where a CTA then runs more tiles than under the split schedule (the schedule table of the
+    benchmark uses it)."""
+    ctas, g = m.sparse_mla_decode_plan(spec["B"], spec["Q"], spec["H"], spec["topk"], cluster="any")
+    assert g >= 1 and ctas == g * spec["B"] * spec["Q"] * max(1, spec["H"] // 32)
+    case = workloads.small_case(seed=77 + spec["B"], **spec)
+    lat, rope, rows = _host_cache(case)
+    cache = _gpu_cache(lat, rope, case.num_pages)
+    ref_out, ref_lse = attention.sparse_decode(case.q_bits, rows, case.page_table, case.topk_indices,
+                                               case.seq_lens, case.softmax_scale)
+    out, lse = _decode(case, cache, cluster="any")
+    assert_close(out, lse, ref_out, ref_lse, f"cluster any G={g} {spec}")

@@ -56,7 +56,7 @@ def test_reference_arm_under_torchrun_prints_one_line():
     env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
            "--master-addr", "127.0.0.1", "--master-port", str(port), "bench.py", "--impl", "reference",
-           "--steps", "1", "--warmup", "0"]
+           "--steps", "1", "--warmup", "0", "--ref-units", "2"]
     r = subprocess.run(cmd, cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stderr[-2000:]
     lines = [line for line in r.stdout.splitlines() if line.startswith("{")]

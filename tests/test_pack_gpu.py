@@ -157,3 +157,25 @@ def test_non_finite_latent_and_rope_bit_exact():
     lat[2, 32:48] = 0x7F80
     with np.errstate(all="ignore"):
         _check_rows(lat, rope)
+
+
+def test_host_memory_rejected_before_launch():
+    """Device inputs but a host-memory cache (pageable, then page-locked): the call returns
+    INVALID_ARG before launching, and the cache bytes are untouched."""
+    import ctypes
+    lib = m.load_library()
+    V = ctypes.c_void_p
+    lat = torch.zeros((64, 512), dtype=torch.bfloat16, device="cuda")
+    rope = torch.zeros((64, 64), dtype=torch.bfloat16, device="cuda")
+    slots = torch.arange(64, device="cuda")
+    for pinned in (False, True):
+        cache = torch.full((1, 64, 352), 0xAB, dtype=torch.uint8)
+        if pinned:
+            cache = cache.pin_memory()
+        rc = lib.mla_kv_pack(V(lat.data_ptr()), 512, V(rope.data_ptr()), 64, V(slots.data_ptr()), 64,
+                             V(cache.data_ptr()), 1, None, None)
+        torch.cuda.synchronize()
+        assert rc == 1, (pinned, rc)
+        assert bool((cache == 0xAB).all())
+    with pytest.raises(ValueError):
+        m.mla_kv_pack(lat.cpu(), rope, slots, torch.zeros((1, 64, 352), dtype=torch.uint8, device="cuda"))

@@ -290,7 +290,7 @@ def device_inputs(case, dev):
             torch.from_numpy(case.seq_lens).to(dev))
 
 
-def time_decode(m, case, cache, inputs, stream, flush, steps, warmup, cluster=False, pre=None):
+def time_decode(m, case, cache, inputs, stream, flush, steps, warmup, cluster=None, pre=None):
     """Mean device time (ms) of one decode call (plus `pre`, a callable enqueued before it, timed
     separately), L2 flushed before each step. Returns (decode ms, pre ms or None)."""
     import torch
@@ -334,7 +334,8 @@ def extra_configs(m, workloads, dev, stream, flush, hbm, steps):
         cache, _, _ = fill_cache(m, workloads, case, dev)
         inputs = device_inputs(case, dev)
         nbytes, flops = algorithmic_cost(case)
-        entry = {"name": workloads.CONFIG_NAMES[cfg], "B": case.B, "Q": case.Q, "H": case.H, "topk": case.topk}
+        entry = {"name": workloads.CONFIG_NAMES[cfg], "B": case.B, "Q": case.Q, "H": case.H, "topk": case.topk,
+                 "cluster": m.sparse_mla_decode_plan(case.B, case.Q, case.H, case.topk)[1]}
         if cfg == 3:
             # the step also packs the 6,000 new rows of every request (192K rows) into fresh pages
             n_new = case.new_slots.size
@@ -371,10 +372,11 @@ def schedule_table(m, workloads, case, cache, dev, stream, flush, steps):
         c.seq_lens, c.page_table, c.topk_indices, c.q_bits = (case.seq_lens[:B], case.page_table[:B],
                                                              case.topk_indices[:B], case.q_bits[:B])
         inputs = device_inputs(c, dev)
-        split_ms, _ = time_decode(m, c, cache, inputs, stream, flush, steps, 5)
+        split_ms, _ = time_decode(m, c, cache, inputs, stream, flush, steps, 5, cluster=False)
         ctas, g = m.sparse_mla_decode_plan(c.B, c.Q, c.H, c.topk, cluster="any")
-        row = {"B": B, "split_us": split_ms * 1e3, "split_ctas": m.sparse_mla_decode_plan(c.B, c.Q, c.H, c.topk)[0],
-               "cluster_size": g}
+        row = {"B": B, "split_us": split_ms * 1e3,
+               "split_ctas": m.sparse_mla_decode_plan(c.B, c.Q, c.H, c.topk, cluster=False)[0], "cluster_size": g,
+               "default_cluster_size": m.sparse_mla_decode_plan(c.B, c.Q, c.H, c.topk)[1]}
         if g > 0:
             cl_ms, _ = time_decode(m, c, cache, inputs, stream, flush, steps, 5, cluster="any")
             row["cluster_us"] = cl_ms * 1e3

@@ -167,15 +167,16 @@ size_t sparse_mla_decode_workspace_size(int B, int Q, int H, int topk, int num_s
  *                     bytes, 256-byte aligned; contents need no
  *                     initialisation and are clobbered
  *   dev_status        optional int32[NVFP4MLA_STATUS_WORDS] (may be NULL)
- *   flags             0, or NVFP4MLA_FLAG_MAX_CTAS(n) to cap the number of
- *                     decode CTAs at n (testing aid; 0 = no cap; a cap also
- *                     selects the split schedule), optionally or-ed with
- *                     NVFP4MLA_FLAG_CLUSTER (allow the cluster schedule, see
- *                     sparse_mla_decode_plan) and, with it,
- *                     NVFP4MLA_FLAG_CLUSTER_ANY (tuning aid: take the cluster
- *                     schedule whenever one wave of clusters fits, even when
- *                     a CTA then runs more tiles than under the split
- *                     schedule), optionally
+ *   flags             0 (the split schedule, see sparse_mla_decode_plan), or
+ *                     NVFP4MLA_FLAG_MAX_CTAS(n) to cap the number of decode
+ *                     CTAs at n (testing aid; 0 = no cap; a cap also selects
+ *                     the split schedule), optionally or-ed with
+ *                     NVFP4MLA_FLAG_SPLIT (always the split schedule) or
+ *                     NVFP4MLA_FLAG_CLUSTER (also take the cluster schedule
+ *                     wherever it is as balanced as the split one) and, with
+ *                     it, NVFP4MLA_FLAG_CLUSTER_ANY (tuning aid: take the
+ *                     cluster schedule whenever one wave of clusters fits),
+ *                     optionally
  *                     or-ed with NVFP4MLA_FLAG_TEST_TIMEOUT (testing aid: the
  *                     decode grid withholds one internal signal, so its
  *                     bounded waits expire after about 2 s; the grid then
@@ -189,6 +190,7 @@ size_t sparse_mla_decode_workspace_size(int B, int Q, int H, int topk, int num_s
 #define NVFP4MLA_FLAG_TEST_TIMEOUT (1u << 31)
 #define NVFP4MLA_FLAG_CLUSTER (1u << 30)
 #define NVFP4MLA_FLAG_CLUSTER_ANY (1u << 29)
+#define NVFP4MLA_FLAG_SPLIT (1u << 28)
 int sparse_mla_decode(const void* q, const void* kv_cache, int64_t num_pages, const int32_t* page_table,
                       int64_t max_pages_per_seq, const int32_t* topk_indices, const int32_t* seq_lens, int B,
                       int Q, int H, int topk, float softmax_scale, void* out, float* lse, void* workspace,
@@ -205,16 +207,17 @@ int sparse_mla_decode(const void* q, const void* kv_cache, int64_t num_pages, co
  * the batch. Two schedules:
  *   - cluster (*cluster = G >= 1): G CTAs (one thread-block cluster, G <= 8)
  *     per (query, head group); each takes a contiguous share of its selected
- *     rows and the partials are merged through distributed shared memory
- *     inside the same grid. Only with NVFP4MLA_FLAG_CLUSTER, and then when
- *     one wave of such clusters fits the GPU and no CTA runs more tiles of
- *     128 rows than under the split schedule. (On GB300 it is not faster than
- *     the split schedule on the measured shapes, whose q-prep and merge grids
- *     overlap the decode grid through programmatic dependent launch, so it is
- *     not the default.)
- *   - split (*cluster = 0, the default): the 128-row tiles of all queries form one
+ *     rows, q is converted in the decode grid and the partials are merged
+ *     through distributed shared memory inside the same grid: one launch.
+ *   - split (*cluster = 0): the 128-row tiles of all queries form one
  *     sequence cut into *ctas contiguous ranges (one CTA per SM); a q-prep
  *     grid runs before it and a merge grid combines the partials.
+ * Without flags the split schedule is used: on GB300 it measured faster at
+ * every size tried (64 queries: 54.2 vs 55.6 us with 2-CTA clusters; 128
+ * queries: 93.9 vs 96.9 us with 1-CTA clusters; 1 and 4 queries: ~8 us faster
+ * than 8-CTA clusters). NVFP4MLA_FLAG_CLUSTER takes the cluster schedule when
+ * one wave of clusters fits and no CTA runs more 128-row tiles than under the
+ * split schedule; NVFP4MLA_FLAG_CLUSTER_ANY whenever one wave fits.
  *   B, Q, H, topk     as for sparse_mla_decode
  *   flags             as for sparse_mla_decode
  *   ctas, cluster     host int pointers (either may be NULL): the grid size

@@ -23,6 +23,7 @@ QK_DIM = 576
 FLAG_TEST_TIMEOUT = 1 << 31   # NVFP4MLA_FLAG_TEST_TIMEOUT
 FLAG_CLUSTER = 1 << 30        # NVFP4MLA_FLAG_CLUSTER
 FLAG_CLUSTER_ANY = 1 << 29    # NVFP4MLA_FLAG_CLUSTER_ANY
+FLAG_SPLIT = 1 << 28          # NVFP4MLA_FLAG_SPLIT
 STATUS_WORDS = 4
 STAT_BAD_INDEX, STAT_BAD_PAGE, STAT_TIMEOUT, STAT_BAD_SLOT = 0, 1, 2, 3
 
@@ -127,15 +128,18 @@ def sparse_mla_decode_workspace_size(B: int, Q: int, H: int, topk: int, num_sms:
 
 
 def _cluster_flags(cluster) -> int:
-    # cluster: False, True (allow the cluster schedule where it is as balanced as the split one) or
-    # "any" (take it whenever one wave of clusters fits; a tuning aid)
-    if not cluster:
+    # cluster: None (the library's default schedule), False/"split" (always the split schedule),
+    # True (also the cluster schedule wherever it is as balanced as the split one) or "any" (the
+    # cluster schedule whenever one wave of clusters fits; a tuning aid)
+    if cluster is None:
         return 0
+    if cluster is False or cluster == "split":
+        return FLAG_SPLIT
     return FLAG_CLUSTER | (FLAG_CLUSTER_ANY if cluster == "any" else 0)
 
 
 def sparse_mla_decode_plan(B: int, Q: int, H: int, topk: int, max_ctas: int = 0,
-                           cluster=False) -> tuple[int, int]:
+                           cluster=None) -> tuple[int, int]:
     """(decode CTAs, cluster size G; 0 = split schedule) that sparse_mla_decode launches on the current device."""
     flags = (max_ctas & 0xFFFF) | _cluster_flags(cluster)
     ctas, g = ctypes.c_int(0), ctypes.c_int(0)
@@ -147,13 +151,14 @@ def sparse_mla_decode_plan(B: int, Q: int, H: int, topk: int, max_ctas: int = 0,
 
 def sparse_mla_decode(q, kv_cache, page_table, topk_indices, seq_lens, softmax_scale, out=None, lse=None,
                       workspace=None, dev_status=None, max_ctas: int = 0, stream=None,
-                      test_timeout: bool = False, cluster=False):
+                      test_timeout: bool = False, cluster=None):
     """One sparse MLA decode step. q bf16 [B,Q,H,576], kv_cache uint8 [P,64,352],
     page_table int32 [B,max_pages], topk_indices int32 [B,Q,K], seq_lens int32 [B].
     Returns (out bf16 [B,Q,H,512], lse fp32 [B,Q,H]). max_ctas and test_timeout are the
     testing aids NVFP4MLA_FLAG_MAX_CTAS and NVFP4MLA_FLAG_TEST_TIMEOUT; cluster=True sets
-    NVFP4MLA_FLAG_CLUSTER (allow the one-grid cluster schedule; cluster="any" also sets
-    NVFP4MLA_FLAG_CLUSTER_ANY). q, page_table, topk_indices,
+    NVFP4MLA_FLAG_CLUSTER (also the one-grid cluster schedule where it is as balanced as the
+    split one; cluster="any" also sets NVFP4MLA_FLAG_CLUSTER_ANY), cluster=False sets
+    NVFP4MLA_FLAG_SPLIT, None keeps the library's default. q, page_table, topk_indices,
     seq_lens, out and lse may be pinned CPU tensors: the kernels then read the inputs from and
     write the results to host memory directly, inside the call's stream order."""
     import torch

@@ -31,8 +31,7 @@ int device_sm_count() {
   return cached[dev];
 }
 
-DecodeSchedule make_schedule(int B, int Q, int H, int topk, int num_sms, int max_ctas, bool allow_cluster,
-                             bool any_balance) {
+DecodeSchedule make_schedule(int B, int Q, int H, int topk, int num_sms, int max_ctas, ClusterPolicy policy) {
   DecodeSchedule s{};
   const int nh = H < kHeadsPerCta ? H : kHeadsPerCta;
   s.units = (int64_t)B * Q * (H / nh);
@@ -44,18 +43,21 @@ DecodeSchedule make_schedule(int B, int Q, int H, int topk, int num_sms, int max
   s.ctas = (int)g;
   s.partial_slots = s.ctas + s.units - 1;
   s.cluster = 0;
-  // Cluster mode when one wave of G CTAs per unit is as balanced as the stream-K split:
-  // G = min(8, SMs / units, tiles per unit). A cluster CTA that runs one tile more than the
-  // busiest stream-K CTA loses more than the separate q-prep and merge launches cost
-  // (any_balance: take it whenever G >= 1, to measure the two schedules against each other).
-  if (allow_cluster && max_ctas == 0 && num_sms > 0) {
+  // Cluster schedule: G = min(8, SMs / units, tiles per unit) CTAs per unit, one wave; it needs no
+  // q-prep and no merge grid. kClusterBalanced takes it when no CTA then runs more tiles than under
+  // the stream-K split, kClusterAny whenever G >= 1 (to measure the schedules against each other).
+  // Measured on GB300 (with the two-part fp16 weights) the split was faster at every size tried:
+  // 64 queries 54.2 vs 55.6 us (G = 2), 128 queries 93.9 vs 96.9 us (G = 1), 1 and 4 queries ~8 us
+  // faster than 8-CTA clusters; so kClusterDefault, the policy without flags, is the split.
+  if (policy != kClusterNone && max_ctas == 0 && num_sms > 0) {
     int64_t c = num_sms / s.units;
     if (c > 8) c = 8;
     if (c > s.tiles_per_unit) c = s.tiles_per_unit;
     if (c >= 1) {
       const int64_t per_cta_cluster = (s.tiles_per_unit + c - 1) / c;
       const int64_t per_cta_split = (s.total_tiles + s.ctas - 1) / s.ctas;
-      if (any_balance || per_cta_cluster <= per_cta_split) {
+      const bool take = policy == kClusterAny || (policy == kClusterBalanced && per_cta_cluster <= per_cta_split);
+      if (take) {
         s.cluster = (int)c;
         s.ctas = (int)(s.units * c);
       }
@@ -163,17 +165,20 @@ static uint64_t next_call_tag() {
   return (z ^ (z >> 31)) | 1ull;
 }
 
-// The decode grid for these sizes on the current device: with NVFP4MLA_FLAG_CLUSTER, the cluster
-// schedule when make_schedule picks it and all its clusters can be resident at once (each CTA takes
-// a whole SM); else stream-K.
-static bool plan_on_device(int B, int Q, int H, int topk, uint32_t flags, DecodeSchedule* out) {
+// The decode grid for these sizes and flags on the current device: the stream-K split unless a
+// cluster flag makes make_schedule pick the cluster schedule and all its clusters can be resident
+// at once. (With results in host memory the split's merge grid streams them over the host link as
+// units finish; host_results keeps it there unless a cluster flag is given.)
+static bool plan_on_device(int B, int Q, int H, int topk, uint32_t flags, bool host_results, DecodeSchedule* out) {
   const int sms = device_sm_count();
   if (sms <= 0) return false;
-  const bool any = (flags & NVFP4MLA_FLAG_CLUSTER_ANY) != 0;
-  DecodeSchedule s = make_schedule(B, Q, H, topk, sms, (int)(flags & 0xFFFFu), (flags & NVFP4MLA_FLAG_CLUSTER) != 0, any);
+  ClusterPolicy policy = host_results ? kClusterNone : kClusterDefault;
+  if (flags & NVFP4MLA_FLAG_CLUSTER) policy = (flags & NVFP4MLA_FLAG_CLUSTER_ANY) ? kClusterAny : kClusterBalanced;
+  if (flags & NVFP4MLA_FLAG_SPLIT) policy = kClusterNone;
+  DecodeSchedule s = make_schedule(B, Q, H, topk, sms, (int)(flags & 0xFFFFu), policy);
   if (s.cluster > 1) {
     const int fit = max_active_clusters(H < kHeadsPerCta ? H : kHeadsPerCta, s.cluster);
-    if (fit < s.units) s = make_schedule(B, Q, H, topk, sms, (int)(flags & 0xFFFFu), false, false);
+    if (fit < s.units) s = make_schedule(B, Q, H, topk, sms, (int)(flags & 0xFFFFu), kClusterNone);
   }
   *out = s;
   return true;
@@ -185,7 +190,7 @@ namespace nvfp4mla {
 int decode_workspace_need(int B, int Q, int H, int topk, uint32_t flags, size_t* need) {
   if (!sizes_ok(B, Q, H, topk)) return NVFP4MLA_ERR_INVALID_ARG;
   DecodeSchedule s;
-  if (!plan_on_device(B, Q, H, topk, flags, &s)) return NVFP4MLA_ERR_CUDA;
+  if (!plan_on_device(B, Q, H, topk, flags, false, &s)) return NVFP4MLA_ERR_CUDA;
   if (s.total_tiles > (int64_t)INT32_MAX) return NVFP4MLA_ERR_UNSUPPORTED;
   *need = workspace_bytes_for(s, H);
   return NVFP4MLA_OK;
@@ -235,7 +240,7 @@ int mla_kv_pack(const void* latent, int64_t latent_row_stride, const void* rope,
 int sparse_mla_decode_plan(int B, int Q, int H, int topk, uint32_t flags, int* ctas, int* cluster) {
   if (!sizes_ok(B, Q, H, topk)) return NVFP4MLA_ERR_INVALID_ARG;
   DecodeSchedule s;
-  if (!plan_on_device(B, Q, H, topk, flags, &s)) return NVFP4MLA_ERR_CUDA;
+  if (!plan_on_device(B, Q, H, topk, flags, false, &s)) return NVFP4MLA_ERR_CUDA;
   if (ctas != nullptr) *ctas = s.ctas;
   if (cluster != nullptr) *cluster = s.cluster;
   return NVFP4MLA_OK;
@@ -245,7 +250,7 @@ size_t sparse_mla_decode_workspace_size(int B, int Q, int H, int topk, int num_s
   if (!sizes_ok(B, Q, H, topk)) return 0;
   if (num_sms <= 0) num_sms = device_sm_count();
   if (num_sms <= 0) return 0;
-  const DecodeSchedule s = make_schedule(B, Q, H, topk, num_sms, 0, false, false);
+  const DecodeSchedule s = make_schedule(B, Q, H, topk, num_sms, 0, kClusterNone);
   if (s.total_tiles > (int64_t)INT32_MAX) return 0;
   return workspace_bytes_for(s, H);
 }
@@ -272,7 +277,7 @@ int sparse_mla_decode(const void* q, const void* kv_cache, int64_t num_pages, co
       (dev_status != nullptr && pointer_kind(dev_status) != kPtrDevice))
     return NVFP4MLA_ERR_INVALID_ARG;
   DecodeSchedule s;
-  if (!plan_on_device(B, Q, H, topk, flags, &s)) return NVFP4MLA_ERR_CUDA;
+  if (!plan_on_device(B, Q, H, topk, flags, k_out == kPtrHost || k_lse == kPtrHost, &s)) return NVFP4MLA_ERR_CUDA;
   const size_t need = workspace_bytes_for(s, H);
   if (workspace == nullptr || workspace_bytes < need) return NVFP4MLA_ERR_WORKSPACE;
   if (!aligned(workspace, 256)) return NVFP4MLA_ERR_ALIGNMENT;

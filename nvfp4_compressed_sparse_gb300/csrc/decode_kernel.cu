@@ -69,7 +69,9 @@ struct alignas(16) Smem {
   uint64_t s_free;                   // softmax has read S of a tile (4 warps): S may be overwritten
   uint64_t v_ready[2];               // half h of the V rows of a tile is in shared memory (4 warps)
   uint64_t mask_full[2];             // vmask of a tile written (4 warps), by tile parity
-  uint64_t p_full[2];                // P of a tile written (128 threads), double-buffered by tile parity
+  // P of a tile written and O rescaled (128 threads). One P buffer serves every tile: P(k+1) is
+  // written after QK(k+1) completes, which each issuer queued behind its PV(k).
+  uint64_t p_full;
   uint64_t o_done;                   // last PV of a unit segment complete (2 issuers)
   uint64_t o_free;                   // epilogue has read O (128 threads)
   uint64_t q_full[2];                // half h of the unit's q image copied in (issuer h's copy)
@@ -517,7 +519,7 @@ struct MmaIssuer {
   __device__ __forceinline__ void pv(int64_t k, const TileInfo& ti) {
     if (ti.first && k > 0) ++ofree_waits;
     tc_fence_after();
-    const uint64_t pd = pd0 + (uint64_t)(((k & 1) * kPBytes) >> 4);
+    // P_hi and P_lo planes: the same V rows times each, into the same fp32 accumulator.
     // Row chunk w (tokens 32w..) of this half is released as soon as its UMMAs complete.
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
@@ -528,8 +530,9 @@ struct MmaIssuer {
         for (int kk = 0; kk < 2; ++kk) {
           const int ks = 2 * w + kk;
           const uint64_t a = vd + (uint64_t)((mb * 32768 + ks * 2048) >> 4);
-          const uint64_t bdesc = pd + (uint64_t)((ks * 2 * kPSbo) >> 4);
+          const uint64_t bdesc = pd0 + (uint64_t)((ks * 2 * kPSbo) >> 4);
           umma_ss(o_col + mb * NH, a, bdesc, kIdPV, (ti.first && ks == 0) ? 0u : 1u);
+          umma_ss(o_col + mb * NH, a, bdesc + (uint64_t)(kPBytes >> 4), kIdPV, 1u);
         }
       }
       umma_commit(&sm->vfree[which][w]);
@@ -575,7 +578,7 @@ __device__ void mma_loop(const DecodeParams& p, Smem* sm, uint8_t* vtile, uint8_
       }
     }
     // ---- PV(k)
-    ok = wait(sm, &sm->p_full[k & 1], (uint32_t)((k >> 1) & 1), p.status);
+    ok = wait(sm, &sm->p_full, (uint32_t)(k & 1), p.status);
     if (ok) ok = wait(sm, &sm->v_ready[which], (uint32_t)(k & 1), p.status);
     if (ok && ti.first && k > 0) ok = wait(sm, &sm->o_free, (uint32_t)(m.ofree_waits & 1), p.status);
     if (!ok) break;
@@ -730,32 +733,31 @@ __device__ bool softmax_loop(const DecodeParams& p, Smem* sm, uint8_t* ps, uint8
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(&sm->s_free);      // S read: the next QK and K tile may proceed
-    // ---- P = 2^(z - m) in fp16, row t of this tile's P buffer (MN-major: heads contiguous)
-    uint32_t pk[16];
+    // ---- P = 2^(z - m) as two fp16 parts, P_hi = fp16(p) and P_lo = fp16(p - P_hi), rows of the two
+    // P planes (MN-major: heads contiguous); PV multiplies V by both and accumulates them in fp32,
+    // so the weights carry ~22 bits instead of fp16's 11. (With P_hi alone, the rounding of a few
+    // heavy weights moved outputs that cancel to near zero, |out| << sum_t w_t |v_t|, by up to
+    // ~90 % of the tolerance on the outlier-heavy keys.) The row sums add the unrounded p.
 #pragma unroll
-    for (int h = 0; h < 32; h += 4) {
-      const float4 mv = *reinterpret_cast<const float4*>(&sm->m_used[h]);
-      const float mm[4] = {mv.x, mv.y, mv.z, mv.w};
-      float pp[4];
+    for (int c = 0; c < NH / 8; ++c) {          // 16-byte chunk c: heads 8c..8c+7
+      uint32_t hi[4], lo[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        pp[i] = (mm[i] == kNegInf) ? 0.f : ex2_approx(z[h + i] - mm[i]);
-        l_part[h + i] += pp[i];
+      for (int i = 0; i < 8; i += 2) {
+        const int h = 8 * c + i;
+        const float m0 = sm->m_used[h], m1 = sm->m_used[h + 1];
+        const float p0 = (m0 == kNegInf) ? 0.f : ex2_approx(z[h] - m0);
+        const float p1 = (m1 == kNegInf) ? 0.f : ex2_approx(z[h + 1] - m1);
+        l_part[h] += p0;
+        l_part[h + 1] += p1;
+        const __half2 ph = __floats2half2_rn(p0, p1);
+        const float2 fh = __half22float2(ph);
+        const __half2 pl = __floats2half2_rn(p0 - fh.x, p1 - fh.y);
+        hi[i >> 1] = *reinterpret_cast<const uint32_t*>(&ph);
+        lo[i >> 1] = *reinterpret_cast<const uint32_t*>(&pl);
       }
-      const __half2 h01 = __floats2half2_rn(pp[0], pp[1]);
-      const __half2 h23 = __floats2half2_rn(pp[2], pp[3]);
-      pk[h >> 1] = *reinterpret_cast<const uint32_t*>(&h01);
-      pk[(h >> 1) + 1] = *reinterpret_cast<const uint32_t*>(&h23);
-    }
-    uint8_t* pbuf = ps + (k & 1) * kPBytes;
-    if (NH == 32) {
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-        *reinterpret_cast<uint4*>(pbuf + t * 64 + ((c ^ ((t >> 1) & 3)) << 4)) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-    } else {
-#pragma unroll
-      for (int c = 0; c < 2; ++c)
-        *reinterpret_cast<uint4*>(pbuf + t * 32 + ((c ^ ((t >> 2) & 1)) << 4)) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      const int off = NH == 32 ? t * 64 + ((c ^ ((t >> 1) & 3)) << 4) : t * 32 + ((c ^ ((t >> 2) & 1)) << 4);
+      *reinterpret_cast<uint4*>(ps + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      *reinterpret_cast<uint4*>(ps + kPBytes + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
     fence_proxy_async_smem();
     // ---- a raised reference: O^T[dim, h] *= alpha[h] before PV(k) adds to it, once PV(k-1) has
@@ -782,7 +784,7 @@ __device__ bool softmax_loop(const DecodeParams& p, Smem* sm, uint8_t* ps, uint8
       tmem_wait_st();
       tc_fence_before();
     }
-    mbar_arrive(&sm->p_full[k & 1]);
+    mbar_arrive(&sm->p_full);
 
     if (ti.last) {
       // ---- epilogue: write this segment's unnormalised partial
@@ -972,8 +974,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     }
     mbar_init(&sm->s_full, 2);
     mbar_init(&sm->s_free, 4);
-    mbar_init(&sm->p_full[0], 128);
-    mbar_init(&sm->p_full[1], 128);
+    mbar_init(&sm->p_full, 128);
     mbar_init(&sm->o_done, 2);
     mbar_init(&sm->o_free, 128);
     mbar_init(&sm->q_full[0], kCluster ? 384 : 1);   // cluster mode: the converting threads

@@ -32,8 +32,11 @@ struct DecodeSchedule {
   int cluster;             // 0 = stream-K, else CTAs per unit
 };
 
-DecodeSchedule make_schedule(int B, int Q, int H, int topk, int num_sms, int max_ctas, bool allow_cluster,
-                             bool any_balance);
+// kClusterNone: stream-K split only; kClusterDefault: the policy without flags (the split, measured
+// faster); kClusterBalanced: the cluster schedule wherever it is as balanced as the split;
+// kClusterAny: whenever one wave of clusters fits.
+enum ClusterPolicy { kClusterNone, kClusterDefault, kClusterBalanced, kClusterAny };
+DecodeSchedule make_schedule(int B, int Q, int H, int topk, int num_sms, int max_ctas, ClusterPolicy policy);
 size_t workspace_bytes_for(const DecodeSchedule& s, int H);
 
 struct DecodeParams {

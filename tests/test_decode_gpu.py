@@ -48,13 +48,14 @@ SMALL = [
 
 
 @pytest.mark.parametrize("spec", SMALL, ids=lambda s: "B{B}Q{Q}H{H}K{topk}".format(**s))
-@pytest.mark.parametrize("max_ctas", [0, 1, 3])
+@pytest.mark.parametrize("max_ctas", [0, "split", 1, 3])
 def test_small_cases_match_oracle(spec, max_ctas):
     case = workloads.small_case(seed=100 + len(str(spec)), **spec)
     lat, rope, rows = _host_cache(case)
     cache = _gpu_cache(lat, rope, case.num_pages)
     np.testing.assert_array_equal(cache.cpu().numpy(), rows)
-    out, lse = _decode(case, cache, max_ctas=max_ctas)
+    kw = dict(cluster=False) if max_ctas == "split" else dict(max_ctas=max_ctas)   # 0: the default schedule
+    out, lse = _decode(case, cache, **kw)
     ref_out, ref_lse = attention.sparse_decode(case.q_bits, rows, case.page_table, case.topk_indices,
                                                case.seq_lens, case.softmax_scale)
     assert_close(out, lse, ref_out, ref_lse, f"{spec} max_ctas={max_ctas}")
@@ -81,7 +82,11 @@ CLUSTER = [
                          "B{B}Q{Q}H{H}K{topk}".format(**x))
 def test_cluster_schedule_matches_oracle(G, spec):
     ctas, cluster = m.sparse_mla_decode_plan(spec["B"], spec["Q"], spec["H"], spec["topk"], cluster=True)
-    assert m.sparse_mla_decode_plan(spec["B"], spec["Q"], spec["H"], spec["topk"])[1] == 0   # default: split
+    # default: the cluster schedule only for clusters of <= 2 CTAs that are at most two tiles per CTA
+    # less balanced than the split; NVFP4MLA_FLAG_SPLIT: never
+    default_g = m.sparse_mla_decode_plan(spec["B"], spec["Q"], spec["H"], spec["topk"])[1]
+    assert default_g in (0, cluster) and (default_g == 0 or default_g <= 2)
+    assert m.sparse_mla_decode_plan(spec["B"], spec["Q"], spec["H"], spec["topk"], cluster=False)[1] == 0
     if torch.cuda.get_device_properties(0).multi_processor_count == 152:
         assert cluster == G, (ctas, cluster)
     else:
@@ -207,8 +212,9 @@ def test_dense_control_equals_dense_oracle():
     assert_close(out, lse, ref_out, ref_lse, "dense control")
 
 
+@pytest.mark.parametrize("schedule", ["default", "split"])
 @pytest.mark.parametrize("cfg", [0, 1, 2, 3, 4])
-def test_full_size_case_every_unit(cfg):
+def test_full_size_case_every_unit(cfg, schedule):
     """The five cases at full size, in the launch configuration the bench uses; the cache is
     packed on the device from device-drawn bf16 rows, and every query token is checked against
     the oracle (which re-encodes the selected rows from the same bf16 inputs), so every
@@ -219,7 +225,7 @@ def test_full_size_case_every_unit(cfg):
     cache = torch.empty((case.num_pages, 64, 352), dtype=torch.uint8, device="cuda")
     m.mla_kv_pack(lat, rope, torch.arange(rows_total, device="cuda"), cache)
     status = torch.zeros(4, dtype=torch.int32, device="cuda")
-    out, lse = _decode(case, cache, dev_status=status)
+    out, lse = _decode(case, cache, dev_status=status, cluster=None if schedule == "default" else False)
     assert status.cpu().tolist() == [0, 0, 0, 0]
     units = [(b, j) for b in range(case.B) for j in range(case.Q)]
     ref = oracle_units_from_device_rows(case, units, lat, rope)
@@ -230,7 +236,7 @@ def test_full_size_case_every_unit(cfg):
     assert np.isfinite(o).all()
 
 
-@pytest.mark.parametrize("kw", [dict(), dict(max_ctas=1), dict(cluster=True)], ids=["split", "split-prep", "cluster"])
+@pytest.mark.parametrize("kw", [dict(cluster=False), dict(max_ctas=1), dict(cluster=True)], ids=["split", "split-prep", "cluster"])
 def test_pinned_host_buffers_match_device_buffers(kw):
     """q, page table, index lists, lengths, out and LSE in page-locked host memory (read and
     written by the kernels over the host link) give bitwise the device-buffer results."""

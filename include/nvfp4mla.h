@@ -256,6 +256,40 @@ int sparse_mla_decode_noalloc(const void* q, const void* kv_cache, int64_t num_p
                               int Q, int H, int topk, float softmax_scale, void* out, float* lse, int32_t* dev_status,
                               uint32_t flags, void* stream);
 
+/*
+ * indexer_topk: the index lists sparse_mla_decode reads, from the indexer's
+ * logits: for each query token, the top-k positions of its causal range.
+ *
+ * Source: "Prime Inference: serving GLM-5.3 to agents is a KV-cache
+ * problem", section "Decode: TP4, and the copies it keeps" (the indexer keeps
+ * the top-2,048 positions of a query); "Prime Inference" (translated), "Native
+ * NVFP4 sparse MLA decode kernel" (unused list entries are -1). The pages do
+ * not define the indexer's logits; they are this call's input.
+ *
+ * For query j of request b, the candidate positions are 0 .. seq_lens[b]-Q+j
+ * (the decode's causal rule), capped at logits_row_stride. The topk largest
+ * logits are selected; logits compare as floats with NaN below every number
+ * and -0.0 below +0.0, and among equal logits the smaller position is taken
+ * first. topk_indices[b, j, :] lists the selected positions in increasing
+ * order; when the range is shorter than topk, all of it is listed and the
+ * rest is -1. The result is exact (no approximation, deterministic).
+ *
+ *   logits            fp32 [B, Q, logits_row_stride] device memory; row (b, j)
+ *                     starts at logits + (b*Q + j) * logits_row_stride;
+ *                     16-byte aligned, stride a multiple of 4, 1 <= stride
+ *                     <= INT32_MAX
+ *   seq_lens          int32 [B] device memory: cached tokens of request b,
+ *                     including its Q new tokens
+ *   B, Q, topk        B >= 1, 1 <= Q <= 16, 1 <= topk <= NVFP4MLA_MAX_TOPK
+ *   topk_indices      int32 [B, Q, topk] device memory (output)
+ *   stream            cudaStream_t
+ * Returns NVFP4MLA_OK, NVFP4MLA_ERR_INVALID_ARG (bad sizes, NULL, memory that
+ * is not device memory of the current device), NVFP4MLA_ERR_ALIGNMENT or
+ * NVFP4MLA_ERR_CUDA; nothing is enqueued on an error.
+ */
+int indexer_topk(const float* logits, int64_t logits_row_stride, const int32_t* seq_lens, int B, int Q, int topk,
+                 int32_t* topk_indices, void* stream);
+
 /* Human-readable name of a return code (static string, never NULL). */
 const char* nvfp4mla_status_string(int status);
 

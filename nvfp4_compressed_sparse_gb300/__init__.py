@@ -7,7 +7,7 @@ raises; there is no CPU fallback.
 
 C entry points (see include/nvfp4mla.h): mla_kv_pack,
 sparse_mla_decode_workspace_size, sparse_mla_decode, sparse_mla_decode_plan,
-nvfp4mla_status_string.
+sparse_mla_decode_noalloc, indexer_topk, nvfp4mla_status_string.
 """
 from __future__ import annotations
 
@@ -64,6 +64,8 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.sparse_mla_decode.restype = i32
         lib.sparse_mla_decode_plan.argtypes = [i32, i32, i32, i32, u32, ctypes.POINTER(i32), ctypes.POINTER(i32)]
         lib.sparse_mla_decode_plan.restype = i32
+        lib.indexer_topk.argtypes = [vp, i64, vp, i32, i32, i32, vp, vp]
+        lib.indexer_topk.restype = i32
         lib.nvfp4mla_status_string.argtypes = [i32]
         lib.nvfp4mla_status_string.restype = ctypes.c_char_p
         _LIB = lib
@@ -121,6 +123,27 @@ def mla_kv_pack(latent, rope, slot_mapping, kv_cache, dev_status=None, stream=No
                                     n, _ptr(kv_cache), kv_cache.shape[0], _ptr(dev_status), _stream_ptr(stream))
     if rc != 0:
         raise NvFp4MlaError(rc, "mla_kv_pack")
+
+
+def indexer_topk(logits, seq_lens, topk: int, out=None, stream=None):
+    """Top-k positions of each query's causal range from indexer logits fp32 [B, Q, S] (S a multiple
+    of 4); seq_lens int32 [B]. Returns int32 [B, Q, topk] (increasing positions, -1 padded)."""
+    import torch
+    _check(logits, "logits", torch.float32, ndim=3)
+    dev = logits.device
+    _check(seq_lens, "seq_lens", torch.int32, dev, 1)
+    B, Q, S = logits.shape
+    if seq_lens.shape[0] != B:
+        raise ValueError("shape mismatch")
+    if out is None:
+        out = torch.empty((B, Q, topk), dtype=torch.int32, device=dev)
+    _check(out, "out", torch.int32, dev, 3)
+    if tuple(out.shape) != (B, Q, topk):
+        raise ValueError("out must be [B, Q, topk]")
+    rc = load_library().indexer_topk(_ptr(logits), S, _ptr(seq_lens), B, Q, topk, _ptr(out), _stream_ptr(stream))
+    if rc != 0:
+        raise NvFp4MlaError(rc, "indexer_topk")
+    return out
 
 
 def sparse_mla_decode_workspace_size(B: int, Q: int, H: int, topk: int, num_sms: int = 0) -> int:

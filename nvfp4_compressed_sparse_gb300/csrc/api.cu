@@ -237,6 +237,22 @@ int mla_kv_pack(const void* latent, int64_t latent_row_stride, const void* rope,
   return err == cudaSuccess ? NVFP4MLA_OK : NVFP4MLA_ERR_CUDA;
 }
 
+int indexer_topk(const float* logits, int64_t logits_row_stride, const int32_t* seq_lens, int B, int Q, int topk,
+                 int32_t* topk_indices, void* stream) {
+  if (B < 1 || Q < 1 || Q > 16 || topk < 1 || topk > NVFP4MLA_MAX_TOPK) return NVFP4MLA_ERR_INVALID_ARG;
+  if ((int64_t)B * Q > (int64_t)INT32_MAX) return NVFP4MLA_ERR_UNSUPPORTED;
+  if (logits == nullptr || seq_lens == nullptr || topk_indices == nullptr) return NVFP4MLA_ERR_INVALID_ARG;
+  if (logits_row_stride < 1 || logits_row_stride > (int64_t)INT32_MAX) return NVFP4MLA_ERR_INVALID_ARG;
+  if (!aligned(logits, 16) || (logits_row_stride % 4) != 0) return NVFP4MLA_ERR_ALIGNMENT;
+  if (!aligned(seq_lens, 4) || !aligned(topk_indices, 4)) return NVFP4MLA_ERR_ALIGNMENT;
+  if (pointer_kind(logits) != kPtrDevice || pointer_kind(seq_lens) != kPtrDevice ||
+      pointer_kind(topk_indices) != kPtrDevice)
+    return NVFP4MLA_ERR_INVALID_ARG;
+  const cudaError_t err = launch_topk(logits, logits_row_stride, seq_lens, B, Q, topk, topk_indices,
+                                      static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? NVFP4MLA_OK : NVFP4MLA_ERR_CUDA;
+}
+
 int sparse_mla_decode_plan(int B, int Q, int H, int topk, uint32_t flags, int* ctas, int* cluster) {
   if (!sizes_ok(B, Q, H, topk)) return NVFP4MLA_ERR_INVALID_ARG;
   DecodeSchedule s;

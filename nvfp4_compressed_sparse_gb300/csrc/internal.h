@@ -75,6 +75,9 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);
 int max_active_clusters(int heads_per_cta, int cluster);   // clusters of the decode grid that fit at once
 cudaError_t launch_merge(const DecodeParams& p, cudaStream_t stream);
 
+cudaError_t launch_topk(const float* logits, int64_t stride, const int32_t* seq_lens, int B, int Q, int K,
+                        int32_t* out, cudaStream_t stream);
+
 int device_sm_count();
 // Workspace bytes sparse_mla_decode needs for these sizes and flags on the current device (same
 // checks and return codes as the call).

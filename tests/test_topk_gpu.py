@@ -1,0 +1,95 @@
+"""indexer_topk on the GPU against the oracle (bit-exact index lists), and the index lists it
+writes feeding sparse_mla_decode on the same stream."""
+import numpy as np
+import pytest
+import torch
+
+import nvfp4_compressed_sparse_gb300 as m
+import workloads
+from oracle import attention, pack, topk
+from tests.gpu_util import assert_close, bf16_dev, i32
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(logits, L, Q, K):
+    out = m.indexer_topk(torch.from_numpy(logits).cuda(), i32(L), K)
+    torch.cuda.synchronize()
+    return out.cpu().numpy()
+
+
+@pytest.mark.parametrize("B,Q,S,K", [(3, 1, 1000, 64), (2, 4, 20000, 2048), (4, 2, 9000, 100), (1, 1, 64, 2048),
+                                     (2, 3, 40000, 8192), (5, 1, 8, 3)])
+def test_random_rows_with_ties_nan_and_signed_zero(B, Q, S, K):
+    rng = np.random.default_rng(B * 1000 + S)
+    logits = rng.standard_normal((B, Q, S)).astype(np.float32)
+    logits[0] = np.round(logits[0] * 4) / 4                      # many ties
+    flat = logits.reshape(-1)
+    flat[rng.integers(0, flat.size, size=max(1, flat.size // 200))] = np.nan
+    flat[rng.integers(0, flat.size, size=max(1, flat.size // 200))] = -0.0
+    flat[rng.integers(0, flat.size, size=max(1, flat.size // 200))] = 0.0
+    flat[rng.integers(0, flat.size, size=max(1, flat.size // 500))] = np.inf
+    L = rng.integers(1, S + Q + 3, size=B).astype(np.int32)      # some ranges exceed the row (capped)
+    L[0] = S + Q - 1                                               # the full row for the last query
+    np.testing.assert_array_equal(_run(logits, L, Q, K), topk.select(logits, L, Q, K))
+
+
+def test_degenerate_rows():
+    S, K = 5000, 2048
+    logits = np.stack([np.full(S, 1.5, np.float32), np.full(S, np.nan, np.float32),
+                       np.arange(S, dtype=np.float32)[::-1].copy(), -np.arange(S, dtype=np.float32)])[:, None]
+    L = np.array([S, S, S, 1000], np.int32)
+    np.testing.assert_array_equal(_run(logits, L, 1, K), topk.select(logits, L, 1, K))
+
+
+def test_headline_shape_is_exact():
+    """B=64 query tokens, ranges uniform in [70K, 160K], K = 2,048, as in the decode workload."""
+    case = workloads.make_case(2)
+    S = int(case.seq_lens.max())
+    S = (S + 3) // 4 * 4
+    rng = np.random.default_rng(5)
+    logits = rng.standard_normal((case.B, 1, S)).astype(np.float32)
+    np.testing.assert_array_equal(_run(logits, case.seq_lens, 1, case.topk),
+                                  topk.select(logits, case.seq_lens, 1, case.topk))
+
+
+def test_topk_feeds_decode_on_one_stream():
+    case = workloads.small_case(B=3, Q=2, H=32, topk=512, L=(3000, 900, 2200), seed=61)
+    lat, rope = workloads.host_rows(case, np.arange(case.num_pages))
+    rows = pack.encode_rows(lat, rope).reshape(case.num_pages, 64, 352)
+    S = 3000
+    logits = np.random.default_rng(62).standard_normal((case.B, case.Q, S)).astype(np.float32)
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        cache = torch.zeros((case.num_pages, 64, 352), dtype=torch.uint8, device="cuda")
+        m.mla_kv_pack(bf16_dev(lat), bf16_dev(rope), torch.arange(case.num_pages * 64, device="cuda"), cache,
+                      stream=stream)
+        sl = i32(case.seq_lens)
+        idx = m.indexer_topk(torch.from_numpy(logits).cuda(), sl, case.topk, stream=stream)
+        out, lse = m.sparse_mla_decode(bf16_dev(case.q_bits), cache, i32(case.page_table), idx, sl,
+                                       case.softmax_scale, stream=stream)
+    torch.cuda.synchronize()
+    ref_idx = topk.select(logits, case.seq_lens, case.Q, case.topk)
+    np.testing.assert_array_equal(idx.cpu().numpy(), ref_idx)
+    ref_out, ref_lse = attention.sparse_decode(case.q_bits, rows, case.page_table, ref_idx, case.seq_lens,
+                                               case.softmax_scale)
+    assert_close(out, lse, ref_out, ref_lse, "indexer_topk -> sparse_mla_decode")
+
+
+def test_rejects_bad_arguments_before_launch():
+    import ctypes
+    lib = m.load_library()
+    V = ctypes.c_void_p
+    x = torch.arange(64, dtype=torch.float32, device="cuda").reshape(1, 1, 64)
+    sl = torch.full((1,), 64, dtype=torch.int32, device="cuda")
+    out = torch.full((1, 1, 8), 7, dtype=torch.int32, device="cuda")
+    P = lambda t: V(t.data_ptr())
+    assert lib.indexer_topk(P(x), 64, P(sl), 1, 1, 8, P(out), None) == 0
+    assert lib.indexer_topk(P(x), 62, P(sl), 1, 1, 8, P(out), None) == 2          # stride not a multiple of 4
+    assert lib.indexer_topk(V(x.data_ptr() + 4), 64, P(sl), 1, 1, 8, P(out), None) == 2
+    assert lib.indexer_topk(P(x), 64, P(sl), 1, 1, 0, P(out), None) == 1
+    assert lib.indexer_topk(P(x), 64, P(sl), 1, 17, 8, P(out), None) == 1
+    host = torch.zeros((1, 1, 64), dtype=torch.float32)
+    assert lib.indexer_topk(P(host), 64, P(sl), 1, 1, 8, P(out), None) == 1       # host memory
+    torch.cuda.synchronize()
+    assert out.cpu().tolist() == [[[56, 57, 58, 59, 60, 61, 62, 63]]]            # only the first call ran

@@ -361,6 +361,48 @@ def extra_configs(m, workloads, dev, stream, flush, hbm, steps):
     return res
 
 
+def topk_table(m, case, cache, dev, stream, flush, hbm, steps):
+    """indexer_topk on the headline case's query tokens (seeded N(0,1) fp32 logits over each causal
+    range), alone and followed by sparse_mla_decode on the same stream. Algorithmic bytes: every
+    logit in range read once plus the index lists written."""
+    import torch
+    g = torch.Generator(device=dev)
+    g.manual_seed(2024)
+    S = (int(case.seq_lens.max()) + 3) // 4 * 4
+    logits = torch.randn((case.B, case.Q, S), generator=g, device=dev, dtype=torch.float32)
+    q, pt, _, sl = device_inputs(case, dev)
+    idx = torch.empty((case.B, case.Q, case.topk), dtype=torch.int32, device=dev)
+    out = torch.empty((case.B, case.Q, case.H, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((case.B, case.Q, case.H), dtype=torch.float32, device=dev)
+    ws = torch.empty(max(1, m.sparse_mla_decode_workspace_size(case.B, case.Q, case.H, case.topk)),
+                     dtype=torch.uint8, device=dev)
+    res = {}
+    for name, with_decode in (("topk", False), ("topk_then_decode", True)):
+        ev = []
+        for i in range(5 + steps):
+            flush.zero_()
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            e[0].record(stream)
+            m.indexer_topk(logits, sl, case.topk, out=idx, stream=stream)
+            if with_decode:
+                m.sparse_mla_decode(q, cache, pt, idx, sl, case.softmax_scale, out=out, lse=lse, workspace=ws,
+                                    stream=stream)
+            e[1].record(stream)
+            if i >= 5:
+                ev.append(e)
+        torch.cuda.synchronize(dev)
+        res[name + "_us"] = statistics.fmean(a.elapsed_time(b) for a, b in ev) * 1e3
+    in_range = sum(max(0, min(int(case.seq_lens[b]) - case.Q + j + 1, S)) for b in range(case.B)
+                   for j in range(case.Q))
+    nbytes = 4 * in_range + 4 * case.B * case.Q * case.topk
+    t = res["topk_us"] * 1e-6
+    res.update({"rows": case.B * case.Q, "topk": case.topk, "logits": "N(0,1) fp32, seeded",
+                "algorithmic_bytes": nbytes, "achieved_gbs": nbytes / t / 1e9,
+                "frac_of_measured_hbm": nbytes / t / 1e9 / hbm,
+                "launches": "one CTA per query row (64 of the SMs)"})
+    return res
+
+
 def schedule_table(m, workloads, case, cache, dev, stream, flush, steps):
     """Split vs cluster schedule (forced wherever one wave of clusters fits) for the first B requests
     of the headline case; cluster_size 0 = no wave of clusters fits."""
@@ -511,6 +553,7 @@ def run_gpu(args, world, rank, local):
     }
     if not args.no_extra and world == 1:
         result["schedules"] = schedule_table(m, workloads, case, cache, dev, stream, flush, min(K, 200))
+        result["indexer_topk"] = topk_table(m, case, cache, dev, stream, flush, hbm, min(K, 200))
         del cache, hq, hpt, htk, hsl, hout, hlse, ws
         torch.cuda.empty_cache()
         result["configs"] = extra_configs(m, workloads, dev, stream, flush, hbm, min(K, 200))

@@ -8,14 +8,27 @@
 // smaller position, NaN below every number; the list holds the positions in increasing order,
 // -1 padded when the range is shorter than K.
 //
-// GB300 design: one 1024-thread CTA per query row, an exact radix select on order-preserving
-// 32-bit keys. Three histogram sweeps (key bits 31..20, 19..8, 7..0, each over the keys that
-// match the digits found so far) find the threshold key T and how many keys equal to T are
-// taken; one compaction sweep writes the positions. Every sweep is coalesced: a thread owns 8
-// consecutive positions (two 16-byte loads), a warp 1 KB of the row, and two such groups are in
-// flight per thread. The compaction keeps position order with one block-wide scan of packed
-// (greater, tie) counts per 8,192 positions.
+// GB300 design: one 1024-thread CTA per query row; an exact radix select on order-preserving
+// 32-bit keys, in three tiers that each verify their own precondition and hand the row to the
+// next one when it fails:
+//   1. sampled bound (rows up to 262,144 positions, K <= 4,096): a 12-bit histogram of a 1/16
+//      sample (8 positions in every 128) gives a key bound with about 1.5 K keys of the row
+//      expected above it; one sweep keeps every key at or above it (a single float compare per
+//      logit) as a candidate in shared memory; with at least K and at most 8,192 candidates the
+//      select finishes there (below);
+//   2. full histogram (rows up to 262,144 positions): a 4,096-bin histogram of the keys' top 12
+//      bits over the row gives the bin of the K-th largest key; a second sweep marks the
+//      positions above that bin in a bitmap and keeps the bin's keys as candidates;
+//   3. general: the remaining digits by sweeps over the row, then a position-ordered compaction
+//      with one block scan of packed (greater, tie) counts per 8,192 positions.
+// Finishing from candidates: the remaining digits of the threshold key T and the number R of
+// keys equal to T that are taken come from histogram rounds over the candidates; candidates above
+// T and equal to T go into two position bitmaps, and one block-wide scan over the bitmap words
+// writes the positions in increasing order (the ties: the first R). The sweeps are coalesced
+// 16-byte loads, 128 bytes per thread in flight.
 #include <cuda_runtime.h>
+
+#include <mutex>
 
 #include "internal.h"
 
@@ -25,27 +38,37 @@ namespace {
 constexpr int kTkThreads = 1024;
 constexpr int kTkPer = 8;                        // consecutive positions per thread per group
 constexpr int kTkGroup = kTkThreads * kTkPer;    // positions per group (8,192)
+constexpr int kTkCandCap = 8192;                 // candidates kept in shared memory (fast path)
+constexpr int kTkMapWords = 8192;                // bitmap words: rows up to 262,144 positions (fast path)
 
 // Unsigned order of the key = selection order of the float (NaN lowest, -0.0 below +0.0).
+// The sign flip maps negative NaNs to [0, 0x007FFFFE] and positive NaNs to (0xFF800000, 2^32);
+// one unsigned range test on k - key(-inf) sends both to 0.
 __device__ __forceinline__ uint32_t order_key(uint32_t bits) {
-  if ((bits & 0x7FFFFFFFu) > 0x7F800000u) return 0u;   // NaN
-  return (bits & 0x80000000u) ? ~bits : (bits | 0x80000000u);
+  const uint32_t k = bits ^ ((uint32_t)((int32_t)bits >> 31) | 0x80000000u);
+  return (k - 0x007FFFFFu) > 0xFF000001u ? 0u : k;
 }
 
-// Keys of positions p0..p0+7 of the row; positions >= n get key 0 and valid = 0.
+__device__ __forceinline__ void keys8(uint4 a, uint4 b, uint32_t (&k)[kTkPer]) {
+  k[0] = order_key(a.x); k[1] = order_key(a.y); k[2] = order_key(a.z); k[3] = order_key(a.w);
+  k[4] = order_key(b.x); k[5] = order_key(b.y); k[6] = order_key(b.z); k[7] = order_key(b.w);
+}
+
+// Keys of positions p0..p0+7 of the row; positions >= n get key 0 and valid = 0. kLastUse loads
+// evict-first (the row's last sweep); otherwise the lines stay in L2 for the next sweep.
+template <bool kLastUse = true>
 __device__ __forceinline__ uint32_t load_keys(const float* row, int64_t p0, int64_t n, uint32_t (&k)[kTkPer]) {
   if (p0 + kTkPer <= n) {
-    const uint4 a = __ldcs(reinterpret_cast<const uint4*>(row + p0));
-    const uint4 b = __ldcs(reinterpret_cast<const uint4*>(row + p0) + 1);
-    k[0] = order_key(a.x); k[1] = order_key(a.y); k[2] = order_key(a.z); k[3] = order_key(a.w);
-    k[4] = order_key(b.x); k[5] = order_key(b.y); k[6] = order_key(b.z); k[7] = order_key(b.w);
+    const uint4* p = reinterpret_cast<const uint4*>(row + p0);
+    if (kLastUse) keys8(__ldcs(p), __ldcs(p + 1), k);
+    else keys8(__ldg(p), __ldg(p + 1), k);
     return 0xFFu;
   }
   uint32_t valid = 0;
 #pragma unroll
   for (int i = 0; i < kTkPer; ++i) {
     const bool in = p0 + i < n;
-    k[i] = in ? order_key(__float_as_uint(__ldcs(row + p0 + i))) : 0u;
+    k[i] = in ? order_key(__float_as_uint(kLastUse ? __ldcs(row + p0 + i) : __ldg(row + p0 + i))) : 0u;
     valid |= (in ? 1u : 0u) << i;
   }
   return valid;
@@ -81,13 +104,291 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* w
 struct TopkShared {
   uint32_t hist[4096];
   uint32_t warp_sums[32];
-  uint32_t found_digit, found_rem;
+  uint32_t found_digit, found_rem, cand_count;
+  uint32_t cand_key[kTkCandCap];
+  int32_t cand_pos[kTkCandCap];
+  uint32_t gt_map_[kTkMapWords];   // positions whose key is above the threshold key
+  uint32_t eq_map_[kTkMapWords];   // positions whose key equals it
 };
+
+__device__ __forceinline__ uint32_t* gt_map(TopkShared& sh) { return sh.gt_map_; }
+__device__ __forceinline__ uint32_t* eq_map(TopkShared& sh) { return sh.eq_map_; }
+
+// The digit of the rem-th largest key from a filled histogram (bins scanned from the top):
+// updates prefix/pmask with the digit at `shift` and rem with the rank left inside its bin.
+__device__ __forceinline__ void take_digit(TopkShared& sh, int bins, int shift, uint32_t& prefix, uint32_t& pmask,
+                                           uint32_t& rem) {
+  const int t = threadIdx.x;
+  const int per = bins / kTkThreads > 0 ? bins / kTkThreads : 1;
+  const int hi = bins - per * t;          // this thread owns bins [hi - per, hi)
+  uint32_t mine = 0;
+  if (hi > 0)
+    for (int i = 1; i <= per; ++i) mine += sh.hist[hi - i];
+  uint32_t total;
+  const uint32_t above = block_exclusive_scan(mine, sh.warp_sums, &total);   // counts in higher bins
+  if (hi > 0 && above < rem && above + mine >= rem) {
+    uint32_t cum = above;
+    for (int i = 1; i <= per; ++i) {
+      const uint32_t h = sh.hist[hi - i];
+      if (cum + h >= rem) {
+        sh.found_digit = (uint32_t)(hi - i);
+        sh.found_rem = rem - cum;
+        break;
+      }
+      cum += h;
+    }
+  }
+  __syncthreads();
+  prefix |= sh.found_digit << shift;
+  pmask |= (uint32_t)(bins - 1) << shift;
+  rem = sh.found_rem;
+  __syncthreads();
+}
+
+// Histogram of the digit at `shift` over the row's keys that match prefix under pmask.
+template <bool kFiltered>
+__device__ __forceinline__ void global_histogram(TopkShared& sh, const float* row, int64_t n, int shift, int bins,
+                                                 uint32_t prefix, uint32_t pmask) {
+  const int t = threadIdx.x;
+  for (int i = t; i < bins; i += kTkThreads) sh.hist[i] = 0;
+  __syncthreads();
+  const uint32_t dmask = (uint32_t)(bins - 1);
+  int64_t base = 0;
+  // full sweeps of 4 groups: no per-position checks
+#pragma unroll 1
+  for (; base + 4 * kTkGroup <= n; base += 4 * kTkGroup) {
+    uint4 a[4], b[4];
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      const uint4* p = reinterpret_cast<const uint4*>(row + base + g * kTkGroup + t * kTkPer);
+      a[g] = __ldg(p);
+      b[g] = __ldg(p + 1);
+    }
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      uint32_t k[kTkPer];
+      keys8(a[g], b[g], k);
+#pragma unroll
+      for (int i = 0; i < kTkPer; ++i)
+        if (!kFiltered || (k[i] & pmask) == prefix) atomicAdd(&sh.hist[(k[i] >> shift) & dmask], 1u);
+    }
+  }
+#pragma unroll 1
+  for (; base < n; base += kTkGroup) {
+    uint32_t k[kTkPer];
+    const uint32_t v = load_keys(row, base + (int64_t)t * kTkPer, n, k);
+#pragma unroll
+    for (int i = 0; i < kTkPer; ++i)
+      if (((v >> i) & 1u) && (!kFiltered || (k[i] & pmask) == prefix))
+        atomicAdd(&sh.hist[(k[i] >> shift) & dmask], 1u);
+  }
+  __syncthreads();
+}
+
+// One element of the candidate sweep: above the top digit -> selected, equal -> candidate.
+__device__ __forceinline__ void classify(TopkShared& sh, uint32_t k, int32_t pos, uint32_t d1) {
+  const uint32_t d = k >> 20;
+  if (d >= d1) {
+    if (d > d1) {
+      atomicOr(&gt_map(sh)[pos >> 5], 1u << (pos & 31));
+    } else {
+      const uint32_t slot = atomicAdd(&sh.cand_count, 1u);
+      if (slot < (uint32_t)kTkCandCap) {
+        sh.cand_key[slot] = k;
+        sh.cand_pos[slot] = pos;
+      }
+    }
+  }
+}
+
+// Candidate sweep over positions [0, n) (row relative). With kFloatTest the hot loop tests each
+// logit against f_lo, the smallest float whose key reaches the top digit d1 (valid for
+// 8 <= d1 <= 0xFF8, where f_lo is a number and no NaN passes); the exact key is formed only for the few that pass.
+// Float order equals key order except that -0.0 == +0.0 there, so the test passes a superset
+// and classify() decides exactly.
+template <bool kFloatTest>
+__device__ __forceinline__ void candidate_sweep(TopkShared& sh, const float* row, int64_t n, uint32_t d1,
+                                                float f_lo) {
+  const int t = threadIdx.x;
+  int64_t base = 0;
+#pragma unroll 1
+  for (; base + 4 * kTkGroup <= n; base += 4 * kTkGroup) {
+    float4 a[4], c[4];
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      const float4* p = reinterpret_cast<const float4*>(row + base + g * kTkGroup + t * kTkPer);
+      a[g] = __ldcs(p);
+      c[g] = __ldcs(p + 1);
+    }
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      const float v[kTkPer] = {a[g].x, a[g].y, a[g].z, a[g].w, c[g].x, c[g].y, c[g].z, c[g].w};
+      const int32_t p0 = (int32_t)(base + g * kTkGroup + t * kTkPer);
+#pragma unroll
+      for (int i = 0; i < kTkPer; ++i) {
+        if (kFloatTest) {
+          if (v[i] >= f_lo) classify(sh, order_key(__float_as_uint(v[i])), p0 + i, d1);
+        } else {
+          classify(sh, order_key(__float_as_uint(v[i])), p0 + i, d1);
+        }
+      }
+    }
+  }
+#pragma unroll 1
+  for (; base < n; base += kTkGroup) {
+    uint32_t k[kTkPer];
+    const int64_t p0 = base + (int64_t)t * kTkPer;
+    const uint32_t v = load_keys(row, p0, n, k);
+#pragma unroll
+    for (int i = 0; i < kTkPer; ++i)
+      if ((v >> i) & 1u) classify(sh, k[i], (int32_t)(p0 + i), d1);
+  }
+}
+
+__device__ __forceinline__ void keep_candidate(TopkShared& sh, uint32_t k, int32_t pos, uint32_t lo) {
+  if (k >= lo) {
+    const uint32_t slot = atomicAdd(&sh.cand_count, 1u);
+    if (slot < (uint32_t)kTkCandCap) {
+      sh.cand_key[slot] = k;
+      sh.cand_pos[slot] = pos;
+    }
+  }
+}
+
+// The rest of the select over the c candidates in shared memory, which hold every key of the
+// row that can still be selected: the digits from d_start on (0: bits 31..20, 1: 19..8, 2: 7..0)
+// of the threshold key T and the count R of ties taken, then the bitmaps and the list.
+// clear_maps: start from empty bitmaps (else gt_map already holds the keys above the candidates).
+__device__ void finish_from_candidates(TopkShared& sh, uint32_t c, int d_start, uint32_t prefix, uint32_t pmask,
+                                       uint32_t rem, int W, bool clear_maps, int32_t* o) {
+  const int t = threadIdx.x;
+#pragma unroll 1
+  for (int d = d_start; d < 3; ++d) {
+    const int shift = d == 0 ? 20 : (d == 1 ? 8 : 0), bins = d < 2 ? 4096 : 256;
+    for (int i = t; i < bins; i += kTkThreads) sh.hist[i] = 0;
+    __syncthreads();
+    for (uint32_t i = t; i < c; i += kTkThreads) {
+      const uint32_t k = sh.cand_key[i];
+      if ((k & pmask) == prefix) atomicAdd(&sh.hist[(k >> shift) & (uint32_t)(bins - 1)], 1u);
+    }
+    __syncthreads();
+    take_digit(sh, bins, shift, prefix, pmask, rem);
+  }
+  const uint32_t T = prefix, R = rem;
+  if (clear_maps) {
+    for (int i = t; i < W; i += kTkThreads) gt_map(sh)[i] = 0, eq_map(sh)[i] = 0;
+    __syncthreads();
+  }
+  for (uint32_t i = t; i < c; i += kTkThreads) {
+    const uint32_t k = sh.cand_key[i];
+    const int32_t pos = sh.cand_pos[i];
+    if (k > T) atomicOr(&gt_map(sh)[pos >> 5], 1u << (pos & 31));
+    else if (k == T) atomicOr(&eq_map(sh)[pos >> 5], 1u << (pos & 31));
+  }
+  __syncthreads();
+  // emit in position order: a word's first slot = (selected bits before it) + min(tie bits
+  // before it, R); its ties are taken while the tie rank stays below R
+  const int wpt = (W + kTkThreads - 1) / kTkThreads;
+  const int w0 = t * wpt, w1 = min(W, w0 + wpt);
+  uint32_t g = 0, e = 0;
+  for (int w = w0; w < w1; ++w) g += __popc(gt_map(sh)[w]), e += __popc(eq_map(sh)[w]);
+  uint32_t tot;
+  const uint32_t ex = block_exclusive_scan(g | (e << 16), sh.warp_sums, &tot);
+  uint32_t gb = ex & 0xFFFFu, eb = ex >> 16;
+  for (int w = w0; w < w1; ++w) {
+    uint32_t gm = gt_map(sh)[w], em = eq_map(sh)[w];
+    uint32_t slot = gb + (eb < R ? eb : R);
+    gb += __popc(gm);
+    uint32_t keep = eb < R ? R - eb : 0u, taken = 0;   // the lowest (R - eb) tie bits of this word
+    eb += __popc(em);
+    while (em != 0u && keep != 0u) {
+      const uint32_t low = em & (0u - em);
+      taken |= low;
+      em ^= low;
+      --keep;
+    }
+    uint32_t sel = gm | taken;
+    while (sel != 0u) {
+      const int bit = __ffs(sel) - 1;
+      o[slot++] = w * 32 + bit;
+      sel &= sel - 1u;
+    }
+  }
+}
+
+// First tier: a sample of the row (8 positions in every 128) bounds the K-th largest key from
+// below, one sweep keeps every key at or above the bound as a candidate, and the select finishes
+// in shared memory. The bound is chosen so that about 1.5 K keys of the row are expected above
+// it; it is checked exactly (at least K candidates, at most the store's capacity), and on a miss
+// the caller takes the next tier. Returns true when the list is written (block-uniform).
+__device__ bool sample_select(TopkShared& sh, const float* row, int64_t n, int K, int32_t* o) {
+  const int t = threadIdx.x;
+  for (int i = t; i < 4096; i += kTkThreads) sh.hist[i] = 0;
+  if (t == 0) sh.cand_count = 0;
+  __syncthreads();
+  uint32_t mine = 0;
+  for (int64_t p0 = (int64_t)t * 128; p0 < n; p0 += (int64_t)kTkThreads * 128) {
+    uint32_t k[kTkPer];
+    const uint32_t v = load_keys<false>(row, p0, n, k);
+#pragma unroll
+    for (int i = 0; i < kTkPer; ++i)
+      if ((v >> i) & 1u) atomicAdd(&sh.hist[k[i] >> 20], 1u);
+    mine += __popc(v);
+  }
+  __syncthreads();
+  uint32_t m;
+  block_exclusive_scan(mine, sh.warp_sums, &m);
+  // rank (from the top) in the sample of the bound: ceil(1.5 K m / n) + 32
+  const int64_t want = (3 * (int64_t)K * m + 2 * n - 1) / (2 * n) + 32;
+  if (want > (int64_t)m) return false;
+  uint32_t prefix = 0, pmask = 0, rem = (uint32_t)want;
+  take_digit(sh, 4096, 20, prefix, pmask, rem);
+  const uint32_t db = prefix >> 20;
+  if (db < 8 || db > 0xFF8) return false;   // the bound would not be a number
+  const uint32_t lo = db << 20;
+  const float f_lo = __uint_as_float(lo >= 0x80000000u ? (lo & 0x7FFFFFFFu) : ~lo);
+
+  // the sweep: every key >= lo becomes a candidate (f_lo passes a superset, see candidate_sweep)
+  int64_t base = 0;
+#pragma unroll 1
+  for (; base + 4 * kTkGroup <= n; base += 4 * kTkGroup) {
+    float4 a[4], c[4];
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      const float4* p = reinterpret_cast<const float4*>(row + base + g * kTkGroup + t * kTkPer);
+      a[g] = __ldcs(p);
+      c[g] = __ldcs(p + 1);
+    }
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      const float v[kTkPer] = {a[g].x, a[g].y, a[g].z, a[g].w, c[g].x, c[g].y, c[g].z, c[g].w};
+      const int32_t p0 = (int32_t)(base + g * kTkGroup + t * kTkPer);
+#pragma unroll
+      for (int i = 0; i < kTkPer; ++i)
+        if (v[i] >= f_lo) keep_candidate(sh, order_key(__float_as_uint(v[i])), p0 + i, lo);
+    }
+  }
+#pragma unroll 1
+  for (; base < n; base += kTkGroup) {
+    uint32_t k[kTkPer];
+    const int64_t p0 = base + (int64_t)t * kTkPer;
+    const uint32_t v = load_keys(row, p0, n, k);
+#pragma unroll
+    for (int i = 0; i < kTkPer; ++i)
+      if ((v >> i) & 1u) keep_candidate(sh, k[i], (int32_t)(p0 + i), lo);
+  }
+  __syncthreads();
+  const uint32_t c = sh.cand_count;
+  if (c < (uint32_t)K || c > (uint32_t)kTkCandCap) return false;
+  finish_from_candidates(sh, c, 0, 0u, 0u, (uint32_t)K, (int)((n + 31) >> 5), true, o);
+  return true;
+}
 
 __global__ void __launch_bounds__(kTkThreads, 1) topk_kernel(const float* __restrict__ logits, int64_t stride,
                                                              const int32_t* __restrict__ seq_lens, int Q, int K,
                                                              int32_t* __restrict__ out) {
-  __shared__ TopkShared sh;
+  extern __shared__ __align__(16) unsigned char topk_smem[];
+  TopkShared& sh = *reinterpret_cast<TopkShared*>(topk_smem);
   const int64_t rowi = blockIdx.x;
   const int b = (int)(rowi / Q), j = (int)(rowi - (int64_t)b * Q);
   int64_t n = (int64_t)__ldg(seq_lens + b) - Q + j + 1;
@@ -101,51 +402,44 @@ __global__ void __launch_bounds__(kTkThreads, 1) topk_kernel(const float* __rest
   }
   const float* row = logits + rowi * stride;
 
-  // ---- radix select of the K-th largest key: digits of 12, 12 and 8 bits
+  const bool maps_fit = n <= 32 * (int64_t)kTkMapWords;
+  if (maps_fit && 2 * K <= kTkCandCap && sample_select(sh, row, n, K, o)) return;
+  __syncthreads();
+
+  // ---- second tier: the top 12 bits of the K-th largest key, over the whole row
   uint32_t prefix = 0, pmask = 0;
   uint32_t rem = (uint32_t)K;   // rank (from the top) of the wanted key among those matching prefix
-#pragma unroll 1
-  for (int d = 0; d < 3; ++d) {
-    const int shift = d == 0 ? 20 : (d == 1 ? 8 : 0), bins = d < 2 ? 4096 : 256;
-    for (int i = t; i < bins; i += kTkThreads) sh.hist[i] = 0;
+  global_histogram<false>(sh, row, n, 20, 4096, 0u, 0u);
+  take_digit(sh, 4096, 20, prefix, pmask, rem);
+
+  if (maps_fit) {
+    // one more sweep marks the keys above that digit in a position bitmap and
+    // keeps the keys in its bin as candidates; the rest of the select runs in shared memory.
+    const int W = (int)((n + 31) >> 5);
+    for (int i = t; i < W; i += kTkThreads) gt_map(sh)[i] = 0, eq_map(sh)[i] = 0;
+    if (t == 0) sh.cand_count = 0;
     __syncthreads();
-#pragma unroll 1
-    for (int64_t base = 0; base < n; base += 2 * kTkGroup) {
-      uint32_t k0[kTkPer], k1[kTkPer];
-      const uint32_t v0 = load_keys(row, base + (int64_t)t * kTkPer, n, k0);
-      const uint32_t v1 = load_keys(row, base + kTkGroup + (int64_t)t * kTkPer, n, k1);
-#pragma unroll
-      for (int i = 0; i < kTkPer; ++i) {
-        if (((v0 >> i) & 1u) && (k0[i] & pmask) == prefix) atomicAdd(&sh.hist[(k0[i] >> shift) & (bins - 1)], 1u);
-        if (((v1 >> i) & 1u) && (k1[i] & pmask) == prefix) atomicAdd(&sh.hist[(k1[i] >> shift) & (bins - 1)], 1u);
-      }
+    const uint32_t d1 = prefix >> 20;
+    if (d1 >= 8 && d1 <= 0xFF8) {   // f_lo finite or +inf; the digits between hold only NaN keys
+      const uint32_t lo = d1 << 20;
+      candidate_sweep<true>(sh, row, n, d1, __uint_as_float(lo >= 0x80000000u ? (lo & 0x7FFFFFFFu) : ~lo));
+    } else {
+      candidate_sweep<false>(sh, row, n, d1, 0.f);
     }
     __syncthreads();
-    // bins are scanned from the top: thread t owns bins [bins - per*(t+1), bins - per*t)
-    const int per = bins / kTkThreads > 0 ? bins / kTkThreads : 1;
-    const int hi = bins - per * t;          // exclusive upper end of this thread's bins
-    uint32_t mine = 0;
-    if (hi > 0)
-      for (int i = 1; i <= per; ++i) mine += sh.hist[hi - i];
-    uint32_t total;
-    const uint32_t above = block_exclusive_scan(mine, sh.warp_sums, &total);   // counts in higher bins
-    if (hi > 0 && above < rem && above + mine >= rem) {
-      uint32_t cum = above;
-      for (int i = 1; i <= per; ++i) {
-        const uint32_t h = sh.hist[hi - i];
-        if (cum + h >= rem) {
-          sh.found_digit = (uint32_t)(hi - i);
-          sh.found_rem = rem - cum;
-          break;
-        }
-        cum += h;
-      }
+    const uint32_t c = sh.cand_count;
+    if (c <= (uint32_t)kTkCandCap) {
+      finish_from_candidates(sh, c, 1, prefix, pmask, rem, W, false, o);
+      return;
     }
-    __syncthreads();
-    prefix |= sh.found_digit << shift;
-    pmask |= (uint32_t)(bins - 1) << shift;
-    rem = sh.found_rem;
-    __syncthreads();
+  }
+
+  // ---- general path: the remaining digits over the row in global memory
+#pragma unroll 1
+  for (int d = 1; d < 3; ++d) {
+    const int shift = d == 1 ? 8 : 0, bins = d == 1 ? 4096 : 256;
+    global_histogram<true>(sh, row, n, shift, bins, prefix, pmask);
+    take_digit(sh, bins, shift, prefix, pmask, rem);
   }
   const uint32_t T = prefix;      // the K-th largest key
   const uint32_t R = rem;         // keys equal to T that are taken (the first R in position order)
@@ -188,7 +482,23 @@ __global__ void __launch_bounds__(kTkThreads, 1) topk_kernel(const float* __rest
 
 cudaError_t launch_topk(const float* logits, int64_t stride, const int32_t* seq_lens, int B, int Q, int K,
                         int32_t* out, cudaStream_t stream) {
-  topk_kernel<<<(unsigned)((int64_t)B * Q), kTkThreads, 0, stream>>>(logits, stride, seq_lens, Q, K, out);
+  // the shared-memory opt-in is per device; set it once for each device that launches
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static bool done[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev < 0 || dev >= kMaxDevices || !done[dev]) {
+      err = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(TopkShared));
+      if (err != cudaSuccess) return err;
+      if (dev >= 0 && dev < kMaxDevices) done[dev] = true;
+    }
+  }
+  topk_kernel<<<(unsigned)((int64_t)B * Q), kTkThreads, sizeof(TopkShared), stream>>>(logits, stride, seq_lens, Q, K,
+                                                                                       out);
   return cudaGetLastError();
 }
 

@@ -29,17 +29,50 @@ def test_random_rows_with_ties_nan_and_signed_zero(B, Q, S, K):
     flat[rng.integers(0, flat.size, size=max(1, flat.size // 200))] = -0.0
     flat[rng.integers(0, flat.size, size=max(1, flat.size // 200))] = 0.0
     flat[rng.integers(0, flat.size, size=max(1, flat.size // 500))] = np.inf
+    flat[rng.integers(0, flat.size, size=max(1, flat.size // 500))] = -np.inf
+    bits = flat.view(np.uint32)                                     # NaNs with the sign set and with payloads
+    for pattern in (0xFFC00000, 0xFF800001, 0xFFFFFFFF, 0x7F800001, 0x7FFFFFFF):
+        bits[rng.integers(0, flat.size, size=max(1, flat.size // 1000))] = pattern
     L = rng.integers(1, S + Q + 3, size=B).astype(np.int32)      # some ranges exceed the row (capped)
     L[0] = S + Q - 1                                               # the full row for the last query
     np.testing.assert_array_equal(_run(logits, L, Q, K), topk.select(logits, L, Q, K))
 
 
-def test_degenerate_rows():
-    S, K = 5000, 2048
-    logits = np.stack([np.full(S, 1.5, np.float32), np.full(S, np.nan, np.float32),
+@pytest.mark.parametrize("S", [5000, 20000])      # 20,000 equal keys overflow the candidate store
+def test_degenerate_rows(S):
+    K = 2048
+    mixed = np.full(S, -np.inf, np.float32)
+    mixed.view(np.uint32)[::3] = 0xFF800001                         # negative NaN
+    mixed.view(np.uint32)[1::3] = 0x7FC00000                        # positive NaN
+    mixed[::97] = -1.0
+    logits = np.stack([np.full(S, 1.5, np.float32), np.full(S, np.nan, np.float32), mixed,
                        np.arange(S, dtype=np.float32)[::-1].copy(), -np.arange(S, dtype=np.float32)])[:, None]
-    L = np.array([S, S, S, 1000], np.int32)
+    L = np.array([S, S, S, S, 1000], np.int32)
     np.testing.assert_array_equal(_run(logits, L, 1, K), topk.select(logits, L, 1, K))
+
+
+def test_sample_that_misleads_the_bound():
+    """The sampled positions (8 in every 128) hold the largest logits, spread over several bins,
+    so a bound taken from the sample leaves fewer than K keys above it and the select must fall
+    back; a second row has its K-th key in a bin of more than 8,192 ties."""
+    rng = np.random.default_rng(11)
+    S, K = 40000, 2048
+    logits = rng.standard_normal((2, 1, S)).astype(np.float32)
+    sampled = (np.arange(S) >> 3) % 16 == 0
+    logits[0, 0, sampled] = 10 + 5 * rng.random(int(sampled.sum()), dtype=np.float32)
+    logits[1, 0, :12000] = 3.0
+    L = np.array([S, S], np.int32)
+    np.testing.assert_array_equal(_run(logits, L, 1, K), topk.select(logits, L, 1, K))
+
+
+def test_rows_longer_than_the_bitmap():
+    """Rows past 262,144 positions take the general path; one row stays just inside."""
+    rng = np.random.default_rng(9)
+    S = 300_000
+    logits = rng.standard_normal((3, 1, S)).astype(np.float32)
+    logits[1, 0] = np.round(logits[1, 0] * 8) / 8
+    L = np.array([S, 262_144, 270_000], np.int32)
+    np.testing.assert_array_equal(_run(logits, L, 1, 2048), topk.select(logits, L, 1, 2048))
 
 
 def test_headline_shape_is_exact():

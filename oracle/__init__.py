@@ -24,6 +24,9 @@ Modules:
   codec      bf16 / FP8-E4M3 / FP4-e2m1 value codecs
   pack       NVFP4 row encoding and the paged cache write
   attention  dequantisation and sparse / dense MLA decode in fp64
+  fp8rows    FP8 576-byte rows (the comparison cache format), the staged
+             NVFP4 -> FP8 copy, and decode over FP8 rows
+  topk       top-k position selection over indexer logits
   timing     runs the oracle on query tokens of a workload over spawned worker
              processes (the benchmark's CPU baseline and reference arm); it
              adds no arithmetic of its own
@@ -33,4 +36,4 @@ that do not come from this package (the pages' row arithmetic, torch's
 float8_e4m3fn conversion, exact rational brute force, closed forms, torch's
 scaled_dot_product_attention in fp64).
 """
-from . import codec, pack, attention  # noqa: F401
+from . import codec, pack, attention, fp8rows, topk  # noqa: F401

@@ -361,6 +361,64 @@ def extra_configs(m, workloads, dev, stream, flush, hbm, steps):
     return res
 
 
+def fp8_table(m, workloads, case, cache, dev, stream, flush, hbm, steps, native_ms):
+    """The pages' three decode paths on the headline case, same rows: native (352-byte NVFP4
+    rows), FP8 cache (576-byte FP8 rows packed from the same bf16 rows) and staged (NVFP4 rows
+    copied to a 576-byte FP8 buffer, then the FP8 decode over it). Device µs per step and the
+    algorithmic bytes per selected row each path moves through HBM."""
+    import torch
+    rows_total = case.num_pages * 64
+    cache8 = torch.empty((case.num_pages, 64, 576), dtype=torch.uint8, device=dev)
+    chunk = 1 << 20
+    for ci, s0 in enumerate(range(0, rows_total, chunk)):
+        n = min(chunk, rows_total - s0)
+        lat, rope = workloads.device_rows(case, n, dev, seed_offset=ci)
+        m.fp8_kv_pack(lat, rope, torch.arange(s0, s0 + n, device=dev), cache8)
+        del lat, rope
+    q, pt, tk, sl = device_inputs(case, dev)
+    out = torch.empty((case.B, case.Q, case.H, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((case.B, case.Q, case.H), dtype=torch.float32, device=dev)
+    ws = torch.empty(max(1, m.sparse_mla_decode_workspace_size(case.B, case.Q, case.H, case.topk)),
+                     dtype=torch.uint8, device=dev)
+    staging = m.nvfp4_stage_fp8(cache, pt, tk, sl, stream=stream)
+    staged, sidx, spt, ssl = staging
+    qs = q.reshape(case.B * case.Q, 1, case.H, 576)
+    out_s, lse_s = out.view(case.B * case.Q, 1, case.H, 512), lse.view(case.B * case.Q, 1, case.H)
+
+    def timed(fns):
+        ev = []
+        for i in range(5 + steps):
+            flush.zero_()
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(len(fns) + 1)]
+            e[0].record(stream)
+            for k, fn in enumerate(fns):
+                fn()
+                e[k + 1].record(stream)
+            if i >= 5:
+                ev.append(e)
+        torch.cuda.synchronize(dev)
+        return [statistics.fmean(e[k].elapsed_time(e[k + 1]) for e in ev) * 1e3 for k in range(len(fns))]
+
+    fp8_us, = timed([lambda: m.sparse_mla_decode_fp8(q, cache8, pt, tk, sl, case.softmax_scale, out=out, lse=lse,
+                                                     workspace=ws, stream=stream)])
+    stage_us, staged_dec_us = timed([
+        lambda: m.nvfp4_stage_fp8(cache, pt, tk, sl, staging=staging, stream=stream),
+        lambda: m.sparse_mla_decode_fp8(qs, staged, spt, sidx, ssl, case.softmax_scale, out=out_s, lse=lse_s,
+                                        workspace=ws, stream=stream)])
+    n_rows = int(sum(min(int(case.seq_lens[b]), case.topk) for b in range(case.B))) * case.Q
+    del cache8, staging, staged
+    torch.cuda.empty_cache()
+    return {
+        "rows_selected": n_rows,
+        "native": {"us": native_ms * 1e3, "bytes_per_row": 352},
+        "fp8_cache": {"us": fp8_us, "bytes_per_row": 576},
+        "staged": {"us": stage_us + staged_dec_us, "stage_us": stage_us, "fp8_decode_us": staged_dec_us,
+                   "bytes_per_row": 352 + 576 + 576},
+        "pages_reference_gb200_us": {"native": 12.0, "staged": 17.7, "fp8": 13.7,
+                                     "note": "the pages' numbers: 15 query tokens per launch on GB200"},
+    }
+
+
 def topk_table(m, case, cache, dev, stream, flush, hbm, steps):
     """indexer_topk on the headline case's query tokens (seeded N(0,1) fp32 logits over each causal
     range), alone and followed by sparse_mla_decode on the same stream. Algorithmic bytes: every
@@ -554,6 +612,7 @@ def run_gpu(args, world, rank, local):
     if not args.no_extra and world == 1:
         result["schedules"] = schedule_table(m, workloads, case, cache, dev, stream, flush, min(K, 200))
         result["indexer_topk"] = topk_table(m, case, cache, dev, stream, flush, hbm, min(K, 200))
+        result["fp8_paths"] = fp8_table(m, workloads, case, cache, dev, stream, flush, hbm, min(K, 200), mean_ms)
         del cache, hq, hpt, htk, hsl, hout, hlse, ws
         torch.cuda.empty_cache()
         result["configs"] = extra_configs(m, workloads, dev, stream, flush, hbm, min(K, 200))

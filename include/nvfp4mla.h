@@ -290,6 +290,72 @@ int sparse_mla_decode_noalloc(const void* q, const void* kv_cache, int64_t num_p
 int indexer_topk(const float* logits, int64_t logits_row_stride, const int32_t* seq_lens, int B, int Q, int topk,
                  int32_t* topk_indices, void* stream);
 
+/*
+ * FP8 comparison paths. The pages compare the native NVFP4 decode with (i) a
+ * staged path, where a gather kernel unpacks each selected 352-byte NVFP4 row
+ * into a 576-byte FP8 copy in GPU memory and an FP8 attention kernel reads the
+ * copy (352 + 576 + 576 = 1,504 bytes per selected row), and (ii) an FP8
+ * attention kernel over a cache of 576-byte FP8 rows ("Prime Inference:
+ * serving GLM-5.3 to agents is a KV-cache problem", section "A kernel that
+ * reads four bits directly"; "Prime Inference" (translated), "Native NVFP4
+ * sparse MLA decode kernel"). These entry points build both on GB300 with the
+ * same decode kernel, so the three paths differ only in the bytes they move.
+ *
+ * FP8 row (576 bytes): byte d < 512 is E4M3 of latent value d, byte 512 + r is
+ * E4M3 of rope value r; no scale. E4M3 rounding: nearest, ties to even,
+ * saturating at +-448; NaN becomes 0x7F with its sign bit.
+ */
+
+/*
+ * fp8_kv_pack: bf16 latent + rope rows -> 576-byte FP8 rows of a paged cache
+ * uint8 [num_pages, 64, 576] (device memory). Arguments, checks, slot rules and
+ * dev_status counting are those of mla_kv_pack.
+ */
+int fp8_kv_pack(const void* latent, int64_t latent_row_stride, const void* rope, int64_t rope_row_stride,
+                const int64_t* slot_mapping, int64_t num_tokens, void* kv_cache_fp8, int64_t num_pages,
+                int32_t* dev_status, void* stream);
+
+/*
+ * nvfp4_stage_fp8: the staging kernel of the staged path, for one decode
+ * step over an NVFP4 cache. For query (b, j) and list entry i it applies the
+ * decode's entry rule (see sparse_mla_decode); a usable entry's row is copied
+ * to staged row (b*Q + j)*topk + i as an FP8 row (latent value e2m1(code) x
+ * E4M3(scale), exact, rounded once to E4M3; a block with a NaN scale byte
+ * becomes 0x7F; rope bytes copied) and staged_indices[b*Q + j, i] = i;
+ * unusable entries get -1 and their staged rows are not written. It also
+ * writes staged_page_table[u, p] = u*(topk/64) + p and staged_seq_lens[u] =
+ * topk, so that sparse_mla_decode_fp8 over the staged rows as B*Q one-query
+ * requests (q viewed as [B*Q, 1, H, 576], cache = staged viewed as
+ * [B*Q*topk/64, 64, 576], max_pages_per_seq = topk/64) computes the step.
+ *   kv_cache ... seq_lens, B, Q   as sparse_mla_decode (device memory)
+ *   topk              64 <= topk <= NVFP4MLA_MAX_TOPK, a multiple of 64
+ *   staged            uint8 [B*Q*topk, 576] device memory, 16-byte aligned
+ *   staged_indices    int32 [B*Q, topk] device memory
+ *   staged_page_table int32 [B*Q, topk/64] device memory
+ *   staged_seq_lens   int32 [B*Q] device memory
+ *   dev_status        optional; counts bad index and bad page entries as
+ *                     sparse_mla_decode does
+ * Returns NVFP4MLA_OK, NVFP4MLA_ERR_INVALID_ARG, NVFP4MLA_ERR_ALIGNMENT,
+ * NVFP4MLA_ERR_UNSUPPORTED (B*Q*topk > INT32_MAX) or NVFP4MLA_ERR_CUDA.
+ */
+int nvfp4_stage_fp8(const void* kv_cache, int64_t num_pages, const int32_t* page_table, int64_t max_pages_per_seq,
+                    const int32_t* topk_indices, const int32_t* seq_lens, int B, int Q, int topk, void* staged,
+                    int32_t* staged_indices, int32_t* staged_page_table, int32_t* staged_seq_lens,
+                    int32_t* dev_status, void* stream);
+
+/*
+ * sparse_mla_decode_fp8: sparse_mla_decode over a cache of 576-byte FP8 rows
+ * (uint8 [num_pages, 64, 576], device memory): the same arguments, entry
+ * rules, outputs and workspace (sparse_mla_decode_workspace_size), computed
+ * by the same kernel with E4M3 -> fp16 conversion in place of the NVFP4
+ * unpacking. Always the split schedule; out and lse must be device memory
+ * (else NVFP4MLA_ERR_UNSUPPORTED).
+ */
+int sparse_mla_decode_fp8(const void* q, const void* kv_cache_fp8, int64_t num_pages, const int32_t* page_table,
+                          int64_t max_pages_per_seq, const int32_t* topk_indices, const int32_t* seq_lens, int B,
+                          int Q, int H, int topk, float softmax_scale, void* out, float* lse, void* workspace,
+                          size_t workspace_bytes, int32_t* dev_status, void* stream);
+
 /* Human-readable name of a return code (static string, never NULL). */
 const char* nvfp4mla_status_string(int status);
 

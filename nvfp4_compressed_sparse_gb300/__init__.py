@@ -7,7 +7,8 @@ raises; there is no CPU fallback.
 
 C entry points (see include/nvfp4mla.h): mla_kv_pack,
 sparse_mla_decode_workspace_size, sparse_mla_decode, sparse_mla_decode_plan,
-sparse_mla_decode_noalloc, indexer_topk, nvfp4mla_status_string.
+sparse_mla_decode_noalloc, indexer_topk, fp8_kv_pack, nvfp4_stage_fp8,
+sparse_mla_decode_fp8, nvfp4mla_status_string.
 """
 from __future__ import annotations
 
@@ -16,6 +17,7 @@ import os
 import threading
 
 ROW_BYTES = 352
+FP8_ROW_BYTES = 576
 PAGE_TOKENS = 64
 LATENT_DIM = 512
 ROPE_DIM = 64
@@ -66,6 +68,13 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.sparse_mla_decode_plan.restype = i32
         lib.indexer_topk.argtypes = [vp, i64, vp, i32, i32, i32, vp, vp]
         lib.indexer_topk.restype = i32
+        lib.fp8_kv_pack.argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, vp, vp]
+        lib.fp8_kv_pack.restype = i32
+        lib.nvfp4_stage_fp8.argtypes = [vp, i64, vp, i64, vp, vp, i32, i32, i32, vp, vp, vp, vp, vp, vp]
+        lib.nvfp4_stage_fp8.restype = i32
+        lib.sparse_mla_decode_fp8.argtypes = [vp, vp, i64, vp, i64, vp, vp, i32, i32, i32, i32, ctypes.c_float,
+                                              vp, vp, vp, sz, vp, vp]
+        lib.sparse_mla_decode_fp8.restype = i32
         lib.nvfp4mla_status_string.argtypes = [i32]
         lib.nvfp4mla_status_string.restype = ctypes.c_char_p
         _LIB = lib
@@ -215,3 +224,119 @@ def sparse_mla_decode(q, kv_cache, page_table, topk_indices, seq_lens, softmax_s
     if rc != 0:
         raise NvFp4MlaError(rc, "sparse_mla_decode")
     return out, lse
+
+
+# ------------------------------------------------------------------ FP8 comparison paths
+def fp8_kv_pack(latent, rope, slot_mapping, kv_cache_fp8, dev_status=None, stream=None) -> None:
+    """Encode bf16 latent [N,512] + rope [N,64] rows as 576-byte FP8 rows into kv_cache_fp8 uint8
+    [P,64,576] at slot_mapping (int64 [N])."""
+    import torch
+    _check(latent, "latent", torch.bfloat16, ndim=2, contiguous=False)
+    _check(rope, "rope", torch.bfloat16, latent.device, 2, contiguous=False)
+    _check(slot_mapping, "slot_mapping", torch.int64, latent.device, 1)
+    _check(kv_cache_fp8, "kv_cache_fp8", torch.uint8, latent.device, 3)
+    if latent.stride(1) != 1 or rope.stride(1) != 1:
+        raise ValueError("latent/rope rows must be contiguous along the feature axis")
+    n = latent.shape[0]
+    if latent.shape[1] != LATENT_DIM or rope.shape != (n, ROPE_DIM) or slot_mapping.shape[0] != n:
+        raise ValueError("shape mismatch")
+    if kv_cache_fp8.shape[1:] != (PAGE_TOKENS, FP8_ROW_BYTES):
+        raise ValueError("kv_cache_fp8 must be [num_pages, 64, 576]")
+    if dev_status is not None:
+        _check(dev_status, "dev_status", torch.int32, latent.device, 1)
+    rc = load_library().fp8_kv_pack(_ptr(latent), latent.stride(0), _ptr(rope), rope.stride(0), _ptr(slot_mapping),
+                                    n, _ptr(kv_cache_fp8), kv_cache_fp8.shape[0], _ptr(dev_status),
+                                    _stream_ptr(stream))
+    if rc != 0:
+        raise NvFp4MlaError(rc, "fp8_kv_pack")
+
+
+def nvfp4_stage_fp8(kv_cache, page_table, topk_indices, seq_lens, staging=None, dev_status=None, stream=None):
+    """The staging kernel of the staged path: FP8 copies of the selected NVFP4 rows of one decode
+    step. Returns staging = (staged uint8 [B*Q*K/64, 64, 576], staged_indices int32 [B*Q, 1, K],
+    staged_page_table int32 [B*Q, K/64], staged_seq_lens int32 [B*Q]), the cache, index lists,
+    page table and lengths of sparse_mla_decode_fp8 over the staged rows (pass a previous result
+    as staging to reuse its buffers)."""
+    import torch
+    _check(kv_cache, "kv_cache", torch.uint8, ndim=3)
+    dev = kv_cache.device
+    _check(page_table, "page_table", torch.int32, dev, 2)
+    _check(topk_indices, "topk_indices", torch.int32, dev, 3)
+    _check(seq_lens, "seq_lens", torch.int32, dev, 1)
+    B, Q, K = topk_indices.shape
+    if kv_cache.shape[1:] != (PAGE_TOKENS, ROW_BYTES) or seq_lens.shape[0] != B or page_table.shape[0] != B:
+        raise ValueError("shape mismatch")
+    if K % PAGE_TOKENS != 0:
+        raise ValueError("topk must be a multiple of 64 for the staged path")
+    U, P = B * Q, K // PAGE_TOKENS
+    if staging is None:
+        staging = (torch.empty((U * P, PAGE_TOKENS, FP8_ROW_BYTES), dtype=torch.uint8, device=dev),
+                   torch.empty((U, 1, K), dtype=torch.int32, device=dev),
+                   torch.empty((U, P), dtype=torch.int32, device=dev),
+                   torch.empty((U,), dtype=torch.int32, device=dev))
+    staged, sidx, spt, ssl = staging
+    if (staged.shape != (U * P, PAGE_TOKENS, FP8_ROW_BYTES) or sidx.shape != (U, 1, K) or spt.shape != (U, P)
+            or ssl.shape != (U,)):
+        raise ValueError("staging buffers do not match the step's sizes")
+    _check(staged, "staged", torch.uint8, dev)
+    for t, name in ((sidx, "staged_indices"), (spt, "staged_page_table"), (ssl, "staged_seq_lens")):
+        _check(t, name, torch.int32, dev)
+    if dev_status is not None:
+        _check(dev_status, "dev_status", torch.int32, dev, 1)
+    rc = load_library().nvfp4_stage_fp8(
+        _ptr(kv_cache), kv_cache.shape[0], _ptr(page_table), page_table.shape[1], _ptr(topk_indices),
+        _ptr(seq_lens), B, Q, K, _ptr(staged), _ptr(sidx), _ptr(spt), _ptr(ssl), _ptr(dev_status),
+        _stream_ptr(stream))
+    if rc != 0:
+        raise NvFp4MlaError(rc, "nvfp4_stage_fp8")
+    return staging
+
+
+def sparse_mla_decode_fp8(q, kv_cache_fp8, page_table, topk_indices, seq_lens, softmax_scale, out=None, lse=None,
+                          workspace=None, dev_status=None, stream=None):
+    """sparse_mla_decode over a cache of 576-byte FP8 rows (uint8 [P,64,576]); device tensors only."""
+    import torch
+    _check(kv_cache_fp8, "kv_cache_fp8", torch.uint8, ndim=3)
+    dev = kv_cache_fp8.device
+    if kv_cache_fp8.shape[1:] != (PAGE_TOKENS, FP8_ROW_BYTES):
+        raise ValueError("kv_cache_fp8 must be [num_pages, 64, 576]")
+    _check(q, "q", torch.bfloat16, dev, 4)
+    _check(page_table, "page_table", torch.int32, dev, 2)
+    _check(topk_indices, "topk_indices", torch.int32, dev, 3)
+    _check(seq_lens, "seq_lens", torch.int32, dev, 1)
+    B, Q, H, D = q.shape
+    K = topk_indices.shape[2]
+    if D != QK_DIM or topk_indices.shape[:2] != (B, Q) or seq_lens.shape[0] != B or page_table.shape[0] != B:
+        raise ValueError("shape mismatch")
+    if out is None:
+        out = torch.empty((B, Q, H, LATENT_DIM), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((B, Q, H), dtype=torch.float32, device=dev)
+    _check(out, "out", torch.bfloat16, dev, 4)
+    _check(lse, "lse", torch.float32, dev, 3)
+    if workspace is None:
+        workspace = torch.empty(max(sparse_mla_decode_workspace_size(B, Q, H, K), 1), dtype=torch.uint8, device=dev)
+    if dev_status is not None:
+        _check(dev_status, "dev_status", torch.int32, dev, 1)
+    rc = load_library().sparse_mla_decode_fp8(
+        _ptr(q), _ptr(kv_cache_fp8), kv_cache_fp8.shape[0], _ptr(page_table), page_table.shape[1],
+        _ptr(topk_indices), _ptr(seq_lens), B, Q, H, K, float(softmax_scale), _ptr(out), _ptr(lse), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream_ptr(stream))
+    if rc != 0:
+        raise NvFp4MlaError(rc, "sparse_mla_decode_fp8")
+    return out, lse
+
+
+def staged_sparse_mla_decode(q, kv_cache, page_table, topk_indices, seq_lens, softmax_scale, staging=None,
+                             out=None, lse=None, workspace=None, dev_status=None, stream=None):
+    """The staged path of one decode step: nvfp4_stage_fp8, then sparse_mla_decode_fp8 over the
+    staged rows as B*Q one-query requests. Same inputs and outputs as sparse_mla_decode (device
+    tensors). Returns (out, lse, staging)."""
+    B, Q, H, _ = q.shape
+    staging = nvfp4_stage_fp8(kv_cache, page_table, topk_indices, seq_lens, staging, dev_status, stream)
+    staged, sidx, spt, ssl = staging
+    o = None if out is None else out.view(B * Q, 1, H, LATENT_DIM)
+    s = None if lse is None else lse.view(B * Q, 1, H)
+    o, s = sparse_mla_decode_fp8(q.reshape(B * Q, 1, H, QK_DIM), staged, spt, sidx, ssl, softmax_scale, o, s,
+                                 workspace, dev_status, stream)
+    return o.view(B, Q, H, LATENT_DIM), s.view(B, Q, H), staging

@@ -136,14 +136,15 @@ static EncodeTiledFn encode_tiled_fn() {
   return fn;
 }
 
-// The cache as a 2-D tensor of uint32: rows of 88 words (352 B), one row per token slot. Row gathers use
-// TMA tile::gather4 with a one-row box; rows outside [0, rows) (the -1 of unused entries) read as zeros.
-static bool encode_cache_map(CUtensorMap* map, const void* cache, int64_t num_pages) {
+// The cache as a 2-D tensor of uint32: rows of row_bytes / 4 words (88 for the 352-byte NVFP4 row,
+// 144 for the 576-byte FP8 row), one row per token slot. Row gathers use TMA tile::gather4 with a
+// one-row box; rows outside [0, rows) (the -1 of unused entries) read as zeros.
+static bool encode_cache_map(CUtensorMap* map, const void* cache, int64_t num_pages, int row_bytes) {
   EncodeTiledFn fn = encode_tiled_fn();
   if (fn == nullptr) return false;
-  const cuuint64_t dims[2] = {(cuuint64_t)(kRowBytes / 4), (cuuint64_t)(num_pages * kPageTokens)};
-  const cuuint64_t strides[1] = {(cuuint64_t)kRowBytes};
-  const cuuint32_t box[2] = {(cuuint32_t)(kRowBytes / 4), 1};
+  const cuuint64_t dims[2] = {(cuuint64_t)(row_bytes / 4), (cuuint64_t)(num_pages * kPageTokens)};
+  const cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+  const cuuint32_t box[2] = {(cuuint32_t)(row_bytes / 4), 1};
   const cuuint32_t estr[2] = {1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(cache), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
@@ -271,16 +272,21 @@ size_t sparse_mla_decode_workspace_size(int B, int Q, int H, int topk, int num_s
   return workspace_bytes_for(s, H);
 }
 
-int sparse_mla_decode(const void* q, const void* kv_cache, int64_t num_pages, const int32_t* page_table,
-                      int64_t max_pages_per_seq, const int32_t* topk_indices, const int32_t* seq_lens, int B,
-                      int Q, int H, int topk, float softmax_scale, void* out, float* lse, void* workspace,
-                      size_t workspace_bytes, int32_t* dev_status, uint32_t flags, void* stream) {
+}  // extern "C"
+
+// sparse_mla_decode over either row format (row_fmt 0: 352-byte NVFP4 rows; 1: 576-byte FP8 rows,
+// split schedule and results in device memory only).
+static int decode_impl(const void* q, const void* kv_cache, int64_t num_pages, const int32_t* page_table,
+                       int64_t max_pages_per_seq, const int32_t* topk_indices, const int32_t* seq_lens, int B, int Q,
+                       int H, int topk, float softmax_scale, void* out, float* lse, void* workspace,
+                       size_t workspace_bytes, int32_t* dev_status, uint32_t flags, void* stream, int row_fmt) {
+  const int row_bytes = row_fmt == 1 ? kFp8RowBytes : kRowBytes;
   if (!sizes_ok(B, Q, H, topk)) return NVFP4MLA_ERR_INVALID_ARG;
   if (q == nullptr || kv_cache == nullptr || page_table == nullptr || topk_indices == nullptr ||
       seq_lens == nullptr || out == nullptr || lse == nullptr)
     return NVFP4MLA_ERR_INVALID_ARG;
   if (num_pages < 1 || max_pages_per_seq < 1) return NVFP4MLA_ERR_INVALID_ARG;
-  if (num_pages > (INT64_MAX / (kPageTokens * kRowBytes)) || num_pages > INT32_MAX) return NVFP4MLA_ERR_INVALID_ARG;
+  if (num_pages > (INT64_MAX / (kPageTokens * row_bytes)) || num_pages > INT32_MAX) return NVFP4MLA_ERR_INVALID_ARG;
   if (!(softmax_scale > 0.f) || softmax_scale != softmax_scale) return NVFP4MLA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(out, 16)) return NVFP4MLA_ERR_ALIGNMENT;
   if (!aligned(page_table, 4) || !aligned(topk_indices, 4) || !aligned(seq_lens, 4) || !aligned(lse, 4))
@@ -292,6 +298,10 @@ int sparse_mla_decode(const void* q, const void* kv_cache, int64_t num_pages, co
       k_lse == kPtrInvalid || pointer_kind(kv_cache) != kPtrDevice ||
       (dev_status != nullptr && pointer_kind(dev_status) != kPtrDevice))
     return NVFP4MLA_ERR_INVALID_ARG;
+  if (row_fmt == 1) {
+    if (k_out != kPtrDevice || k_lse != kPtrDevice) return NVFP4MLA_ERR_UNSUPPORTED;
+    flags = (flags & ~(NVFP4MLA_FLAG_CLUSTER | NVFP4MLA_FLAG_CLUSTER_ANY)) | NVFP4MLA_FLAG_SPLIT;
+  }
   DecodeSchedule s;
   if (!plan_on_device(B, Q, H, topk, flags, k_out == kPtrHost || k_lse == kPtrHost, &s)) return NVFP4MLA_ERR_CUDA;
   const size_t need = workspace_bytes_for(s, H);
@@ -302,7 +312,8 @@ int sparse_mla_decode(const void* q, const void* kv_cache, int64_t num_pages, co
   if (s.total_tiles > (int64_t)INT32_MAX) return NVFP4MLA_ERR_UNSUPPORTED;               // int32 tile numbers
 
   DecodeParams p{};
-  if (!encode_cache_map(&p.cache_map, kv_cache, num_pages)) return NVFP4MLA_ERR_CUDA;
+  if (!encode_cache_map(&p.cache_map, kv_cache, num_pages, row_bytes)) return NVFP4MLA_ERR_CUDA;
+  p.row_fmt = row_fmt;
   p.q = static_cast<const uint16_t*>(q);
   p.cache = static_cast<const uint8_t*>(kv_cache);
   p.num_pages = num_pages;
@@ -339,6 +350,76 @@ int sparse_mla_decode(const void* q, const void* kv_cache, int64_t num_pages, co
   if (launch_decode(p, st) != cudaSuccess) return NVFP4MLA_ERR_CUDA;
   if (p.cluster == 0 && launch_merge(p, st) != cudaSuccess) return NVFP4MLA_ERR_CUDA;
   return NVFP4MLA_OK;
+}
+
+extern "C" {
+
+int sparse_mla_decode(const void* q, const void* kv_cache, int64_t num_pages, const int32_t* page_table,
+                      int64_t max_pages_per_seq, const int32_t* topk_indices, const int32_t* seq_lens, int B,
+                      int Q, int H, int topk, float softmax_scale, void* out, float* lse, void* workspace,
+                      size_t workspace_bytes, int32_t* dev_status, uint32_t flags, void* stream) {
+  return decode_impl(q, kv_cache, num_pages, page_table, max_pages_per_seq, topk_indices, seq_lens, B, Q, H, topk,
+                     softmax_scale, out, lse, workspace, workspace_bytes, dev_status, flags, stream, 0);
+}
+
+int sparse_mla_decode_fp8(const void* q, const void* kv_cache_fp8, int64_t num_pages, const int32_t* page_table,
+                          int64_t max_pages_per_seq, const int32_t* topk_indices, const int32_t* seq_lens, int B,
+                          int Q, int H, int topk, float softmax_scale, void* out, float* lse, void* workspace,
+                          size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  return decode_impl(q, kv_cache_fp8, num_pages, page_table, max_pages_per_seq, topk_indices, seq_lens, B, Q, H,
+                     topk, softmax_scale, out, lse, workspace, workspace_bytes, dev_status, 0u, stream, 1);
+}
+
+int fp8_kv_pack(const void* latent, int64_t latent_row_stride, const void* rope, int64_t rope_row_stride,
+                const int64_t* slot_mapping, int64_t num_tokens, void* kv_cache_fp8, int64_t num_pages,
+                int32_t* dev_status, void* stream) {
+  if (num_tokens < 0 || num_pages < 1) return NVFP4MLA_ERR_INVALID_ARG;
+  if (num_tokens == 0) return NVFP4MLA_OK;
+  if (latent == nullptr || rope == nullptr || slot_mapping == nullptr || kv_cache_fp8 == nullptr)
+    return NVFP4MLA_ERR_INVALID_ARG;
+  if (latent_row_stride < kLatent || rope_row_stride < kRope) return NVFP4MLA_ERR_INVALID_ARG;
+  if (num_pages > (INT64_MAX / (kPageTokens * kFp8RowBytes))) return NVFP4MLA_ERR_INVALID_ARG;
+  if (!aligned(latent, 16) || (latent_row_stride % 8) != 0) return NVFP4MLA_ERR_ALIGNMENT;
+  if (!aligned(rope, 4) || (rope_row_stride % 2) != 0) return NVFP4MLA_ERR_ALIGNMENT;
+  if (!aligned(kv_cache_fp8, 16) || !aligned(slot_mapping, 8)) return NVFP4MLA_ERR_ALIGNMENT;
+  if (dev_status != nullptr && !aligned(dev_status, 4)) return NVFP4MLA_ERR_ALIGNMENT;
+  if (pointer_kind(latent) != kPtrDevice || pointer_kind(rope) != kPtrDevice ||
+      pointer_kind(slot_mapping) != kPtrDevice || pointer_kind(kv_cache_fp8) != kPtrDevice ||
+      (dev_status != nullptr && pointer_kind(dev_status) != kPtrDevice))
+    return NVFP4MLA_ERR_INVALID_ARG;
+  const cudaError_t err = launch_fp8_pack(static_cast<const uint16_t*>(latent), latent_row_stride,
+                                          static_cast<const uint16_t*>(rope), rope_row_stride, slot_mapping,
+                                          num_tokens, static_cast<uint8_t*>(kv_cache_fp8), num_pages, dev_status,
+                                          static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? NVFP4MLA_OK : NVFP4MLA_ERR_CUDA;
+}
+
+int nvfp4_stage_fp8(const void* kv_cache, int64_t num_pages, const int32_t* page_table, int64_t max_pages_per_seq,
+                    const int32_t* topk_indices, const int32_t* seq_lens, int B, int Q, int topk, void* staged,
+                    int32_t* staged_indices, int32_t* staged_page_table, int32_t* staged_seq_lens,
+                    int32_t* dev_status, void* stream) {
+  if (B < 1 || Q < 1 || Q > 16 || topk < kPageTokens || topk > NVFP4MLA_MAX_TOPK || topk % kPageTokens != 0)
+    return NVFP4MLA_ERR_INVALID_ARG;
+  if (num_pages < 1 || max_pages_per_seq < 1 || num_pages > INT32_MAX) return NVFP4MLA_ERR_INVALID_ARG;
+  if ((int64_t)B * Q * topk > (int64_t)INT32_MAX) return NVFP4MLA_ERR_UNSUPPORTED;   // staged rows in int32
+  if (kv_cache == nullptr || page_table == nullptr || topk_indices == nullptr || seq_lens == nullptr ||
+      staged == nullptr || staged_indices == nullptr || staged_page_table == nullptr || staged_seq_lens == nullptr)
+    return NVFP4MLA_ERR_INVALID_ARG;
+  if (!aligned(kv_cache, 16) || !aligned(staged, 16)) return NVFP4MLA_ERR_ALIGNMENT;
+  if (!aligned(page_table, 4) || !aligned(topk_indices, 4) || !aligned(seq_lens, 4) || !aligned(staged_indices, 4) ||
+      !aligned(staged_page_table, 4) || !aligned(staged_seq_lens, 4))
+    return NVFP4MLA_ERR_ALIGNMENT;
+  if (dev_status != nullptr && !aligned(dev_status, 4)) return NVFP4MLA_ERR_ALIGNMENT;
+  const void* ptrs[8] = {kv_cache, page_table, topk_indices, seq_lens, staged, staged_indices, staged_page_table,
+                         staged_seq_lens};
+  for (const void* ptr : ptrs)
+    if (pointer_kind(ptr) != kPtrDevice) return NVFP4MLA_ERR_INVALID_ARG;
+  if (dev_status != nullptr && pointer_kind(dev_status) != kPtrDevice) return NVFP4MLA_ERR_INVALID_ARG;
+  const cudaError_t err =
+      launch_stage(static_cast<const uint8_t*>(kv_cache), num_pages, page_table, max_pages_per_seq, topk_indices,
+                   seq_lens, B, Q, topk, static_cast<uint8_t*>(staged), staged_indices, staged_page_table,
+                   staged_seq_lens, dev_status, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? NVFP4MLA_OK : NVFP4MLA_ERR_CUDA;
 }
 
 }  // extern "C"

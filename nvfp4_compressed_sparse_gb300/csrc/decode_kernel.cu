@@ -44,9 +44,18 @@ namespace {
 using namespace ptx;
 
 constexpr int kThreads = 512;
-constexpr int kRingStages = 4;            // one tile of 4 x 32 rows
-constexpr int kRingRowStride = kRowBytes; // rows land densely: gather4 writes 4 x 352 B per instruction
-constexpr int kRingStageBytes = 32 * kRingRowStride;   // 11264 = 88 x 128 B
+constexpr int kRingStages = 4;            // a tile's rows in 4 quarters of 32 rows, each with its own barrier
+// Cache row formats. kFmt 0: the 352-byte NVFP4 row; the ring holds a whole tile (4 buffers of 32
+// rows). kFmt 1: the 576-byte FP8 row of the comparison path; a whole tile does not fit next to the
+// V tile, so the ring holds 2 buffers and quarter q uses buffer q % 2 (quarters 0, 1 land first,
+// then 2, 3). Rows land densely: gather4 writes 4 rows per instruction.
+template <int kFmt>
+struct RowFmt {
+  static constexpr int kBytes = kFmt == 0 ? kRowBytes : kFp8RowBytes;
+  static constexpr int kBufs = kFmt == 0 ? 4 : 2;
+  static constexpr int kStageBytes = 32 * kBytes;        // 11264 = 88 x 128 B; 18432 = 144 x 128 B
+  static constexpr int kRingBytes = kBufs * kStageBytes;
+};
 constexpr int kVBytes = 8 * 128 * 128;    // 8 SW128 atoms x 128 rows x 128 B
 constexpr int kTmemCols = 512;
 constexpr int kTmemK = 0;                 // K tile: 288 columns (576 fp16 per lane)
@@ -308,19 +317,22 @@ __device__ void producer_loop(const DecodeParams& p, Smem* sm, int64_t t_begin, 
   }
 }
 
-// Refill ring stage q with the 32 rows of tile k (8 gather4 copies, lanes 0..7), once the producer
-// has resolved them. Returns false on timeout/abort.
+// Refill the ring buffer of quarter q with the 32 rows of tile k (8 gather4 copies, lanes 0..7),
+// once the producer has resolved them. Returns false on timeout/abort.
+template <int kFmt>
 __device__ __forceinline__ bool issue_stage(const DecodeParams& p, Smem* sm, uint8_t* ring, int64_t k, int q, int lane) {
+  using F = RowFmt<kFmt>;
   bool good = true;
   if (lane == 0) {
     good = wait(sm, &sm->rows_full, (uint32_t)(k & 1), p.status);
-    if (good) mbar_arrive_expect_tx(&sm->ring_full[q], (uint32_t)kRingStageBytes);
+    if (good) mbar_arrive_expect_tx(&sm->ring_full[q], (uint32_t)F::kStageBytes);
   }
   good = __shfl_sync(0xffffffffu, good, 0);
   if (!good) return false;
   if (lane < 8) {
     const int4 r = *reinterpret_cast<const int4*>(&sm->rowbuf[q * 32 + 4 * lane]);
-    gather4(ring + q * kRingStageBytes + lane * 4 * kRowBytes, &p.cache_map, r.x, r.y, r.z, r.w, &sm->ring_full[q]);
+    gather4(ring + (q % F::kBufs) * F::kStageBytes + lane * 4 * F::kBytes, &p.cache_map, r.x, r.y, r.z, r.w,
+            &sm->ring_full[q]);
   }
   __syncwarp();   // every lane has read its row numbers before the table is released
   if (lane == 0) mbar_arrive(&sm->rows_empty);
@@ -349,27 +361,47 @@ __device__ __forceinline__ void convert_group(const uint8_t* rowp, int g, uint32
   }
 }
 
+// FP8 rows: 64 E4M3 bytes -> 32 fp16 pairs (exact). Rows are 576 B apart, so the 16-byte loads of a
+// quarter-warp meet four-way bank conflicts; the comparison path keeps the simple layout.
+__device__ __forceinline__ void convert_fp8_64(const uint8_t* src, uint32_t (&r)[32]) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const uint4 v = *reinterpret_cast<const uint4*>(src + 16 * c);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      r[8 * c + 2 * i] = e4m3x2_to_f16x2(w[i] & 0xFFFFu);
+      r[8 * c + 2 * i + 1] = e4m3x2_to_f16x2(w[i] >> 16);
+    }
+  }
+}
+
 // Each dequant warp owns one TMEM lane quarter (tile rows 32q..32q+31) and half of the columns.
 // Pass A converts its rows into the fp16 K tile in TMEM (the A operand of the QK UMMA) and then
 // releases the ring stage. Pass B copies the latent part of those K rows from TMEM into the
 // V tile in shared memory (the A operand of PV, read MN-major) once PV of the previous tile is done
 // with those V rows, so the compressed rows are converted only once and leave the ring early.
+template <int kFmt>
 __device__ void dequant_loop(const DecodeParams& p, Smem* sm, uint8_t* ring, uint8_t* vtile,
                              int64_t t_begin, int64_t t_end, int warp) {
+  using F = RowFmt<kFmt>;
   const int lane = threadIdx.x & 31;
-  const int q = warp & 3;               // TMEM lane quarter == ring stage == tile rows 32q..32q+31
+  const int q = warp & 3;               // TMEM lane quarter == tile rows 32q..32q+31
   const int half = (warp - 4) >> 2;
   const int row = 32 * q + lane;
   const uint32_t tmem_row = sm->tmem_base + ((uint32_t)(32 * q) << 16);
-  const uint8_t* rowp = ring + q * kRingStageBytes + lane * kRingRowStride;
+  const uint8_t* rowp = ring + (q % F::kBufs) * F::kStageBytes + lane * F::kBytes;
   int64_t n = t_end - t_begin;
-  int64_t issued = 0;   // tiles whose rows this warp has requested for stage q
+  // the last fill this warp requested (quarter, tile); -1: none
+  int last_q = -1;
+  int64_t last_k = -1;
   // The ring is refilled by the dequant warps themselves: the second of the two warps that read a
-  // stage issues the stage's gathers for the next tile as soon as both are done with it. The lo
-  // warp of each quarter issues tile 0.
-  if (half == 0 && n > 0) {
-    if (!issue_stage(p, sm, ring, 0, q, lane)) n = 0;
-    else issued = 1;
+  // quarter's buffer issues its next fill as soon as both are done with it (NVFP4: the same
+  // quarter of the next tile; FP8: quarter q+2 of this tile, or quarter q-2 of the next). The lo
+  // warps issue the first fills.
+  if (half == 0 && n > 0 && q < F::kBufs) {
+    if (!issue_stage<kFmt>(p, sm, ring, 0, q, lane)) n = 0;
+    else last_q = q, last_k = 0;
   }
   for (int64_t g = t_begin; g < t_begin + n; ++g) {
     const int64_t k = g - t_begin;
@@ -386,28 +418,30 @@ __device__ void dequant_loop(const DecodeParams& p, Smem* sm, uint8_t* ring, uin
     tc_fence_after();
     const uint32_t mask = sm->maskbuf[k & 1][q];
     uint32_t r[32];
-    // the 16 block scales of this half: one 16-byte load instead of four word loads
-    const uint4 sc = *reinterpret_cast<const uint4*>(rowp + kScaleOff + 16 * half);
-    // Rows of unusable entries arrive zero-filled (scale bytes 0), so they dequantise to zeros.
+    if constexpr (kFmt == 0) {
+      // the 16 block scales of this half: one 16-byte load instead of four word loads
+      const uint4 sc = *reinterpret_cast<const uint4*>(rowp + kScaleOff + 16 * half);
+      // Rows of unusable entries arrive zero-filled (scale bytes 0), so they dequantise to zeros.
 #pragma unroll 1
-    for (int gi = 0; gi < 4; ++gi) {
-      const int grp = 4 * half + gi;
-      const uint32_t sw = gi == 0 ? sc.x : gi == 1 ? sc.y : gi == 2 ? sc.z : sc.w;
-      convert_group(rowp, grp, sw, r);
-      __syncwarp();
-      tmem_st32(tmem_row + kTmemK + 32 * grp, r);
+      for (int gi = 0; gi < 4; ++gi) {
+        const int grp = 4 * half + gi;
+        const uint32_t sw = gi == 0 ? sc.x : gi == 1 ? sc.y : gi == 2 ? sc.z : sc.w;
+        convert_group(rowp, grp, sw, r);
+        __syncwarp();
+        tmem_st32(tmem_row + kTmemK + 32 * grp, r);
+      }
+    } else {
+      // FP8 rows: latent byte d is dim d (zero-filled rows give zeros)
+#pragma unroll 1
+      for (int gi = 0; gi < 4; ++gi) {
+        const int grp = 4 * half + gi;
+        convert_fp8_64(rowp + 64 * grp, r);
+        __syncwarp();
+        tmem_st32(tmem_row + kTmemK + 32 * grp, r);
+      }
     }
     if (half == 1) {
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const uint4 v = *reinterpret_cast<const uint4*>(rowp + kRopeOff + 16 * c);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          r[8 * c + 2 * i] = e4m3x2_to_f16x2(w[i] & 0xFFFFu);
-          r[8 * c + 2 * i + 1] = e4m3x2_to_f16x2(w[i] >> 16);
-        }
-      }
+      convert_fp8_64(rowp + (kFmt == 0 ? kRopeOff : kLatent), r);   // the rope bytes are E4M3 in both formats
       __syncwarp();
       tmem_st32(tmem_row + kTmemK + 256, r);
     }
@@ -421,14 +455,18 @@ __device__ void dequant_loop(const DecodeParams& p, Smem* sm, uint8_t* ring, uin
       }
       mbar_arrive(&sm->kv_ready[half]);
     }
-    // ---- refill: the second warp done with stage q requests tile k+1's rows into it
+    // ---- refill: the second warp done with this quarter's buffer requests its next fill
     {
       uint32_t old = 0;
       if (lane == 0) asm volatile("atom.add.acq_rel.cta.shared::cta.u32 %0, [%1], 1;" : "=r"(old) : "r"(smem_u32(&sm->stage_cnt[q])) : "memory");
       old = __shfl_sync(0xffffffffu, old, 0);
-      if ((old & 1u) && k + 1 < n) {
-        if (!issue_stage(p, sm, ring, k + 1, q, lane)) break;
-        issued = k + 2;
+      if (old & 1u) {
+        const int nq = F::kBufs == 4 ? q : (q + 2) & 3;
+        const int64_t nk = (F::kBufs == 4 || q >= 2) ? k + 1 : k;
+        if (nk < n) {
+          if (!issue_stage<kFmt>(p, sm, ring, nk, nq, lane)) break;
+          last_q = nq, last_k = nk;
+        }
       }
     }
     // ---- pass B: latent K rows (TMEM) -> V rows (shared memory, SW128 K-major atoms)
@@ -452,8 +490,11 @@ __device__ void dequant_loop(const DecodeParams& p, Smem* sm, uint8_t* ring, uin
     __syncwarp();
     if (lane == 0) mbar_arrive(&sm->v_ready[half]);
   }
-  // After an abort, never leave with gathers in flight: wait (bounded) for the last refill issued.
-  if (lane == 0 && issued > 0 && sm->abort) mbar_wait(&sm->ring_full[q], (uint32_t)((issued - 1) & 1), nullptr, kWaitTimeoutNs);
+  // After an abort, never leave with gathers in flight: wait (bounded) for the last fill this warp
+  // requested. (Every earlier fill of the same buffer was waited on before the next one was
+  // requested, so the last fills of the warps cover every copy still in flight.)
+  if (lane == 0 && last_k >= 0 && sm->abort)
+    mbar_wait(&sm->ring_full[last_q], (uint32_t)(last_k & 1), nullptr, kWaitTimeoutNs);
   __syncwarp();
 }
 
@@ -931,16 +972,17 @@ __device__ void cluster_merge(const DecodeParams& p, ClusterScratch* sm, uint8_t
 // kCluster: the cluster schedule (in-kernel q, DSMEM merge). kPublish: the split schedule with a
 // polling merge grid (results in host memory): each CTA tags its partial slots when done. The
 // tagging is a separate instance because its mere presence slowed the other split kernel by ~2 %.
-template <int NH, bool kCluster, bool kPublish>
+template <int NH, bool kCluster, bool kPublish, int kFmt = 0>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ DecodeParams p) {
+  static_assert(kFmt == 0 || !kCluster, "FP8 rows run on the split schedule only");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* vtile = base;                                   // 131072
   uint8_t* qs = vtile + kVBytes;                           // 9 * NH * 128
   uint8_t* ps = qs + 9 * NH * 128;                         // 2 x 128 * NH * 2 (P, double-buffered)
-  uint8_t* ring = ps + 2 * 128 * NH * 2;                   // 4 * 32 * 352
-  static_assert((kRingStages * kRingStageBytes) % 16 == 0, "control block must stay 16-byte aligned");
-  Smem* sm = reinterpret_cast<Smem*>(ring + kRingStages * kRingStageBytes);
+  uint8_t* ring = ps + 2 * 128 * NH * 2;                   // RowFmt<kFmt>::kRingBytes
+  static_assert(RowFmt<kFmt>::kRingBytes % 16 == 0, "control block must stay 16-byte aligned");
+  Smem* sm = reinterpret_cast<Smem*>(ring + RowFmt<kFmt>::kRingBytes);
 
   const int warp = threadIdx.x >> 5;
   const int64_t cta = blockIdx.x;
@@ -1009,7 +1051,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     if ((threadIdx.x & 31) == 0) mma_loop<NH, kCluster>(p, sm, vtile, qs, ps, t_begin, t_end, warp - 1);
     __syncwarp();
   } else if (warp >= 4 && warp < 12) {
-    dequant_loop(p, sm, ring, vtile, t_begin, t_end, warp);
+    dequant_loop<kFmt>(p, sm, ring, vtile, t_begin, t_end, warp);
   } else if (warp >= 12) {
     const bool ok = softmax_loop<NH, kCluster>(p, sm, ps, vtile, reinterpret_cast<ClusterScratch*>(ring), t_begin,
                                                t_end, cta, qscale);
@@ -1189,11 +1231,13 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeParams
   if (d8 == 0) p.lse[row] = lsum > 0.f ? (mstar + log2f(lsum)) * 0.69314718055994530942f : kNegInf;
 }
 
-template <int NH>
+template <int NH, int kFmt = 0>
 constexpr size_t decode_smem_bytes() {
-  return 1024 + kVBytes + 9 * NH * 128 + 2 * 128 * NH * 2 + kRingStages * kRingStageBytes + sizeof(Smem);
+  return 1024 + kVBytes + 9 * NH * 128 + 2 * 128 * NH * 2 + RowFmt<kFmt>::kRingBytes + sizeof(Smem);
 }
 static_assert(decode_smem_bytes<32>() <= 232448, "decode CTA exceeds the 227 KB shared-memory limit");
+static_assert(decode_smem_bytes<32, 1>() <= 232448, "FP8 decode CTA exceeds the 227 KB shared-memory limit");
+static_assert(sizeof(ClusterScratch) <= RowFmt<0>::kRingBytes, "cluster scratch lives in the ring");
 
 }  // namespace
 
@@ -1217,13 +1261,15 @@ static cudaError_t set_attributes() {
     const cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess && result == cudaSuccess) result = e;
   }
-  const void* big[6] = {(const void*)decode_kernel<32, false, false>, (const void*)decode_kernel<32, false, true>,
-                        (const void*)decode_kernel<32, true, false>,  (const void*)decode_kernel<16, false, false>,
-                        (const void*)decode_kernel<16, false, true>,  (const void*)decode_kernel<16, true, false>};
-  const int bytes[6] = {(int)decode_smem_bytes<32>(), (int)decode_smem_bytes<32>(), (int)decode_smem_bytes<32>(),
-                        (int)decode_smem_bytes<16>(), (int)decode_smem_bytes<16>(), (int)decode_smem_bytes<16>()};
+  const void* big[8] = {(const void*)decode_kernel<32, false, false>,   (const void*)decode_kernel<32, false, true>,
+                        (const void*)decode_kernel<32, true, false>,    (const void*)decode_kernel<16, false, false>,
+                        (const void*)decode_kernel<16, false, true>,    (const void*)decode_kernel<16, true, false>,
+                        (const void*)decode_kernel<32, false, false, 1>, (const void*)decode_kernel<16, false, false, 1>};
+  const int bytes[8] = {(int)decode_smem_bytes<32>(),    (int)decode_smem_bytes<32>(), (int)decode_smem_bytes<32>(),
+                        (int)decode_smem_bytes<16>(),    (int)decode_smem_bytes<16>(), (int)decode_smem_bytes<16>(),
+                        (int)decode_smem_bytes<32, 1>(), (int)decode_smem_bytes<16, 1>()};
   static_assert(sizeof(big) / sizeof(big[0]) == sizeof(bytes) / sizeof(bytes[0]), "one size per decode instance");
-  for (int i = 0; i < 6; ++i) {
+  for (int i = 0; i < 8; ++i) {
     const cudaError_t e = cudaFuncSetAttribute(big[i], cudaFuncAttributeMaxDynamicSharedMemorySize, bytes[i]);
     if (e != cudaSuccess && result == cudaSuccess) result = e;
   }
@@ -1276,7 +1322,8 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream) {
   if (h32) q_prep_kernel<32><<<(unsigned)p.units, 256, 0, stream>>>(p);
   else q_prep_kernel<16><<<(unsigned)p.units, 256, 0, stream>>>(p);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  const size_t smem = h32 ? decode_smem_bytes<32>() : decode_smem_bytes<16>();
+  const size_t smem = p.row_fmt == 1 ? (h32 ? decode_smem_bytes<32, 1>() : decode_smem_bytes<16, 1>())
+                                     : (h32 ? decode_smem_bytes<32>() : decode_smem_bytes<16>());
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)p.ctas, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
@@ -1285,6 +1332,10 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream) {
   cudaLaunchAttribute attr[1] = {pdl_attr()};
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (p.row_fmt == 1) {   // FP8 rows: results in device memory (the host checks)
+    if (h32) return cudaLaunchKernelEx(&cfg, decode_kernel<32, false, false, 1>, p);
+    return cudaLaunchKernelEx(&cfg, decode_kernel<16, false, false, 1>, p);
+  }
   if (p.merge_poll) {
     if (h32) return cudaLaunchKernelEx(&cfg, decode_kernel<32, false, true>, p);
     return cudaLaunchKernelEx(&cfg, decode_kernel<16, false, true>, p);

@@ -1,0 +1,149 @@
+// Kernels of the FP8 comparison paths: the 576-byte FP8 row pack and the staged NVFP4 -> FP8 copy.
+//
+// What they compute ("Prime Inference: serving GLM-5.3 to agents is a KV-cache problem", sections
+// "Four bits per latent value: where 352 comes from" and "A kernel that reads four bits directly";
+// "Prime Inference", translated page, "Native NVFP4 sparse MLA decode kernel"): an FP8 cache row is
+// one E4M3 byte per value of the 576-value row (512 latent + 64 rope); the staged path reads each
+// selected 352-byte NVFP4 row and writes a 576-byte FP8 copy that an FP8 attention kernel then
+// reads (1,504 bytes per selected row through HBM, against 352 for the native kernel).
+//
+// Roundings (this build's readings): E4M3 nearest-even, saturating at +-448, NaN -> 0x7F with its
+// sign; a staged latent value is e2m1(code) * E4M3(scale), exact in fp16, rounded once; a block with
+// a NaN scale byte stages as 0x7F; rope bytes are copied.
+//
+// Both kernels are one warp per row, every load of a row issued before any is used, 16-byte
+// coalesced stores.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <atomic>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace nvfp4mla {
+namespace {
+
+constexpr int kFp8Warps = 8;   // warps per block of either kernel
+
+// bf16 rows -> FP8 rows. Lane l converts latent values 16l..16l+15 (two 16-byte loads; the warp
+// reads the 1 KB latent row coalesced) and rope values 2l, 2l+1.
+__global__ void __launch_bounds__(kFp8Warps * 32) fp8_pack_kernel(
+    const uint16_t* __restrict__ latent, int64_t lstride, const uint16_t* __restrict__ rope, int64_t rstride,
+    const int64_t* __restrict__ slots, int64_t n, uint8_t* __restrict__ cache, int64_t num_pages,
+    int32_t* __restrict__ status) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nslots = num_pages * kPageTokens;
+  for (int64_t row = (int64_t)blockIdx.x * kFp8Warps + (threadIdx.x >> 5); row < n;
+       row += (int64_t)gridDim.x * kFp8Warps) {
+    const int64_t slot = __ldcs(slots + row);
+    const uint4* lp = reinterpret_cast<const uint4*>(latent + row * lstride) + 2 * lane;
+    const uint4 a = __ldcs(lp), b = __ldcs(lp + 1);
+    const uint32_t r = __ldcs(reinterpret_cast<const unsigned int*>(rope + row * rstride) + lane);
+    if (slot < 0 || slot >= nslots) {
+      if (slot != -1 && lane == 0 && status != nullptr) atomicAdd(status + 3, 1);
+      continue;
+    }
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      o[i] = ptx::bf16x2_to_e4m3x2(w[2 * i]) | (ptx::bf16x2_to_e4m3x2(w[2 * i + 1]) << 16);
+    uint8_t* dst = cache + slot * kFp8RowBytes;
+    __stcs(reinterpret_cast<uint4*>(dst) + lane, make_uint4(o[0], o[1], o[2], o[3]));
+    __stcs(reinterpret_cast<unsigned short*>(dst + kLatent) + lane, (unsigned short)ptx::bf16x2_to_e4m3x2(r));
+  }
+}
+
+// One warp per (query, list entry) of a decode step: resolve the entry with the decode's rule,
+// then lane l stages latent block l (8 nibble bytes and its scale byte) into 16 E4M3 bytes and
+// lanes 0..3 copy the 64 rope bytes. Also writes the staged decode's index list (i or -1), its
+// identity page table and its lengths.
+__global__ void __launch_bounds__(kFp8Warps * 32) stage_kernel(
+    const uint8_t* __restrict__ cache, int64_t num_pages, const int32_t* __restrict__ page_table, int64_t max_pages,
+    const int32_t* __restrict__ idx, const int32_t* __restrict__ seq_lens, int Q, int K, int64_t entries,
+    uint8_t* __restrict__ staged, int32_t* __restrict__ staged_idx, int32_t* __restrict__ staged_pt,
+    int32_t* __restrict__ staged_sl, int32_t* __restrict__ status) {
+  const int lane = threadIdx.x & 31;
+  const int pages_per_unit = K / kPageTokens;
+  for (int64_t e = (int64_t)blockIdx.x * kFp8Warps + (threadIdx.x >> 5); e < entries;
+       e += (int64_t)gridDim.x * kFp8Warps) {
+    const int64_t u = e / K;
+    const int i = (int)(e - u * K);
+    const int b = (int)(u / Q), j = (int)(u - (int64_t)b * Q);
+    if (lane == 0 && i < pages_per_unit) staged_pt[u * pages_per_unit + i] = (int32_t)(u * pages_per_unit + i);
+    if (lane == 0 && i == 0) staged_sl[u] = K;
+    const int L = __ldg(seq_lens + b);
+    const int x = __ldcs(idx + e);
+    const bool in_range = x >= 0 && x < L && x <= L - Q + j;
+    const bool col_ok = in_range && (int64_t)(x >> 6) < max_pages;
+    const int page = col_ok ? __ldg(page_table + (int64_t)b * max_pages + (x >> 6)) : -1;
+    const bool ok = col_ok && page >= 0 && page < num_pages;
+    if (lane == 0) {
+      staged_idx[e] = ok ? i : -1;
+      if (status != nullptr) {
+        if (x != -1 && !in_range) atomicAdd(status + 0, 1);
+        if (in_range && !ok) atomicAdd(status + 1, 1);
+      }
+    }
+    if (!ok) continue;
+    const uint8_t* row = cache + ((int64_t)page * kPageTokens + (x & 63)) * kRowBytes;
+    const uint2 nib = __ldcs(reinterpret_cast<const uint2*>(row) + lane);
+    const uint32_t sc = __ldcs(row + kScaleOff + lane);
+    uint4 rp = make_uint4(0u, 0u, 0u, 0u);
+    if (lane < 4) rp = __ldcs(reinterpret_cast<const uint4*>(row + kRopeOff) + lane);
+    uint32_t o[4];
+    if ((sc & 0x7Fu) == 0x7Fu) {
+      o[0] = o[1] = o[2] = o[3] = 0x7F7F7F7Fu;   // NaN scale
+    } else {
+      const uint32_t s2 = ptx::e4m3x2_to_f16x2(sc | (sc << 8));   // (scale, scale), exact
+      uint32_t c0[4], c1[4];   // values 0..7 and 8..15 of the block as f16 pairs
+      ptx::e2m1x8_to_f16x2x4(nib.x, c0);
+      ptx::e2m1x8_to_f16x2x4(nib.y, c1);
+      // products e2m1 x E4M3 have at most 5 significant bits and lie within [2^-10, 2688]: exact in fp16
+      o[0] = ptx::f16x2_to_e4m3x2(ptx::hmul2(c0[0], s2)) | (ptx::f16x2_to_e4m3x2(ptx::hmul2(c0[1], s2)) << 16);
+      o[1] = ptx::f16x2_to_e4m3x2(ptx::hmul2(c0[2], s2)) | (ptx::f16x2_to_e4m3x2(ptx::hmul2(c0[3], s2)) << 16);
+      o[2] = ptx::f16x2_to_e4m3x2(ptx::hmul2(c1[0], s2)) | (ptx::f16x2_to_e4m3x2(ptx::hmul2(c1[1], s2)) << 16);
+      o[3] = ptx::f16x2_to_e4m3x2(ptx::hmul2(c1[2], s2)) | (ptx::f16x2_to_e4m3x2(ptx::hmul2(c1[3], s2)) << 16);
+    }
+    uint8_t* dst = staged + e * kFp8RowBytes;
+    __stcs(reinterpret_cast<uint4*>(dst) + lane, make_uint4(o[0], o[1], o[2], o[3]));
+    if (lane < 4) __stcs(reinterpret_cast<uint4*>(dst + kLatent) + lane, rp);
+  }
+}
+
+int blocks_for(int64_t warps_needed, const void* kernel) {
+  const int sms = device_sm_count();
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kFp8Warps * 32, 0) != cudaSuccess || per_sm < 1) {
+    (void)cudaGetLastError();
+    per_sm = 4;
+  }
+  const int64_t want = (warps_needed + kFp8Warps - 1) / kFp8Warps;
+  const int64_t cap = (int64_t)(sms > 0 ? sms : 148) * per_sm;
+  return (int)(want < cap ? (want > 0 ? want : 1) : cap);
+}
+
+}  // namespace
+
+cudaError_t launch_fp8_pack(const uint16_t* latent, int64_t lstride, const uint16_t* rope, int64_t rstride,
+                            const int64_t* slots, int64_t n, uint8_t* cache, int64_t num_pages, int32_t* status,
+                            cudaStream_t stream) {
+  const int grid = blocks_for(n, (const void*)fp8_pack_kernel);
+  fp8_pack_kernel<<<grid, kFp8Warps * 32, 0, stream>>>(latent, lstride, rope, rstride, slots, n, cache, num_pages,
+                                                       status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_stage(const uint8_t* cache, int64_t num_pages, const int32_t* page_table, int64_t max_pages,
+                         const int32_t* idx, const int32_t* seq_lens, int B, int Q, int K, uint8_t* staged,
+                         int32_t* staged_idx, int32_t* staged_pt, int32_t* staged_sl, int32_t* status,
+                         cudaStream_t stream) {
+  const int64_t entries = (int64_t)B * Q * K;
+  const int grid = blocks_for(entries, (const void*)stage_kernel);
+  stage_kernel<<<grid, kFp8Warps * 32, 0, stream>>>(cache, num_pages, page_table, max_pages, idx, seq_lens, Q, K,
+                                                     entries, staged, staged_idx, staged_pt, staged_sl, status);
+  return cudaGetLastError();
+}
+
+}  // namespace nvfp4mla

@@ -11,6 +11,7 @@ constexpr int kLatent = 512;
 constexpr int kRope = 64;
 constexpr int kQK = 576;
 constexpr int kRowBytes = 352;
+constexpr int kFp8RowBytes = 576;   // FP8 comparison rows: 512 latent + 64 rope E4M3 bytes
 constexpr int kPageTokens = 64;
 constexpr int kScaleOff = 256;
 constexpr int kRopeOff = 288;
@@ -40,9 +41,9 @@ DecodeSchedule make_schedule(int B, int Q, int H, int topk, int num_sms, int max
 size_t workspace_bytes_for(const DecodeSchedule& s, int H);
 
 struct DecodeParams {
-  CUtensorMap cache_map;      // 2-D view of the cache: [num_pages*64 rows, 88 x uint32], one-row box
+  CUtensorMap cache_map;      // 2-D view of the cache: [num_pages*64 rows, row bytes / 4 x uint32], one-row box
   const uint16_t* q;          // bf16 [B, Q, H, 576]
-  const uint8_t* cache;       // [num_pages, 64, 352]
+  const uint8_t* cache;       // [num_pages, 64, 352] (FP8 rows: [num_pages, 64, 576])
   int64_t num_pages;
   const int32_t* page_table;  // [B, max_pages]
   int64_t max_pages;
@@ -66,11 +67,19 @@ struct DecodeParams {
   int tiles_per_unit, ctas;
   int cluster;                // 0 = stream-K split, else CTAs per unit (one cluster per unit)
   uint32_t withhold;          // testing aid: 1 = the producers never publish tile 1's row table
+  int row_fmt;                // 0 = 352-byte NVFP4 rows, 1 = 576-byte FP8 rows (split schedule only)
 };
 
 cudaError_t launch_pack(const uint16_t* latent, int64_t lstride, const uint16_t* rope, int64_t rstride,
                         const int64_t* slots, int64_t n, uint8_t* cache, int64_t num_pages, int32_t* status,
                         cudaStream_t stream);
+cudaError_t launch_fp8_pack(const uint16_t* latent, int64_t lstride, const uint16_t* rope, int64_t rstride,
+                            const int64_t* slots, int64_t n, uint8_t* cache, int64_t num_pages, int32_t* status,
+                            cudaStream_t stream);
+cudaError_t launch_stage(const uint8_t* cache, int64_t num_pages, const int32_t* page_table, int64_t max_pages,
+                         const int32_t* idx, const int32_t* seq_lens, int B, int Q, int K, uint8_t* staged,
+                         int32_t* staged_idx, int32_t* staged_pt, int32_t* staged_sl, int32_t* status,
+                         cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);
 int max_active_clusters(int heads_per_cta, int cluster);   // clusters of the decode grid that fit at once
 cudaError_t launch_merge(const DecodeParams& p, cudaStream_t stream);

@@ -102,16 +102,6 @@ __device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t sc) {
   return __half22float2(*reinterpret_cast<const __half2*>(&h2));
 }
 
-// Rope bytes of a NaN input are E4M3 NaN with the input's sign (0x7F / 0xFF), set here explicitly
-// rather than left to whatever NaN pattern the conversion returns. r holds the two bf16 inputs
-// (element 2l in the low half), rr their two E4M3 bytes (element 2l in the low byte).
-__device__ __forceinline__ uint32_t rope_nan_sign(uint32_t r, uint32_t rr) {
-  const uint32_t lo = r & 0xFFFFu, hi = r >> 16;
-  if ((lo & 0x7FFFu) > 0x7F80u) rr = (rr & 0xFF00u) | 0x7Fu | ((lo >> 8) & 0x80u);
-  if ((hi & 0x7FFFu) > 0x7F80u) rr = (rr & 0x00FFu) | ((0x7Fu | ((hi >> 8) & 0x80u)) << 8);
-  return rr;
-}
-
 constexpr int kRowsPerWarp = 2;
 
 // RN32(1/6) = (1/6)(1 + 2^-25). For a bf16 amax, amax * RN32(1/6) rounds to the same E4M3 value as
@@ -162,7 +152,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, 4) pack_kernel(
       const Thresholds ta = make_thresholds(s.x);
       const Thresholds tb = make_thresholds(s.y);
       const uint32_t wa = encode8(a, ta), wb = encode8(b, tb);
-      const uint32_t rr = rope_nan_sign(r, ptx::f32x2_to_e4m3x2(bf_lo(r), bf_hi(r)));
+      const uint32_t rr = ptx::bf16x2_to_e4m3x2(r);   // NaN keeps its sign (0x7F / 0xFF)
 
       *reinterpret_cast<uint32_t*>(srow + 4 * lane) = wa;
       *reinterpret_cast<uint32_t*>(srow + 128 + 4 * lane) = wb;

@@ -298,6 +298,22 @@ __device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float a, float b) {
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(b), "f"(a));
   return r;
 }
+// f16x2 -> E4M3 pair, round to nearest even, saturating to +-448; the low half lands in the low byte.
+__device__ __forceinline__ uint32_t f16x2_to_e4m3x2(uint32_t h2) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(r) : "r"(h2));
+  return r;
+}
+// Two bf16 values (low half first) -> E4M3 pair: nearest even, saturating to +-448, and a NaN
+// becomes 0x7F with its own sign bit (set here explicitly rather than left to the NaN pattern the
+// conversion returns).
+__device__ __forceinline__ uint32_t bf16x2_to_e4m3x2(uint32_t r) {
+  uint32_t rr = f32x2_to_e4m3x2(__uint_as_float(r << 16), __uint_as_float(r & 0xFFFF0000u));
+  const uint32_t lo = r & 0xFFFFu, hi = r >> 16;
+  if ((lo & 0x7FFFu) > 0x7F80u) rr = (rr & 0xFF00u) | 0x7Fu | ((lo >> 8) & 0x80u);
+  if ((hi & 0x7FFFu) > 0x7F80u) rr = (rr & 0x00FFu) | ((0x7Fu | ((hi >> 8) & 0x80u)) << 8);
+  return rr;
+}
 __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
   uint32_t r;
   asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));

@@ -36,10 +36,11 @@ def assert_close(out, lse, ref_out, ref_lse, what=""):
     assert np.all(d <= LSE_ATOL), f"{what}: lse outside tolerance, worst {np.nanmax(d):.3e}"
 
 
-def oracle_units_from_device_rows(case, units, lat_dev, rope_dev):
+def oracle_units_from_device_rows(case, units, lat_dev, rope_dev, fmt="nvfp4"):
     """Oracle outputs for (b, j) units, encoding the selected rows from their bf16
-    inputs (gathered from the device input tensors by physical slot). The CPU work
-    runs in a pool of spawned worker processes."""
+    inputs (gathered from the device input tensors by physical slot) in the cache format
+    fmt ("nvfp4", "fp8" or "staged"). The CPU work runs in a pool of spawned worker
+    processes."""
     from tests import oracle_pool
     keys, jobs = [], []
     for b, j in units:
@@ -49,6 +50,6 @@ def oracle_units_from_device_rows(case, units, lat_dev, rope_dev):
         sel = idx[ok]
         slots = case.page_table[b][sel // 64].astype(np.int64) * 64 + sel % 64
         st = torch.from_numpy(slots).to(lat_dev.device)
-        jobs.append((case.q_bits[b, j], bits_of(lat_dev[st]), bits_of(rope_dev[st]), case.softmax_scale))
+        jobs.append((case.q_bits[b, j], bits_of(lat_dev[st]), bits_of(rope_dev[st]), case.softmax_scale, fmt))
         keys.append((b, j))
     return dict(zip(keys, oracle_pool.attend_units(jobs)))

@@ -18,7 +18,8 @@ Readings (listed in the design notes):
     scale (the 576 bytes leave none);
   * the staged copy of an NVFP4 row rounds each dequantised latent value e2m1(code) * E4M3(scale)
     (exact in float64) once to E4M3 the same way, so values past 448 saturate; the rope bytes are
-    E4M3 already and are copied unchanged;
+    E4M3 already and are copied unchanged; a block whose scale byte is the E4M3 NaN (0x7F or 0xFF,
+    which pack never writes) stages as 0x7F for each of its 16 values;
   * the staging of one decode step writes, for query (b, j) and list entry i, the copy of the
     selected row to staged row (b*Q + j)*K + i and makes the FP8 decode's list entry i equal to i
     when the entry is usable under the decode's rule (oracle.attention.valid_entries), else -1;
@@ -31,7 +32,8 @@ import numpy as np
 
 from . import codec
 from .attention import D_QK, attend, dequant_rows, valid_entries
-from .pack import D_LATENT, D_ROPE, FP8_ROW_BYTES, PAGE_TOKENS, ROPE_OFFSET, ROW_BYTES
+from .pack import (BLOCK, D_LATENT, D_ROPE, FP8_ROW_BYTES, N_BLOCKS, PAGE_TOKENS, ROPE_OFFSET, ROW_BYTES,
+                   SCALE_OFFSET)
 
 
 def encode_rows_fp8(latent_bits: np.ndarray, rope_bits: np.ndarray) -> np.ndarray:
@@ -50,8 +52,10 @@ def dequant_rows_fp8(rows: np.ndarray) -> np.ndarray:
 def stage_rows(rows: np.ndarray) -> np.ndarray:
     """352-byte NVFP4 rows -> their 576-byte FP8 copies (latent re-rounded, rope bytes copied)."""
     rows = np.asarray(rows, dtype=np.uint8).reshape(-1, ROW_BYTES)
-    lat = dequant_rows(rows)[:, :D_LATENT]
-    return np.concatenate([codec.e4m3_encode(lat), rows[:, ROPE_OFFSET:ROPE_OFFSET + D_ROPE]], axis=1)
+    lat = codec.e4m3_encode(dequant_rows(rows)[:, :D_LATENT])
+    nan_scale = (rows[:, SCALE_OFFSET:SCALE_OFFSET + N_BLOCKS] & 0x7F) == 0x7F
+    lat = np.where(np.repeat(nan_scale, BLOCK, axis=1), np.uint8(0x7F), lat)
+    return np.concatenate([lat, rows[:, ROPE_OFFSET:ROPE_OFFSET + D_ROPE]], axis=1)
 
 
 def write_cache_fp8(cache: np.ndarray, latent_bits, rope_bits, slot_mapping) -> None:

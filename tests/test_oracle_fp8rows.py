@@ -55,6 +55,13 @@ def test_staged_copy_rounds_the_dequantised_value_once():
     np.testing.assert_array_equal(staged[:, :512][~small] & 0x7F, 0x7E)
     np.testing.assert_array_equal(staged[:, :512][~small] >> 7, (val[~small] < 0).astype(np.uint8))
     np.testing.assert_array_equal(staged[:, 512:], rows[:, 288:352])
+    # a NaN scale byte (never written by pack) stages its block as 0x7F
+    odd = rows[:2].copy()
+    odd[0, 256] = 0x7F
+    odd[1, 257] = 0xFF
+    st = fp8rows.stage_rows(odd)
+    assert (st[0, :16] == 0x7F).all() and (st[1, 16:32] == 0x7F).all()
+    np.testing.assert_array_equal(st[0, 16:], staged[0, 16:])
     # the staged value is the E4M3 value nearest the dequantised one: never off by more than half a step
     got = fp8rows.dequant_rows_fp8(staged)[:, :512]
     assert np.all(np.abs(got[small] - val[small]) <= np.maximum(np.abs(val[small]) / 16, 2.0 ** -10))

@@ -11,8 +11,9 @@
 // sign; a staged latent value is e2m1(code) * E4M3(scale), exact in fp16, rounded once; a block with
 // a NaN scale byte stages as 0x7F; rope bytes are copied.
 //
-// Both kernels are one warp per row, every load of a row issued before any is used, 16-byte
-// coalesced stores.
+// The pack is one warp per row; the staging resolves 32 entries per warp at once and copies their
+// rows four at a time. Every load of a row is issued before any is used; stores are 16-byte
+// coalesced.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -55,10 +56,31 @@ __global__ void __launch_bounds__(kFp8Warps * 32) fp8_pack_kernel(
   }
 }
 
-// One warp per (query, list entry) of a decode step: resolve the entry with the decode's rule,
-// then lane l stages latent block l (8 nibble bytes and its scale byte) into 16 E4M3 bytes and
-// lanes 0..3 copy the 64 rope bytes. Also writes the staged decode's index list (i or -1), its
-// identity page table and its lengths.
+// FP8 copy of one NVFP4 row: lane l stages latent block l (8 nibble bytes, scale byte sc) into
+// 16 E4M3 bytes; lanes 0..3 carry 16 rope bytes each (rp).
+__device__ __forceinline__ uint4 stage_block(uint2 nib, uint32_t sc) {
+  if ((sc & 0x7Fu) == 0x7Fu) return make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);   // NaN scale
+  const uint32_t s2 = ptx::e4m3x2_to_f16x2(sc | (sc << 8));   // (scale, scale), exact
+  uint32_t c0[4], c1[4];   // values 0..7 and 8..15 of the block as f16 pairs
+  ptx::e2m1x8_to_f16x2x4(nib.x, c0);
+  ptx::e2m1x8_to_f16x2x4(nib.y, c1);
+  // products e2m1 x E4M3 have at most 5 significant bits and lie within [2^-10, 2688]: exact in fp16
+  uint4 o;
+  o.x = ptx::f16x2_to_e4m3x2(ptx::hmul2(c0[0], s2)) | (ptx::f16x2_to_e4m3x2(ptx::hmul2(c0[1], s2)) << 16);
+  o.y = ptx::f16x2_to_e4m3x2(ptx::hmul2(c0[2], s2)) | (ptx::f16x2_to_e4m3x2(ptx::hmul2(c0[3], s2)) << 16);
+  o.z = ptx::f16x2_to_e4m3x2(ptx::hmul2(c1[0], s2)) | (ptx::f16x2_to_e4m3x2(ptx::hmul2(c1[1], s2)) << 16);
+  o.w = ptx::f16x2_to_e4m3x2(ptx::hmul2(c1[2], s2)) | (ptx::f16x2_to_e4m3x2(ptx::hmul2(c1[3], s2)) << 16);
+  return o;
+}
+
+constexpr int kStageRowsInFlight = 4;
+
+// A warp takes 32 consecutive (query, list entry) pairs of a decode step. Lane l resolves entry
+// e0 + l with the decode's rule (the index, then its page-table word: all 32 in flight at once)
+// and writes the staged decode's list entry (i or -1). The warp then copies the usable rows,
+// kStageRowsInFlight at a time with every load of a group issued before any is used: lane l
+// stages latent block l of each row, lanes 0..3 copy its 64 rope bytes. Also writes the staged
+// decode's identity page table and lengths.
 __global__ void __launch_bounds__(kFp8Warps * 32) stage_kernel(
     const uint8_t* __restrict__ cache, int64_t num_pages, const int32_t* __restrict__ page_table, int64_t max_pages,
     const int32_t* __restrict__ idx, const int32_t* __restrict__ seq_lens, int Q, int K, int64_t entries,
@@ -66,49 +88,58 @@ __global__ void __launch_bounds__(kFp8Warps * 32) stage_kernel(
     int32_t* __restrict__ staged_sl, int32_t* __restrict__ status) {
   const int lane = threadIdx.x & 31;
   const int pages_per_unit = K / kPageTokens;
-  for (int64_t e = (int64_t)blockIdx.x * kFp8Warps + (threadIdx.x >> 5); e < entries;
-       e += (int64_t)gridDim.x * kFp8Warps) {
-    const int64_t u = e / K;
+  for (int64_t e0 = ((int64_t)blockIdx.x * kFp8Warps + (threadIdx.x >> 5)) * 32; e0 < entries;
+       e0 += (int64_t)gridDim.x * kFp8Warps * 32) {
+    const int64_t e = e0 + lane;
+    const bool live = e < entries;
+    const int64_t u = live ? e / K : 0;
     const int i = (int)(e - u * K);
     const int b = (int)(u / Q), j = (int)(u - (int64_t)b * Q);
-    if (lane == 0 && i < pages_per_unit) staged_pt[u * pages_per_unit + i] = (int32_t)(u * pages_per_unit + i);
-    if (lane == 0 && i == 0) staged_sl[u] = K;
-    const int L = __ldg(seq_lens + b);
-    const int x = __ldcs(idx + e);
+    if (live && i < pages_per_unit) staged_pt[u * pages_per_unit + i] = (int32_t)(u * pages_per_unit + i);
+    if (live && i == 0) staged_sl[u] = K;
+    const int L = live ? __ldg(seq_lens + b) : 0;
+    const int x = live ? __ldcs(idx + e) : -1;
     const bool in_range = x >= 0 && x < L && x <= L - Q + j;
     const bool col_ok = in_range && (int64_t)(x >> 6) < max_pages;
     const int page = col_ok ? __ldg(page_table + (int64_t)b * max_pages + (x >> 6)) : -1;
     const bool ok = col_ok && page >= 0 && page < num_pages;
-    if (lane == 0) {
+    if (live) {
       staged_idx[e] = ok ? i : -1;
       if (status != nullptr) {
         if (x != -1 && !in_range) atomicAdd(status + 0, 1);
         if (in_range && !ok) atomicAdd(status + 1, 1);
       }
     }
-    if (!ok) continue;
-    const uint8_t* row = cache + ((int64_t)page * kPageTokens + (x & 63)) * kRowBytes;
-    const uint2 nib = __ldcs(reinterpret_cast<const uint2*>(row) + lane);
-    const uint32_t sc = __ldcs(row + kScaleOff + lane);
-    uint4 rp = make_uint4(0u, 0u, 0u, 0u);
-    if (lane < 4) rp = __ldcs(reinterpret_cast<const uint4*>(row + kRopeOff) + lane);
-    uint32_t o[4];
-    if ((sc & 0x7Fu) == 0x7Fu) {
-      o[0] = o[1] = o[2] = o[3] = 0x7F7F7F7Fu;   // NaN scale
-    } else {
-      const uint32_t s2 = ptx::e4m3x2_to_f16x2(sc | (sc << 8));   // (scale, scale), exact
-      uint32_t c0[4], c1[4];   // values 0..7 and 8..15 of the block as f16 pairs
-      ptx::e2m1x8_to_f16x2x4(nib.x, c0);
-      ptx::e2m1x8_to_f16x2x4(nib.y, c1);
-      // products e2m1 x E4M3 have at most 5 significant bits and lie within [2^-10, 2688]: exact in fp16
-      o[0] = ptx::f16x2_to_e4m3x2(ptx::hmul2(c0[0], s2)) | (ptx::f16x2_to_e4m3x2(ptx::hmul2(c0[1], s2)) << 16);
-      o[1] = ptx::f16x2_to_e4m3x2(ptx::hmul2(c0[2], s2)) | (ptx::f16x2_to_e4m3x2(ptx::hmul2(c0[3], s2)) << 16);
-      o[2] = ptx::f16x2_to_e4m3x2(ptx::hmul2(c1[0], s2)) | (ptx::f16x2_to_e4m3x2(ptx::hmul2(c1[1], s2)) << 16);
-      o[3] = ptx::f16x2_to_e4m3x2(ptx::hmul2(c1[2], s2)) | (ptx::f16x2_to_e4m3x2(ptx::hmul2(c1[3], s2)) << 16);
+    const int64_t row_off = ok ? ((int64_t)page * kPageTokens + (x & 63)) * kRowBytes : -1;
+    uint32_t todo = __ballot_sync(0xffffffffu, ok);
+    while (todo != 0u) {
+      int src[kStageRowsInFlight];
+      const uint8_t* row[kStageRowsInFlight];
+#pragma unroll
+      for (int r = 0; r < kStageRowsInFlight; ++r) {
+        src[r] = todo != 0u ? __ffs(todo) - 1 : -1;
+        if (todo != 0u) todo &= todo - 1u;
+        const int64_t off = __shfl_sync(0xffffffffu, row_off, src[r] < 0 ? 0 : src[r]);
+        row[r] = src[r] < 0 ? nullptr : cache + off;
+      }
+      uint2 nib[kStageRowsInFlight];
+      uint32_t sc[kStageRowsInFlight];
+      uint4 rp[kStageRowsInFlight];
+#pragma unroll
+      for (int r = 0; r < kStageRowsInFlight; ++r) {
+        if (row[r] == nullptr) continue;
+        nib[r] = __ldcs(reinterpret_cast<const uint2*>(row[r]) + lane);
+        sc[r] = __ldcs(row[r] + kScaleOff + lane);
+        if (lane < 4) rp[r] = __ldcs(reinterpret_cast<const uint4*>(row[r] + kRopeOff) + lane);
+      }
+#pragma unroll
+      for (int r = 0; r < kStageRowsInFlight; ++r) {
+        if (row[r] == nullptr) continue;
+        uint8_t* dst = staged + (e0 + src[r]) * kFp8RowBytes;
+        __stcs(reinterpret_cast<uint4*>(dst) + lane, stage_block(nib[r], sc[r]));
+        if (lane < 4) __stcs(reinterpret_cast<uint4*>(dst + kLatent) + lane, rp[r]);
+      }
     }
-    uint8_t* dst = staged + e * kFp8RowBytes;
-    __stcs(reinterpret_cast<uint4*>(dst) + lane, make_uint4(o[0], o[1], o[2], o[3]));
-    if (lane < 4) __stcs(reinterpret_cast<uint4*>(dst + kLatent) + lane, rp);
   }
 }
 
@@ -140,7 +171,7 @@ cudaError_t launch_stage(const uint8_t* cache, int64_t num_pages, const int32_t*
                          int32_t* staged_idx, int32_t* staged_pt, int32_t* staged_sl, int32_t* status,
                          cudaStream_t stream) {
   const int64_t entries = (int64_t)B * Q * K;
-  const int grid = blocks_for(entries, (const void*)stage_kernel);
+  const int grid = blocks_for((entries + 31) / 32, (const void*)stage_kernel);
   stage_kernel<<<grid, kFp8Warps * 32, 0, stream>>>(cache, num_pages, page_table, max_pages, idx, seq_lens, Q, K,
                                                      entries, staged, staged_idx, staged_pt, staged_sl, status);
   return cudaGetLastError();

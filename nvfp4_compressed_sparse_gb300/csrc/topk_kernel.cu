@@ -185,20 +185,42 @@ __device__ __forceinline__ void global_histogram(TopkShared& sh, const float* ro
   __syncthreads();
 }
 
-// One element of the candidate sweep: above the top digit -> selected, equal -> candidate.
-__device__ __forceinline__ void classify(TopkShared& sh, uint32_t k, int32_t pos, uint32_t d1) {
-  const uint32_t d = k >> 20;
-  if (d >= d1) {
-    if (d > d1) {
-      atomicOr(&gt_map(sh)[pos >> 5], 1u << (pos & 31));
-    } else {
-      const uint32_t slot = atomicAdd(&sh.cand_count, 1u);
+// Appends the keys flagged in `bits` (key i at position p0 + i) to the candidate store with one
+// shared atomic per warp: a warp scan of the per-lane counts gives every lane its slots. Called by
+// all 32 lanes; slots past the store's capacity are counted but not written.
+__device__ __forceinline__ void append_candidates(TopkShared& sh, uint32_t bits, const uint32_t (&keys)[kTkPer],
+                                                  int32_t p0) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t cnt = __popc(bits);
+  uint32_t incl = cnt;
+#pragma unroll
+  for (int s = 1; s < 32; s <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, s);
+    if (lane >= s) incl += y;
+  }
+  const uint32_t total = __shfl_sync(0xffffffffu, incl, 31);
+  if (total == 0u) return;
+  uint32_t base = 0;
+  if (lane == 31) base = atomicAdd(&sh.cand_count, total);
+  uint32_t slot = __shfl_sync(0xffffffffu, base, 31) + incl - cnt;
+#pragma unroll
+  for (int i = 0; i < kTkPer; ++i) {
+    if ((bits >> i) & 1u) {
       if (slot < (uint32_t)kTkCandCap) {
-        sh.cand_key[slot] = k;
-        sh.cand_pos[slot] = pos;
+        sh.cand_key[slot] = keys[i];
+        sh.cand_pos[slot] = p0 + i;
       }
+      ++slot;
     }
   }
+}
+
+// One element of the candidate sweep: above the top digit -> marked selected; returns whether it
+// is a candidate (in the top digit's bin).
+__device__ __forceinline__ bool classify(TopkShared& sh, uint32_t k, int32_t pos, uint32_t d1) {
+  const uint32_t d = k >> 20;
+  if (d > d1) atomicOr(&gt_map(sh)[pos >> 5], 1u << (pos & 31));
+  return d == d1;
 }
 
 // Candidate sweep over positions [0, n) (row relative). With kFloatTest the hot loop tests each
@@ -224,34 +246,27 @@ __device__ __forceinline__ void candidate_sweep(TopkShared& sh, const float* row
     for (int g = 0; g < 4; ++g) {
       const float v[kTkPer] = {a[g].x, a[g].y, a[g].z, a[g].w, c[g].x, c[g].y, c[g].z, c[g].w};
       const int32_t p0 = (int32_t)(base + g * kTkGroup + t * kTkPer);
+      uint32_t keys[kTkPer], bits = 0;
 #pragma unroll
       for (int i = 0; i < kTkPer; ++i) {
-        if (kFloatTest) {
-          if (v[i] >= f_lo) classify(sh, order_key(__float_as_uint(v[i])), p0 + i, d1);
-        } else {
-          classify(sh, order_key(__float_as_uint(v[i])), p0 + i, d1);
+        keys[i] = 0u;
+        if (!kFloatTest || v[i] >= f_lo) {
+          keys[i] = order_key(__float_as_uint(v[i]));
+          if (classify(sh, keys[i], p0 + i, d1)) bits |= 1u << i;
         }
       }
+      append_candidates(sh, bits, keys, p0);
     }
   }
 #pragma unroll 1
   for (; base < n; base += kTkGroup) {
-    uint32_t k[kTkPer];
+    uint32_t k[kTkPer], bits = 0;
     const int64_t p0 = base + (int64_t)t * kTkPer;
     const uint32_t v = load_keys(row, p0, n, k);
 #pragma unroll
     for (int i = 0; i < kTkPer; ++i)
-      if ((v >> i) & 1u) classify(sh, k[i], (int32_t)(p0 + i), d1);
-  }
-}
-
-__device__ __forceinline__ void keep_candidate(TopkShared& sh, uint32_t k, int32_t pos, uint32_t lo) {
-  if (k >= lo) {
-    const uint32_t slot = atomicAdd(&sh.cand_count, 1u);
-    if (slot < (uint32_t)kTkCandCap) {
-      sh.cand_key[slot] = k;
-      sh.cand_pos[slot] = pos;
-    }
+      if (((v >> i) & 1u) && classify(sh, k[i], (int32_t)(p0 + i), d1)) bits |= 1u << i;
+    append_candidates(sh, bits, k, (int32_t)p0);
   }
 }
 
@@ -363,19 +378,27 @@ __device__ bool sample_select(TopkShared& sh, const float* row, int64_t n, int K
     for (int g = 0; g < 4; ++g) {
       const float v[kTkPer] = {a[g].x, a[g].y, a[g].z, a[g].w, c[g].x, c[g].y, c[g].z, c[g].w};
       const int32_t p0 = (int32_t)(base + g * kTkGroup + t * kTkPer);
+      uint32_t keys[kTkPer], bits = 0;
 #pragma unroll
-      for (int i = 0; i < kTkPer; ++i)
-        if (v[i] >= f_lo) keep_candidate(sh, order_key(__float_as_uint(v[i])), p0 + i, lo);
+      for (int i = 0; i < kTkPer; ++i) {
+        keys[i] = 0u;
+        if (v[i] >= f_lo) {
+          keys[i] = order_key(__float_as_uint(v[i]));
+          if (keys[i] >= lo) bits |= 1u << i;
+        }
+      }
+      append_candidates(sh, bits, keys, p0);
     }
   }
 #pragma unroll 1
   for (; base < n; base += kTkGroup) {
-    uint32_t k[kTkPer];
+    uint32_t k[kTkPer], bits = 0;
     const int64_t p0 = base + (int64_t)t * kTkPer;
     const uint32_t v = load_keys(row, p0, n, k);
 #pragma unroll
     for (int i = 0; i < kTkPer; ++i)
-      if ((v >> i) & 1u) keep_candidate(sh, k[i], (int32_t)(p0 + i), lo);
+      if (((v >> i) & 1u) && k[i] >= lo) bits |= 1u << i;
+    append_candidates(sh, bits, k, (int32_t)p0);
   }
   __syncthreads();
   const uint32_t c = sh.cand_count;

@@ -329,7 +329,7 @@ def extra_configs(m, workloads, dev, stream, flush, hbm, steps):
     """Device-timed µs and roofline fractions of the decode-shard, spec-verify and capacity cases."""
     import torch
     res = {}
-    for cfg in (1, 3, 4):
+    for cfg in (1, 3, "3s", 4):
         case = workloads.make_case(cfg)
         cache, _, _ = fill_cache(m, workloads, case, dev)
         inputs = device_inputs(case, dev)
@@ -355,6 +355,11 @@ def extra_configs(m, workloads, dev, stream, flush, hbm, steps):
             entry["decode"] = roofline_entry(nbytes, flops, dec_ms, hbm)
         if cfg == 4:
             entry["aliased_page_fraction"] = case.notes.get("aliased_fraction")
+        if cfg in (3, "3s"):
+            # distinct rows a request's query tokens select, against the entries of their lists
+            uniq = [np.unique(case.topk_indices[b].reshape(-1)).size for b in range(case.B)]
+            entry["distinct_rows_per_request"] = float(np.mean(uniq))
+            entry["list_entries_per_request"] = case.Q * case.topk
         res[str(cfg)] = entry
         del cache, inputs
         torch.cuda.empty_cache()
@@ -494,7 +499,8 @@ def run_gpu(args, world, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     m.load_library()
-    case = workloads.make_case(2)
+    case_id = int(args.case) if args.case.isdigit() else args.case
+    case = workloads.make_case(case_id)
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     cache, pack_ms, pack_rows = fill_cache(m, workloads, case, dev, timed_pack=(stream, flush))
@@ -586,7 +592,8 @@ def run_gpu(args, world, rank, local):
         "metric": METRIC, "value": mean_ms * 1000.0, "unit": "us/step", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": mean_ms, "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": "f16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "B": case.B, "Q": case.Q, "H": case.H, "topk": case.topk,
+        "config": {"workload": WORKLOAD if case_id == 2 else workloads.CONFIG_NAMES[case_id], "B": case.B,
+                   "Q": case.Q, "H": case.H, "topk": case.topk,
                    "cache_pages": case.num_pages, "l2": "flushed before every step (256 MiB write)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "achieved_hbm_gbs": achieved,
@@ -609,14 +616,14 @@ def run_gpu(args, world, rank, local):
         "dev_status": st,
         "wall_s_timed_region": wall,
     }
-    if not args.no_extra and world == 1:
+    if not args.no_extra and world == 1 and case_id == 2:
         result["schedules"] = schedule_table(m, workloads, case, cache, dev, stream, flush, min(K, 200))
         result["indexer_topk"] = topk_table(m, case, cache, dev, stream, flush, hbm, min(K, 200))
         result["fp8_paths"] = fp8_table(m, workloads, case, cache, dev, stream, flush, hbm, min(K, 200), mean_ms)
         del cache, hq, hpt, htk, hsl, hout, hlse, ws
         torch.cuda.empty_cache()
         result["configs"] = extra_configs(m, workloads, dev, stream, flush, hbm, min(K, 200))
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and case_id == 2:
         result["cpu_baseline"] = cpu_baseline(case)
     return result
 
@@ -629,6 +636,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="skip the extra cases and the schedule table")
+    ap.add_argument("--case", default="2", choices=["0", "1", "2", "3", "3s", "4"],
+                    help="workload of the timed line (default 2, the headline; the others for profiling, "
+                         "without the extra tables)")
     ap.add_argument("--ref-units", type=int, default=0,
                     help="reference arm: query tokens per step (0 = all of the headline case)")
     args = ap.parse_args()

@@ -44,10 +44,17 @@ SMALL = [
     dict(B=1, Q=1, H=128, topk=129, L=(400,)),                            # four head groups
     dict(B=2, Q=2, H=32, topk=384, L=(1500, 1400), invalid_frac=0.25, dup=True, causal_tail=True),
     dict(B=4, Q=1, H=16, topk=50, L=(40, 60, 2000, 64)),                  # short contexts leave -1 entries
+    dict(B=2, Q=2, H=32, topk=256, L=(3000, 2600), shared=0.9),           # draft tokens sharing 90 % of rows
+    dict(B=1, Q=4, H=16, topk=512, L=(5000,), shared=0.9),
+    dict(B=2, Q=4, H=32, topk=300, L=(4000, 1900), shared=0.5),
 ]
 
 
-@pytest.mark.parametrize("spec", SMALL, ids=lambda s: "B{B}Q{Q}H{H}K{topk}".format(**s))
+def _spec_id(s):
+    return "B{B}Q{Q}H{H}K{topk}".format(**s) + (f"S{s['shared']}" if "shared" in s else "")
+
+
+@pytest.mark.parametrize("spec", SMALL, ids=_spec_id)
 @pytest.mark.parametrize("max_ctas", [0, "split", 1, 3])
 def test_small_cases_match_oracle(spec, max_ctas):
     case = workloads.small_case(seed=100 + len(str(spec)), **spec)
@@ -213,7 +220,7 @@ def test_dense_control_equals_dense_oracle():
 
 
 @pytest.mark.parametrize("schedule", ["default", "split"])
-@pytest.mark.parametrize("cfg", [0, 1, 2, 3, 4])
+@pytest.mark.parametrize("cfg", [0, 1, 2, 3, "3s", 4])
 def test_full_size_case_every_unit(cfg, schedule):
     """The five cases at full size, in the launch configuration the bench uses; the cache is
     packed on the device from device-drawn bf16 rows, and every query token is checked against

@@ -15,6 +15,8 @@ The five cases are:
   2 mixed agent     B=64, Q=1, H=32, L~U[70K,160K], top-k 2,048
   3 spec verify     B=32, Q=4, H=32, L_ctx~U[100K,150K] + 6,000 packed rows
   4 capacity        B=128, Q=1, H=32, 1.63M-token shared pool, lognormal L
+  3s spec verify, shared lists: case 3 with the 4 draft tokens' index lists sharing 90 % of
+                    their positions (one request-level set plus 10 % of each token's own)
   4d dense control  B=8, Q=1, H=32, L=8,000, top-k = every position in order
 
 Row values: latent = N(0,1) * c_d with c_d ~ lognormal(0, 0.5) per channel,
@@ -45,7 +47,9 @@ CONFIG_NAMES = {
     3: "spec-verify B=32 Q=4 H=32 L~U[100K,150K]+6000 topk=2048",
     4: "capacity B=128 H=32 pool=1.63M tokens topk=2048",
     "4d": "dense-control B=8 H=32 L=8000 topk=8000",
+    "3s": "spec-verify-shared B=32 Q=4 H=32 L~U[100K,150K]+6000 topk=2048, lists 90% shared",
 }
+SHARED_FRACTION = 0.9   # case 3s: fraction of a draft token's list taken from the request's shared set
 
 
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
@@ -96,6 +100,24 @@ def _queries(rng: np.random.Generator, B: int, Q: int, H: int) -> np.ndarray:
 def _draw_without_replacement(rng, lo: int, hi: int, n: int) -> np.ndarray:
     """n distinct integers uniform in [lo, hi)."""
     return (lo + rng.choice(hi - lo, size=n, replace=False)).astype(np.int64)
+
+
+def _shared_lists(rng, L: int, Q: int, K: int, shared: float) -> np.ndarray:
+    """Index lists [Q, K] of one request whose Q query tokens share most positions, as the draft
+    tokens of a speculative-verify step do: a set of K positions valid for every token (before
+    L - Q + 1); token j keeps round(shared * K) of them (its own random choice) and draws the rest
+    from its own causal range outside the set. Each list is in increasing position order (the
+    order a top-k selection writes)."""
+    base = _draw_without_replacement(rng, 0, L - Q + 1, K)
+    n_keep = int(round(shared * K))
+    out = np.empty((Q, K), dtype=np.int64)
+    for j in range(Q):
+        hi = L - Q + j + 1
+        keep = base[rng.permutation(K)[:n_keep]]
+        rest = np.setdiff1d(np.arange(hi, dtype=np.int64), base, assume_unique=True)
+        own = rest[rng.choice(rest.size, size=K - n_keep, replace=False)]
+        out[j] = np.sort(np.concatenate([keep, own]))
+    return out
 
 
 def host_rows(case: DecodeCase, pages: np.ndarray):
@@ -164,7 +186,7 @@ def _pages_for(lengths, perm, cycle=False):
 def make_case(cfg, seed: Optional[int] = None) -> DecodeCase:
     """Build the index structures and queries of one case (cfg in 0..4 or '4d')."""
     if seed is None:
-        seed = 1000 + (4 if cfg == "4d" else int(cfg)) + (500 if cfg == "4d" else 0)
+        seed = {"4d": 1504, "3s": 1703}.get(cfg, 1000 + (int(cfg) if cfg not in ("4d", "3s") else 0))
     rng = np.random.default_rng(seed)
     c = _channel_scale(rng)
     row_seed = int(rng.integers(1, 2**31 - 1))
@@ -201,7 +223,7 @@ def make_case(cfg, seed: Optional[int] = None) -> DecodeCase:
             sel = _draw_without_replacement(rng, 0, int(L[b]), n)
             topk[b, 0] = np.concatenate([sel, -np.ones(K - n, dtype=np.int64)])
         notes = {}
-    elif cfg == 3:
+    elif cfg in (3, "3s"):
         B, Q, H, K = 32, 4, 32, 2048
         new_rows = 6000
         L_ctx = (rng.integers(100_000, 150_001, size=B) // PAGE_TOKENS) * PAGE_TOKENS
@@ -215,10 +237,15 @@ def make_case(cfg, seed: Optional[int] = None) -> DecodeCase:
             slots.append(table[b, pos // PAGE_TOKENS].astype(np.int64) * PAGE_TOKENS + pos % PAGE_TOKENS)
         topk = np.empty((B, Q, K), dtype=np.int64)
         for b in range(B):
+            if cfg == "3s":
+                topk[b] = _shared_lists(rng, int(L[b]), Q, K, SHARED_FRACTION)
+                continue
             for j in range(Q):
                 causal = int(L[b]) - Q + j       # last position query j may see
                 topk[b, j] = _draw_without_replacement(rng, 0, causal + 1, K)
         notes = {"new_rows_per_request": new_rows, "L_ctx": L_ctx}
+        if cfg == "3s":
+            notes["shared_fraction"] = SHARED_FRACTION
         case_new_slots = np.concatenate(slots)
     elif cfg == 4:
         B, Q, H, K = 128, 1, 32, 2048
@@ -249,18 +276,19 @@ def make_case(cfg, seed: Optional[int] = None) -> DecodeCase:
         name=CONFIG_NAMES[cfg], B=B, Q=Q, H=H, topk=K, num_pages=num_pages,
         seq_lens=L.astype(np.int32), page_table=table, topk_indices=topk.astype(np.int32),
         q_bits=q_bits, channel_scale=c, row_seed=row_seed, notes=notes)
-    if cfg == 3:
+    if cfg in (3, "3s"):
         case.new_slots = case_new_slots
     return case
 
 
 def small_case(B=2, Q=1, H=16, topk=200, L=(700, 1000), num_pages=None, seed=7,
-               invalid_frac=0.0, dup=False, causal_tail=False) -> DecodeCase:
+               invalid_frac=0.0, dup=False, causal_tail=False, shared=None) -> DecodeCase:
     """A small random case for parity tests (a few tiles and a ragged tail).
 
     invalid_frac replaces that fraction of index entries with -1 or with
     positions past the sequence; causal_tail makes some entries point past the
-    query's causal position.
+    query's causal position; shared (a fraction) gives the Q tokens of a request
+    lists that share that fraction of their positions (see _shared_lists).
     """
     rng = np.random.default_rng(seed)
     L = np.asarray(L, dtype=np.int64)
@@ -273,11 +301,18 @@ def small_case(B=2, Q=1, H=16, topk=200, L=(700, 1000), num_pages=None, seed=7,
     topk = np.empty((B, Q, topk), dtype=np.int64)
     K = topk.shape[2]
     for b in range(B):
+        shared_rows = None
+        if shared is not None:
+            assert int(L[b]) - Q + 1 >= 2 * K, "shared lists need a range of at least 2K positions"
+            shared_rows = _shared_lists(rng, int(L[b]), Q, K, shared)
         for j in range(Q):
             hi = int(L[b]) - Q + j + 1
             n = min(K, hi)
-            sel = _draw_without_replacement(rng, 0, hi, n)
-            row = np.concatenate([sel, -np.ones(K - n, dtype=np.int64)])
+            if shared_rows is not None:
+                row = shared_rows[j].copy()
+            else:
+                sel = _draw_without_replacement(rng, 0, hi, n)
+                row = np.concatenate([sel, -np.ones(K - n, dtype=np.int64)])
             if dup and n >= 2:
                 row[1] = row[0]
             if invalid_frac > 0:

@@ -12,6 +12,11 @@ What the pages fix:
   * every path computes the same attention (oracle.attention), only over differently rounded
     rows.
 
+  * TokenSpeed's per-token FP8 cache (the "TokenSpeed" walkthrough, section 8 "MLA KV layout", its
+    per_token_head write path): the latent is stored as FP8 E4M3 of latent / scale with one fp32
+    scale = max(amax, 1e-26) / 448 per token (amax the largest |latent value|), computed in fp32;
+    the rope part is divided by the same scale and kept in the model dtype (bf16).
+
 Readings (listed in the design notes):
   * an FP8 row is E4M3 of each value (codec.e4m3_encode: nearest, ties to even, saturating at
     +-448, NaN kept as 0x7F with its sign), latent in bytes 0..511, rope in bytes 512..575, and no
@@ -24,7 +29,14 @@ Readings (listed in the design notes):
     selected row to staged row (b*Q + j)*K + i and makes the FP8 decode's list entry i equal to i
     when the entry is usable under the decode's rule (oracle.attention.valid_entries), else -1;
     staged rows of unusable entries are not written. The FP8 decode then runs over the staged
-    rows as B*Q one-query requests of length K whose page table is the identity.
+    rows as B*Q one-query requests of length K whose page table is the identity;
+  * the per-token FP8 row (GB300 layout of TokenSpeed's three buffers) is 672 bytes: bytes
+    0..511 the E4M3 latent codes, 512..639 the 64 bf16 rope values, 640..643 the fp32 scale
+    (little-endian), 644..671 zero; one row keeps a token's bytes together for one gather, and
+    four rows are a whole number of 128-byte units. The arithmetic follows TokenSpeed's write
+    path: amax, the scale and both divisions in fp32 (IEEE, round to nearest even), then E4M3
+    (nearest even, saturating) and bf16 (nearest even) rounding. Dequantised values are
+    E4M3(code) * scale and bf16(rope) * scale (exact in float64).
 """
 from __future__ import annotations
 
@@ -101,9 +113,70 @@ def stage(cache, page_table, topk_indices, seq_lens, Q: int):
     return staged, written, new_topk, pt, np.full(B * Q, K, dtype=np.int32)
 
 
+TOKEN_ROW_BYTES = 672
+TOKEN_ROPE_OFFSET = 512
+TOKEN_SCALE_OFFSET = 640
+
+
+def _f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """float32 values -> bf16 bit patterns, round to nearest even (NaN kept as a quiet NaN)."""
+    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    rounded = (b + 0x7FFF + ((b >> 16) & 1)) >> 16
+    nan = np.isnan(x)
+    return np.where(nan, (b >> 16) | 0x40, rounded).astype(np.uint16)
+
+
+def encode_rows_token(latent_bits: np.ndarray, rope_bits: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns (uint16 [N, 512], [N, 64]) -> per-token FP8 rows uint8 [N, 672]."""
+    lat = codec.bf16_bits_to_f64(np.asarray(latent_bits, dtype=np.uint16).reshape(-1, D_LATENT)).astype(np.float32)
+    rope = codec.bf16_bits_to_f64(np.asarray(rope_bits, dtype=np.uint16).reshape(-1, D_ROPE)).astype(np.float32)
+    n = lat.shape[0]
+    amax = np.abs(lat).max(axis=1, keepdims=True)                     # fp32, exact
+    scale = (np.maximum(amax, np.float32(1e-26)) / np.float32(448.0)).astype(np.float32)
+    codes = codec.e4m3_encode((lat / scale).astype(np.float32).astype(np.float64))
+    rope_bf = _f32_to_bf16_bits((rope / scale).astype(np.float32))
+    rows = np.zeros((n, TOKEN_ROW_BYTES), dtype=np.uint8)
+    rows[:, :D_LATENT] = codes
+    rows[:, TOKEN_ROPE_OFFSET:TOKEN_SCALE_OFFSET] = rope_bf.view(np.uint8).reshape(n, 2 * D_ROPE)
+    rows[:, TOKEN_SCALE_OFFSET:TOKEN_SCALE_OFFSET + 4] = scale.astype('<f4').view(np.uint8).reshape(n, 4)
+    return rows
+
+
+def dequant_rows_token(rows: np.ndarray) -> np.ndarray:
+    """Per-token FP8 rows uint8 [..., 672] -> float64 [N, 576]."""
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.uint8).reshape(-1, TOKEN_ROW_BYTES))
+    scale = rows[:, TOKEN_SCALE_OFFSET:TOKEN_SCALE_OFFSET + 4].copy().view('<f4').astype(np.float64)   # [N, 1]
+    lat = codec.e4m3_decode(rows[:, :D_LATENT]) * scale
+    rope_bits = rows[:, TOKEN_ROPE_OFFSET:TOKEN_SCALE_OFFSET].copy().view('<u2')
+    rope = codec.bf16_bits_to_f64(rope_bits) * scale
+    return np.concatenate([lat, rope], axis=1)
+
+
+def write_cache_token(cache: np.ndarray, latent_bits, rope_bits, slot_mapping) -> None:
+    """Write per-token FP8 rows into cache uint8 [num_pages, 64, 672] at the slots (slot -1, or any
+    slot outside the cache, is skipped)."""
+    rows = encode_rows_token(latent_bits, rope_bits)
+    flat = cache.reshape(-1, TOKEN_ROW_BYTES)
+    for r, s in enumerate(np.asarray(slot_mapping, dtype=np.int64)):
+        if 0 <= s < flat.shape[0]:
+            flat[s] = rows[r]
+
+
+def sparse_decode_token(q_bits, cache, page_table, topk_indices, seq_lens, scale, units=None):
+    """Sparse MLA decode over a paged per-token FP8 cache uint8 [num_pages, 64, 672]; the same
+    rules and outputs as attention.sparse_decode."""
+    return _sparse_decode_rows(q_bits, cache, page_table, topk_indices, seq_lens, scale, units,
+                               dequant_rows_token, TOKEN_ROW_BYTES)
+
+
 def sparse_decode_fp8(q_bits, cache, page_table, topk_indices, seq_lens, scale, units=None):
     """Sparse MLA decode over a paged FP8 cache uint8 [num_pages, 64, 576]; the same rules and
     outputs as attention.sparse_decode."""
+    return _sparse_decode_rows(q_bits, cache, page_table, topk_indices, seq_lens, scale, units,
+                               dequant_rows_fp8, FP8_ROW_BYTES)
+
+
+def _sparse_decode_rows(q_bits, cache, page_table, topk_indices, seq_lens, scale, units, dequant, row_bytes):
     q = codec.bf16_bits_to_f64(q_bits)
     B, Q, H, _ = q.shape
     num_pages = cache.shape[0]
@@ -116,6 +189,6 @@ def sparse_decode_fp8(q_bits, cache, page_table, topk_indices, seq_lens, scale, 
         ok = valid_entries(idx, L, L - Q + j, page_table[b], num_pages)
         sel = idx[ok]
         pages = np.asarray(page_table[b], dtype=np.int64)[sel // PAGE_TOKENS]
-        c = dequant_rows_fp8(cache[pages, sel % PAGE_TOKENS]) if sel.size else np.zeros((0, D_QK))
+        c = dequant(cache[pages, sel % PAGE_TOKENS]) if sel.size else np.zeros((0, D_QK))
         out[b, j], lse[b, j] = attend(q[b, j], c, scale)
     return out, lse

@@ -136,3 +136,52 @@ def test_fp8_decode_matches_torch_sdpa_and_the_staged_pipeline():
             np.testing.assert_allclose(so[u, 0], o, rtol=1e-13, atol=1e-13)
             np.testing.assert_allclose(sls[u, 0], l, rtol=1e-13, atol=1e-13)
     assert np.max(np.abs(so.reshape(no.shape) - no)) < 0.1 * np.max(np.abs(no))
+
+
+def test_per_token_rows_against_torch_roundings_and_bounds():
+    """Per-token FP8 rows: fp32 scale and divisions, then torch's E4M3 and bf16 conversions (library
+    roundings) on the same fp32 quotients; the latent's largest element codes as 448; the
+    dequantised latent is within half an E4M3 step of the input; the layout byte by byte."""
+    rng = np.random.default_rng(7)
+    n = 64
+    lat32 = (rng.standard_normal((n, 512)) * rng.lognormal(0, 2, (n, 1))).astype(np.float32)
+    lat32[0] = 0.0                                                     # all-zero row: scale from the 1e-26 floor
+    lat = workloads.f32_to_bf16_bits(lat32)
+    rope = workloads.f32_to_bf16_bits((rng.standard_normal((n, 64)) * 2).astype(np.float32))
+    rows = fp8rows.encode_rows_token(lat, rope)
+    assert rows.shape == (n, 672) and not rows[:, 644:].any()
+    x = torch.from_numpy(codec.bf16_bits_to_f64(lat)).float()
+    r = torch.from_numpy(codec.bf16_bits_to_f64(rope)).float()
+    scale = torch.clamp(x.abs().amax(dim=1, keepdim=True), min=1e-26) / 448.0
+    np.testing.assert_array_equal(rows[:, 640:644].copy().view("<f4"), scale.numpy())
+    np.testing.assert_array_equal(rows[:, :512], (x / scale).to(torch.float8_e4m3fn).view(torch.uint8).numpy())
+    np.testing.assert_array_equal(rows[:, 512:640].copy().view("<u2"),
+                                  (r / scale).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16))
+    big = np.abs(codec.bf16_bits_to_f64(lat)).argmax(axis=1)
+    assert all((rows[i, big[i]] & 0x7F) == 0x7E for i in range(1, n))           # amax -> 448
+    d = fp8rows.dequant_rows_token(rows)
+    xl = codec.bf16_bits_to_f64(lat)
+    s = rows[:, 640:644].copy().view("<f4").astype(np.float64)
+    assert np.all(np.abs(d[:, :512] - xl) <= np.maximum(np.abs(xl) / 16, s * 2.0 ** -10) * (1 + 1e-6))
+    assert np.all(np.abs(d[:, 512:] - codec.bf16_bits_to_f64(rope)) <= np.abs(codec.bf16_bits_to_f64(rope)) * 2.0 ** -8 + 1e-30)
+
+
+def test_per_token_decode_matches_torch_sdpa():
+    case, _, lat, rope = _small_case_cache(B=2, Q=2, H=4, topk=128, L=(500, 900), seed=13)
+    cache = np.zeros((case.num_pages, 64, 672), np.uint8)
+    fp8rows.write_cache_token(cache, lat, rope, np.arange(case.num_pages * 64))
+    out, lse = fp8rows.sparse_decode_token(case.q_bits, cache, case.page_table, case.topk_indices,
+                                           case.seq_lens, case.softmax_scale)
+    q = codec.bf16_bits_to_f64(case.q_bits)
+    for b in range(case.B):
+        for j in range(case.Q):
+            idx = case.topk_indices[b, j].astype(np.int64)
+            rr = cache[case.page_table[b][idx // 64], idx % 64]
+            s = torch.from_numpy(rr[:, 640:644].copy().view("<f4").astype(np.float64))
+            lat_v = torch.from_numpy(rr[:, :512].copy()).view(torch.float8_e4m3fn).to(torch.float64) * s
+            rope_v = torch.from_numpy(rr[:, 512:640].copy()).view(torch.bfloat16).to(torch.float64) * s
+            c = torch.cat([lat_v, rope_v], dim=1)
+            ref = torch.nn.functional.scaled_dot_product_attention(
+                torch.from_numpy(q[b, j])[None, :, None, :], c[None, None].expand(1, case.H, -1, -1),
+                c[None, None, :, :512].expand(1, case.H, -1, -1), scale=case.softmax_scale)
+            np.testing.assert_allclose(out[b, j], ref[0, :, 0].numpy(), rtol=1e-12, atol=1e-12)

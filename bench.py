@@ -406,17 +406,31 @@ def fp8_table(m, workloads, case, cache, dev, stream, flush, hbm, steps, native_
 
     fp8_us, = timed([lambda: m.sparse_mla_decode_fp8(q, cache8, pt, tk, sl, case.softmax_scale, out=out, lse=lse,
                                                      workspace=ws, stream=stream)])
+    del cache8
+    torch.cuda.empty_cache()
+    cache_t = torch.empty((case.num_pages, 64, 672), dtype=torch.uint8, device=dev)
+    for ci, s0 in enumerate(range(0, rows_total, chunk)):
+        n = min(chunk, rows_total - s0)
+        lat, rope = workloads.device_rows(case, n, dev, seed_offset=ci)
+        m.fp8_token_kv_pack(lat, rope, torch.arange(s0, s0 + n, device=dev), cache_t)
+        del lat, rope
+    tok_us, = timed([lambda: m.sparse_mla_decode_fp8_token(q, cache_t, pt, tk, sl, case.softmax_scale, out=out,
+                                                           lse=lse, workspace=ws, stream=stream)])
+    del cache_t
+    torch.cuda.empty_cache()
     stage_us, staged_dec_us = timed([
         lambda: m.nvfp4_stage_fp8(cache, pt, tk, sl, staging=staging, stream=stream),
         lambda: m.sparse_mla_decode_fp8(qs, staged, spt, sidx, ssl, case.softmax_scale, out=out_s, lse=lse_s,
                                         workspace=ws, stream=stream)])
     n_rows = int(sum(min(int(case.seq_lens[b]), case.topk) for b in range(case.B))) * case.Q
-    del cache8, staging, staged
+    del staging, staged
     torch.cuda.empty_cache()
     return {
         "rows_selected": n_rows,
         "native": {"us": native_ms * 1e3, "bytes_per_row": 352},
         "fp8_cache": {"us": fp8_us, "bytes_per_row": 576},
+        "fp8_per_token_cache": {"us": tok_us, "bytes_per_row": 672,
+                                "format": "E4M3 latent / scale, bf16 rope / scale, fp32 scale per token"},
         "staged": {"us": stage_us + staged_dec_us, "stage_us": stage_us, "fp8_decode_us": staged_dec_us,
                    "bytes_per_row": 352 + 576 + 576},
         "pages_reference_gb200_us": {"native": 12.0, "staged": 17.7, "fp8": 13.7,

@@ -356,6 +356,40 @@ int sparse_mla_decode_fp8(const void* q, const void* kv_cache_fp8, int64_t num_p
                           int Q, int H, int topk, float softmax_scale, void* out, float* lse, void* workspace,
                           size_t workspace_bytes, int32_t* dev_status, void* stream);
 
+/*
+ * Per-token FP8 comparison path: the per-token FP8 cache of the "TokenSpeed"
+ * engine walkthrough (section 8, "MLA KV layout", its per_token_head write
+ * path: the latent divided by scale = max(amax, 1e-26) / 448 of the token,
+ * stored as E4M3; the rope divided by the same scale, kept in bf16; the scale
+ * in fp32). GB300 layout (672 bytes per row): bytes 0..511 the E4M3 codes,
+ * 512..639 the 64 bf16 rope values, 640..643 the fp32 scale (little-endian),
+ * 644..671 zero. Four rows are a whole number of 128-byte units, so a gather
+ * of four rows lands on the 128-byte boundaries the TMA unit requires.
+ *
+ * fp8_token_kv_pack: bf16 latent + rope rows -> such rows of a paged cache
+ * uint8 [num_pages, 64, 672] (device memory); amax, scale and divisions in
+ * IEEE fp32, then E4M3 (nearest even, saturating) and bf16 (nearest even).
+ * Arguments, checks, slot rules and dev_status counting as mla_kv_pack;
+ * inputs must be finite (a NaN or an infinity gives an unspecified row).
+ */
+int fp8_token_kv_pack(const void* latent, int64_t latent_row_stride, const void* rope, int64_t rope_row_stride,
+                      const int64_t* slot_mapping, int64_t num_tokens, void* kv_cache_tok, int64_t num_pages,
+                      int32_t* dev_status, void* stream);
+
+/*
+ * sparse_mla_decode_fp8_token: sparse_mla_decode over a per-token FP8 cache
+ * (uint8 [num_pages, 64, 672], device memory): the same arguments, entry rules,
+ * outputs and workspace. The kernel scores q against E4M3 / bf16 values
+ * converted to fp16 (the rope exactly for values in fp16's normal range) and
+ * applies each row's scale to its score and to its softmax weight. Always the
+ * split schedule; out and lse must be device memory (else
+ * NVFP4MLA_ERR_UNSUPPORTED).
+ */
+int sparse_mla_decode_fp8_token(const void* q, const void* kv_cache_tok, int64_t num_pages, const int32_t* page_table,
+                                int64_t max_pages_per_seq, const int32_t* topk_indices, const int32_t* seq_lens,
+                                int B, int Q, int H, int topk, float softmax_scale, void* out, float* lse,
+                                void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream);
+
 /* Human-readable name of a return code (static string, never NULL). */
 const char* nvfp4mla_status_string(int status);
 

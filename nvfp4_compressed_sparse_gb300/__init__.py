@@ -8,7 +8,8 @@ raises; there is no CPU fallback.
 C entry points (see include/nvfp4mla.h): mla_kv_pack,
 sparse_mla_decode_workspace_size, sparse_mla_decode, sparse_mla_decode_plan,
 sparse_mla_decode_noalloc, indexer_topk, fp8_kv_pack, nvfp4_stage_fp8,
-sparse_mla_decode_fp8, nvfp4mla_status_string.
+sparse_mla_decode_fp8, fp8_token_kv_pack, sparse_mla_decode_fp8_token,
+nvfp4mla_status_string.
 """
 from __future__ import annotations
 
@@ -18,6 +19,7 @@ import threading
 
 ROW_BYTES = 352
 FP8_ROW_BYTES = 576
+TOKEN_ROW_BYTES = 672
 PAGE_TOKENS = 64
 LATENT_DIM = 512
 ROPE_DIM = 64
@@ -75,6 +77,11 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.sparse_mla_decode_fp8.argtypes = [vp, vp, i64, vp, i64, vp, vp, i32, i32, i32, i32, ctypes.c_float,
                                               vp, vp, vp, sz, vp, vp]
         lib.sparse_mla_decode_fp8.restype = i32
+        lib.fp8_token_kv_pack.argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, vp, vp]
+        lib.fp8_token_kv_pack.restype = i32
+        lib.sparse_mla_decode_fp8_token.argtypes = [vp, vp, i64, vp, i64, vp, vp, i32, i32, i32, i32, ctypes.c_float,
+                                                    vp, vp, vp, sz, vp, vp]
+        lib.sparse_mla_decode_fp8_token.restype = i32
         lib.nvfp4mla_status_string.argtypes = [i32]
         lib.nvfp4mla_status_string.restype = ctypes.c_char_p
         _LIB = lib
@@ -230,6 +237,16 @@ def sparse_mla_decode(q, kv_cache, page_table, topk_indices, seq_lens, softmax_s
 def fp8_kv_pack(latent, rope, slot_mapping, kv_cache_fp8, dev_status=None, stream=None) -> None:
     """Encode bf16 latent [N,512] + rope [N,64] rows as 576-byte FP8 rows into kv_cache_fp8 uint8
     [P,64,576] at slot_mapping (int64 [N])."""
+    _pack_rows("fp8_kv_pack", FP8_ROW_BYTES, latent, rope, slot_mapping, kv_cache_fp8, dev_status, stream)
+
+
+def fp8_token_kv_pack(latent, rope, slot_mapping, kv_cache_tok, dev_status=None, stream=None) -> None:
+    """Encode bf16 latent [N,512] + rope [N,64] rows as 672-byte per-token FP8 rows (E4M3 latent /
+    scale, bf16 rope / scale, fp32 scale) into kv_cache_tok uint8 [P,64,672] at slot_mapping."""
+    _pack_rows("fp8_token_kv_pack", TOKEN_ROW_BYTES, latent, rope, slot_mapping, kv_cache_tok, dev_status, stream)
+
+
+def _pack_rows(entry, row_bytes, latent, rope, slot_mapping, kv_cache_fp8, dev_status, stream):
     import torch
     _check(latent, "latent", torch.bfloat16, ndim=2, contiguous=False)
     _check(rope, "rope", torch.bfloat16, latent.device, 2, contiguous=False)
@@ -240,15 +257,15 @@ def fp8_kv_pack(latent, rope, slot_mapping, kv_cache_fp8, dev_status=None, strea
     n = latent.shape[0]
     if latent.shape[1] != LATENT_DIM or rope.shape != (n, ROPE_DIM) or slot_mapping.shape[0] != n:
         raise ValueError("shape mismatch")
-    if kv_cache_fp8.shape[1:] != (PAGE_TOKENS, FP8_ROW_BYTES):
-        raise ValueError("kv_cache_fp8 must be [num_pages, 64, 576]")
+    if kv_cache_fp8.shape[1:] != (PAGE_TOKENS, row_bytes):
+        raise ValueError(f"the cache must be [num_pages, 64, {row_bytes}]")
     if dev_status is not None:
         _check(dev_status, "dev_status", torch.int32, latent.device, 1)
-    rc = load_library().fp8_kv_pack(_ptr(latent), latent.stride(0), _ptr(rope), rope.stride(0), _ptr(slot_mapping),
-                                    n, _ptr(kv_cache_fp8), kv_cache_fp8.shape[0], _ptr(dev_status),
-                                    _stream_ptr(stream))
+    rc = getattr(load_library(), entry)(_ptr(latent), latent.stride(0), _ptr(rope), rope.stride(0),
+                                        _ptr(slot_mapping), n, _ptr(kv_cache_fp8), kv_cache_fp8.shape[0],
+                                        _ptr(dev_status), _stream_ptr(stream))
     if rc != 0:
-        raise NvFp4MlaError(rc, "fp8_kv_pack")
+        raise NvFp4MlaError(rc, entry)
 
 
 def nvfp4_stage_fp8(kv_cache, page_table, topk_indices, seq_lens, staging=None, dev_status=None, stream=None):
@@ -295,11 +312,24 @@ def nvfp4_stage_fp8(kv_cache, page_table, topk_indices, seq_lens, staging=None, 
 def sparse_mla_decode_fp8(q, kv_cache_fp8, page_table, topk_indices, seq_lens, softmax_scale, out=None, lse=None,
                           workspace=None, dev_status=None, stream=None):
     """sparse_mla_decode over a cache of 576-byte FP8 rows (uint8 [P,64,576]); device tensors only."""
+    return _decode_rows("sparse_mla_decode_fp8", FP8_ROW_BYTES, q, kv_cache_fp8, page_table, topk_indices, seq_lens,
+                        softmax_scale, out, lse, workspace, dev_status, stream)
+
+
+def sparse_mla_decode_fp8_token(q, kv_cache_tok, page_table, topk_indices, seq_lens, softmax_scale, out=None,
+                                lse=None, workspace=None, dev_status=None, stream=None):
+    """sparse_mla_decode over a cache of 672-byte per-token FP8 rows (uint8 [P,64,672]); device tensors only."""
+    return _decode_rows("sparse_mla_decode_fp8_token", TOKEN_ROW_BYTES, q, kv_cache_tok, page_table, topk_indices,
+                        seq_lens, softmax_scale, out, lse, workspace, dev_status, stream)
+
+
+def _decode_rows(entry, row_bytes, q, kv_cache_fp8, page_table, topk_indices, seq_lens, softmax_scale, out, lse,
+                 workspace, dev_status, stream):
     import torch
-    _check(kv_cache_fp8, "kv_cache_fp8", torch.uint8, ndim=3)
+    _check(kv_cache_fp8, "kv_cache", torch.uint8, ndim=3)
     dev = kv_cache_fp8.device
-    if kv_cache_fp8.shape[1:] != (PAGE_TOKENS, FP8_ROW_BYTES):
-        raise ValueError("kv_cache_fp8 must be [num_pages, 64, 576]")
+    if kv_cache_fp8.shape[1:] != (PAGE_TOKENS, row_bytes):
+        raise ValueError(f"the cache must be [num_pages, 64, {row_bytes}]")
     _check(q, "q", torch.bfloat16, dev, 4)
     _check(page_table, "page_table", torch.int32, dev, 2)
     _check(topk_indices, "topk_indices", torch.int32, dev, 3)
@@ -318,12 +348,12 @@ def sparse_mla_decode_fp8(q, kv_cache_fp8, page_table, topk_indices, seq_lens, s
         workspace = torch.empty(max(sparse_mla_decode_workspace_size(B, Q, H, K), 1), dtype=torch.uint8, device=dev)
     if dev_status is not None:
         _check(dev_status, "dev_status", torch.int32, dev, 1)
-    rc = load_library().sparse_mla_decode_fp8(
+    rc = getattr(load_library(), entry)(
         _ptr(q), _ptr(kv_cache_fp8), kv_cache_fp8.shape[0], _ptr(page_table), page_table.shape[1],
         _ptr(topk_indices), _ptr(seq_lens), B, Q, H, K, float(softmax_scale), _ptr(out), _ptr(lse), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream_ptr(stream))
     if rc != 0:
-        raise NvFp4MlaError(rc, "sparse_mla_decode_fp8")
+        raise NvFp4MlaError(rc, entry)
     return out, lse
 
 

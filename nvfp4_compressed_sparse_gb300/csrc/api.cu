@@ -280,7 +280,7 @@ static int decode_impl(const void* q, const void* kv_cache, int64_t num_pages, c
                        int64_t max_pages_per_seq, const int32_t* topk_indices, const int32_t* seq_lens, int B, int Q,
                        int H, int topk, float softmax_scale, void* out, float* lse, void* workspace,
                        size_t workspace_bytes, int32_t* dev_status, uint32_t flags, void* stream, int row_fmt) {
-  const int row_bytes = row_fmt == 1 ? kFp8RowBytes : kRowBytes;
+  const int row_bytes = row_fmt == 1 ? kFp8RowBytes : (row_fmt == 2 ? kTokRowBytes : kRowBytes);
   if (!sizes_ok(B, Q, H, topk)) return NVFP4MLA_ERR_INVALID_ARG;
   if (q == nullptr || kv_cache == nullptr || page_table == nullptr || topk_indices == nullptr ||
       seq_lens == nullptr || out == nullptr || lse == nullptr)
@@ -298,7 +298,7 @@ static int decode_impl(const void* q, const void* kv_cache, int64_t num_pages, c
       k_lse == kPtrInvalid || pointer_kind(kv_cache) != kPtrDevice ||
       (dev_status != nullptr && pointer_kind(dev_status) != kPtrDevice))
     return NVFP4MLA_ERR_INVALID_ARG;
-  if (row_fmt == 1) {
+  if (row_fmt != 0) {
     if (k_out != kPtrDevice || k_lse != kPtrDevice) return NVFP4MLA_ERR_UNSUPPORTED;
     flags = (flags & ~(NVFP4MLA_FLAG_CLUSTER | NVFP4MLA_FLAG_CLUSTER_ANY)) | NVFP4MLA_FLAG_SPLIT;
   }
@@ -368,6 +368,48 @@ int sparse_mla_decode_fp8(const void* q, const void* kv_cache_fp8, int64_t num_p
                           size_t workspace_bytes, int32_t* dev_status, void* stream) {
   return decode_impl(q, kv_cache_fp8, num_pages, page_table, max_pages_per_seq, topk_indices, seq_lens, B, Q, H,
                      topk, softmax_scale, out, lse, workspace, workspace_bytes, dev_status, 0u, stream, 1);
+}
+
+int sparse_mla_decode_fp8_token(const void* q, const void* kv_cache_tok, int64_t num_pages, const int32_t* page_table,
+                                int64_t max_pages_per_seq, const int32_t* topk_indices, const int32_t* seq_lens,
+                                int B, int Q, int H, int topk, float softmax_scale, void* out, float* lse,
+                                void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  return decode_impl(q, kv_cache_tok, num_pages, page_table, max_pages_per_seq, topk_indices, seq_lens, B, Q, H,
+                     topk, softmax_scale, out, lse, workspace, workspace_bytes, dev_status, 0u, stream, 2);
+}
+
+// Shared checks of the bf16-row packs (mla_kv_pack's rules); row_bytes of the destination format.
+static int check_pack_args(const void* latent, int64_t latent_row_stride, const void* rope, int64_t rope_row_stride,
+                           const int64_t* slot_mapping, int64_t num_tokens, const void* cache, int64_t num_pages,
+                           const int32_t* dev_status, int row_bytes) {
+  if (num_tokens < 0 || num_pages < 1) return NVFP4MLA_ERR_INVALID_ARG;
+  if (latent == nullptr || rope == nullptr || slot_mapping == nullptr || cache == nullptr)
+    return NVFP4MLA_ERR_INVALID_ARG;
+  if (latent_row_stride < kLatent || rope_row_stride < kRope) return NVFP4MLA_ERR_INVALID_ARG;
+  if (num_pages > (INT64_MAX / (kPageTokens * (int64_t)row_bytes))) return NVFP4MLA_ERR_INVALID_ARG;
+  if (!aligned(latent, 16) || (latent_row_stride % 8) != 0) return NVFP4MLA_ERR_ALIGNMENT;
+  if (!aligned(rope, 4) || (rope_row_stride % 2) != 0) return NVFP4MLA_ERR_ALIGNMENT;
+  if (!aligned(cache, 16) || !aligned(slot_mapping, 8)) return NVFP4MLA_ERR_ALIGNMENT;
+  if (dev_status != nullptr && !aligned(dev_status, 4)) return NVFP4MLA_ERR_ALIGNMENT;
+  if (pointer_kind(latent) != kPtrDevice || pointer_kind(rope) != kPtrDevice ||
+      pointer_kind(slot_mapping) != kPtrDevice || pointer_kind(cache) != kPtrDevice ||
+      (dev_status != nullptr && pointer_kind(dev_status) != kPtrDevice))
+    return NVFP4MLA_ERR_INVALID_ARG;
+  return NVFP4MLA_OK;
+}
+
+int fp8_token_kv_pack(const void* latent, int64_t latent_row_stride, const void* rope, int64_t rope_row_stride,
+                      const int64_t* slot_mapping, int64_t num_tokens, void* kv_cache_tok, int64_t num_pages,
+                      int32_t* dev_status, void* stream) {
+  if (num_tokens == 0 && num_pages >= 1) return NVFP4MLA_OK;
+  const int rc = check_pack_args(latent, latent_row_stride, rope, rope_row_stride, slot_mapping, num_tokens,
+                                 kv_cache_tok, num_pages, dev_status, kTokRowBytes);
+  if (rc != NVFP4MLA_OK) return rc;
+  const cudaError_t err = launch_token_pack(static_cast<const uint16_t*>(latent), latent_row_stride,
+                                            static_cast<const uint16_t*>(rope), rope_row_stride, slot_mapping,
+                                            num_tokens, static_cast<uint8_t*>(kv_cache_tok), num_pages, dev_status,
+                                            static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? NVFP4MLA_OK : NVFP4MLA_ERR_CUDA;
 }
 
 int fp8_kv_pack(const void* latent, int64_t latent_row_stride, const void* rope, int64_t rope_row_stride,

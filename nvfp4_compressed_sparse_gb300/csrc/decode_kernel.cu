@@ -46,15 +46,20 @@ using namespace ptx;
 constexpr int kThreads = 512;
 constexpr int kRingStages = 4;            // a tile's rows in 4 quarters of 32 rows, each with its own barrier
 // Cache row formats. kFmt 0: the 352-byte NVFP4 row; the ring holds a whole tile (4 buffers of 32
-// rows). kFmt 1: the 576-byte FP8 row of the comparison path; a whole tile does not fit next to the
-// V tile, so the ring holds 2 buffers and quarter q uses buffer q % 2 (quarters 0, 1 land first,
-// then 2, 3). Rows land densely: gather4 writes 4 rows per instruction.
+// rows). kFmt 1: the 576-byte FP8 row of the comparison path; kFmt 2: the 672-byte per-token FP8
+// row (E4M3 latent / scale, bf16 rope / scale, fp32 scale). For 1 and 2 a whole tile does not fit
+// next to the V tile, so the ring holds 2 buffers and quarter q uses buffer q % 2 (quarters 0, 1
+// land first, then 2, 3). Rows land densely: gather4 writes 4 rows per instruction, and 4 rows of
+// every format are a whole number of 128-byte units (gather destinations must be 128-byte aligned).
+// kFmt 2 also keeps the per-row scales of the two tiles in flight (2 x 128 fp32) after the ring.
 template <int kFmt>
 struct RowFmt {
-  static constexpr int kBytes = kFmt == 0 ? kRowBytes : kFp8RowBytes;
+  static constexpr int kBytes = kFmt == 0 ? kRowBytes : (kFmt == 1 ? kFp8RowBytes : kTokRowBytes);
   static constexpr int kBufs = kFmt == 0 ? 4 : 2;
-  static constexpr int kStageBytes = 32 * kBytes;        // 11264 = 88 x 128 B; 18432 = 144 x 128 B
+  static constexpr int kStageBytes = 32 * kBytes;        // 11264 = 88, 18432 = 144, 21504 = 168 x 128 B
   static constexpr int kRingBytes = kBufs * kStageBytes;
+  static constexpr int kScaleBytes = kFmt == 2 ? 2 * kTileTokens * 4 : 0;
+  static_assert((4 * kBytes) % 128 == 0, "gather4 destinations must stay 128-byte aligned");
 };
 constexpr int kVBytes = 8 * 128 * 128;    // 8 SW128 atoms x 128 rows x 128 B
 constexpr int kTmemCols = 512;
@@ -382,7 +387,7 @@ __device__ __forceinline__ void convert_fp8_64(const uint8_t* src, uint32_t (&r)
 // V tile in shared memory (the A operand of PV, read MN-major) once PV of the previous tile is done
 // with those V rows, so the compressed rows are converted only once and leave the ring early.
 template <int kFmt>
-__device__ void dequant_loop(const DecodeParams& p, Smem* sm, uint8_t* ring, uint8_t* vtile,
+__device__ void dequant_loop(const DecodeParams& p, Smem* sm, uint8_t* ring, uint8_t* vtile, float* rowscale,
                              int64_t t_begin, int64_t t_end, int warp) {
   using F = RowFmt<kFmt>;
   const int lane = threadIdx.x & 31;
@@ -441,13 +446,32 @@ __device__ void dequant_loop(const DecodeParams& p, Smem* sm, uint8_t* ring, uin
       }
     }
     if (half == 1) {
-      convert_fp8_64(rowp + (kFmt == 0 ? kRopeOff : kLatent), r);   // the rope bytes are E4M3 in both formats
+      if constexpr (kFmt == 2) {
+        // bf16 rope / scale -> fp16 (exact for values in fp16's normal range)
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 v = *reinterpret_cast<const uint4*>(rowp + kTokRopeOff + 16 * c);
+          const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const __half2 h2 = __floats2half2_rn(__uint_as_float(w4[i] << 16), __uint_as_float(w4[i] & 0xFFFF0000u));
+            r[4 * c + i] = *reinterpret_cast<const uint32_t*>(&h2);
+          }
+        }
+      } else {
+        convert_fp8_64(rowp + (kFmt == 0 ? kRopeOff : kLatent), r);   // the rope bytes are E4M3 in both formats
+      }
       __syncwarp();
       tmem_st32(tmem_row + kTmemK + 256, r);
     }
     tmem_wait_st();
     tc_fence_before();
     __syncwarp();
+    if constexpr (kFmt == 2) {
+      // the row's scale, for the softmax (published with the row mask)
+      if (half == 0) rowscale[(k & 1) * kTileTokens + row] = *reinterpret_cast<const float*>(rowp + kTokScaleOff);
+      __syncwarp();
+    }
     if (lane == 0) {
       if (half == 0) {
         sm->vmask[k & 1][q] = mask;
@@ -689,9 +713,15 @@ __device__ __forceinline__ void load_scores(uint32_t taddr, bool valid, float qs
 // units of headroom, 2,047 tokens 17 units below a dominant one lost 1.5 % of the mass.)
 constexpr float kLazy = 15.f;
 // Returns false when the group gave up (abort); every thread of the group returns the same value.
-template <int NH, bool kCluster>
+// kFmt 2 (per-token FP8 rows, k = scale_t * k'): the score of row t is scale_t times the UMMA's
+// q . k'_t, and PV must weight v'_t by p_t * scale_t. The softmax keeps its reference on the shifted
+// exponent z_t + log2(scale_t), so P' = 2^(z_t + log2(scale_t) - m) = p_t * scale_t * 2^-m stays
+// inside fp16's range exactly as P does for the other formats, and the row sums add P' / scale_t.
+// O and the sums share the reference, so the quotient and the LSE (m + log2 of the sum) are
+// unchanged.
+template <int NH, bool kCluster, int kFmt = 0>
 __device__ bool softmax_loop(const DecodeParams& p, Smem* sm, uint8_t* ps, uint8_t* vtile, ClusterScratch* cs,
-                             int64_t t_begin, int64_t t_end, int64_t cta, float qscale) {
+                             const float* rowscale, int64_t t_begin, int64_t t_end, int64_t cta, float qscale) {
   constexpr uint32_t kPBytes = 128 * NH * 2;
   const int t = threadIdx.x - 384;          // 0..127: tile row / TMEM lane
   const int w = t >> 5, lane = t & 31;
@@ -723,7 +753,22 @@ __device__ bool softmax_loop(const DecodeParams& p, Smem* sm, uint8_t* ps, uint8
     __syncwarp();
     float z[32];
     const bool valid = (sm->vmask[k & 1][w] >> lane) & 1u;
-    load_scores<NH>(tmem_lane + s_col, valid, qscale, z);
+    float inv_rs = 1.f;   // kFmt 2: 1 / scale of this row (0 for an unusable row)
+    if constexpr (kFmt == 2) {
+      const float rs = rowscale[(k & 1) * kTileTokens + t];
+      const bool use = valid && rs > 0.f;
+      load_scores<NH>(tmem_lane + s_col, use, qscale * rs, z);
+      if (use) {
+        const float lrs = __log2f(rs);
+#pragma unroll
+        for (int h = 0; h < 32; ++h) z[h] += lrs;
+        inv_rs = 1.f / rs;
+      } else {
+        inv_rs = 0.f;
+      }
+    } else {
+      load_scores<NH>(tmem_lane + s_col, valid, qscale, z);
+    }
     // ---- lazy running max: vote whether any score exceeds max + kLazy (the first tile of a unit
     // always sets the max, so it skips the vote)
     bool raise = ti.first;
@@ -788,8 +833,13 @@ __device__ bool softmax_loop(const DecodeParams& p, Smem* sm, uint8_t* ps, uint8
         const float m0 = sm->m_used[h], m1 = sm->m_used[h + 1];
         const float p0 = (m0 == kNegInf) ? 0.f : ex2_approx(z[h] - m0);
         const float p1 = (m1 == kNegInf) ? 0.f : ex2_approx(z[h + 1] - m1);
-        l_part[h] += p0;
-        l_part[h + 1] += p1;
+        if constexpr (kFmt == 2) {
+          l_part[h] += p0 * inv_rs;
+          l_part[h + 1] += p1 * inv_rs;
+        } else {
+          l_part[h] += p0;
+          l_part[h + 1] += p1;
+        }
         const __half2 ph = __floats2half2_rn(p0, p1);
         const float2 fh = __half22float2(ph);
         const __half2 pl = __floats2half2_rn(p0 - fh.x, p1 - fh.y);
@@ -975,6 +1025,7 @@ __device__ void cluster_merge(const DecodeParams& p, ClusterScratch* sm, uint8_t
 template <int NH, bool kCluster, bool kPublish, int kFmt = 0>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ DecodeParams p) {
   static_assert(kFmt == 0 || !kCluster, "FP8 rows run on the split schedule only");
+  static_assert(kFmt == 0 || !kPublish, "FP8 rows write their results to device memory only");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* vtile = base;                                   // 131072
@@ -982,7 +1033,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   uint8_t* ps = qs + 9 * NH * 128;                         // 2 x 128 * NH * 2 (P, double-buffered)
   uint8_t* ring = ps + 2 * 128 * NH * 2;                   // RowFmt<kFmt>::kRingBytes
   static_assert(RowFmt<kFmt>::kRingBytes % 16 == 0, "control block must stay 16-byte aligned");
-  Smem* sm = reinterpret_cast<Smem*>(ring + RowFmt<kFmt>::kRingBytes);
+  float* rowscale = reinterpret_cast<float*>(ring + RowFmt<kFmt>::kRingBytes);   // kFmt 2 only
+  Smem* sm = reinterpret_cast<Smem*>(ring + RowFmt<kFmt>::kRingBytes + RowFmt<kFmt>::kScaleBytes);
 
   const int warp = threadIdx.x >> 5;
   const int64_t cta = blockIdx.x;
@@ -1051,10 +1103,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     if ((threadIdx.x & 31) == 0) mma_loop<NH, kCluster>(p, sm, vtile, qs, ps, t_begin, t_end, warp - 1);
     __syncwarp();
   } else if (warp >= 4 && warp < 12) {
-    dequant_loop<kFmt>(p, sm, ring, vtile, t_begin, t_end, warp);
+    dequant_loop<kFmt>(p, sm, ring, vtile, rowscale, t_begin, t_end, warp);
   } else if (warp >= 12) {
-    const bool ok = softmax_loop<NH, kCluster>(p, sm, ps, vtile, reinterpret_cast<ClusterScratch*>(ring), t_begin,
-                                               t_end, cta, qscale);
+    const bool ok = softmax_loop<NH, kCluster, kFmt>(p, sm, ps, vtile, reinterpret_cast<ClusterScratch*>(ring),
+                                                     rowscale, t_begin, t_end, cta, qscale);
     if constexpr (kPublish) {
       // Polling merge (results in host memory): publish this CTA's partials. Every writer fences
       // its stores at GPU scope, then one thread tags the CTA's slots, which the merge grid polls
@@ -1233,10 +1285,12 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeParams
 
 template <int NH, int kFmt = 0>
 constexpr size_t decode_smem_bytes() {
-  return 1024 + kVBytes + 9 * NH * 128 + 2 * 128 * NH * 2 + RowFmt<kFmt>::kRingBytes + sizeof(Smem);
+  return 1024 + kVBytes + 9 * NH * 128 + 2 * 128 * NH * 2 + RowFmt<kFmt>::kRingBytes + RowFmt<kFmt>::kScaleBytes +
+         sizeof(Smem);
 }
 static_assert(decode_smem_bytes<32>() <= 232448, "decode CTA exceeds the 227 KB shared-memory limit");
 static_assert(decode_smem_bytes<32, 1>() <= 232448, "FP8 decode CTA exceeds the 227 KB shared-memory limit");
+static_assert(decode_smem_bytes<32, 2>() <= 232448, "per-token FP8 decode CTA exceeds the 227 KB shared-memory limit");
 static_assert(sizeof(ClusterScratch) <= RowFmt<0>::kRingBytes, "cluster scratch lives in the ring");
 
 }  // namespace
@@ -1261,15 +1315,17 @@ static cudaError_t set_attributes() {
     const cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess && result == cudaSuccess) result = e;
   }
-  const void* big[8] = {(const void*)decode_kernel<32, false, false>,   (const void*)decode_kernel<32, false, true>,
-                        (const void*)decode_kernel<32, true, false>,    (const void*)decode_kernel<16, false, false>,
-                        (const void*)decode_kernel<16, false, true>,    (const void*)decode_kernel<16, true, false>,
-                        (const void*)decode_kernel<32, false, false, 1>, (const void*)decode_kernel<16, false, false, 1>};
-  const int bytes[8] = {(int)decode_smem_bytes<32>(),    (int)decode_smem_bytes<32>(), (int)decode_smem_bytes<32>(),
-                        (int)decode_smem_bytes<16>(),    (int)decode_smem_bytes<16>(), (int)decode_smem_bytes<16>(),
-                        (int)decode_smem_bytes<32, 1>(), (int)decode_smem_bytes<16, 1>()};
+  const void* big[10] = {(const void*)decode_kernel<32, false, false>,    (const void*)decode_kernel<32, false, true>,
+                         (const void*)decode_kernel<32, true, false>,     (const void*)decode_kernel<16, false, false>,
+                         (const void*)decode_kernel<16, false, true>,     (const void*)decode_kernel<16, true, false>,
+                         (const void*)decode_kernel<32, false, false, 1>, (const void*)decode_kernel<16, false, false, 1>,
+                         (const void*)decode_kernel<32, false, false, 2>, (const void*)decode_kernel<16, false, false, 2>};
+  const int bytes[10] = {(int)decode_smem_bytes<32>(),    (int)decode_smem_bytes<32>(), (int)decode_smem_bytes<32>(),
+                         (int)decode_smem_bytes<16>(),    (int)decode_smem_bytes<16>(), (int)decode_smem_bytes<16>(),
+                         (int)decode_smem_bytes<32, 1>(), (int)decode_smem_bytes<16, 1>(),
+                         (int)decode_smem_bytes<32, 2>(), (int)decode_smem_bytes<16, 2>()};
   static_assert(sizeof(big) / sizeof(big[0]) == sizeof(bytes) / sizeof(bytes[0]), "one size per decode instance");
-  for (int i = 0; i < 8; ++i) {
+  for (int i = 0; i < 10; ++i) {
     const cudaError_t e = cudaFuncSetAttribute(big[i], cudaFuncAttributeMaxDynamicSharedMemorySize, bytes[i]);
     if (e != cudaSuccess && result == cudaSuccess) result = e;
   }
@@ -1322,8 +1378,9 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream) {
   if (h32) q_prep_kernel<32><<<(unsigned)p.units, 256, 0, stream>>>(p);
   else q_prep_kernel<16><<<(unsigned)p.units, 256, 0, stream>>>(p);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  const size_t smem = p.row_fmt == 1 ? (h32 ? decode_smem_bytes<32, 1>() : decode_smem_bytes<16, 1>())
-                                     : (h32 ? decode_smem_bytes<32>() : decode_smem_bytes<16>());
+  const size_t smem = p.row_fmt == 1   ? (h32 ? decode_smem_bytes<32, 1>() : decode_smem_bytes<16, 1>())
+                     : p.row_fmt == 2 ? (h32 ? decode_smem_bytes<32, 2>() : decode_smem_bytes<16, 2>())
+                                      : (h32 ? decode_smem_bytes<32>() : decode_smem_bytes<16>());
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)p.ctas, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
@@ -1335,6 +1392,10 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream) {
   if (p.row_fmt == 1) {   // FP8 rows: results in device memory (the host checks)
     if (h32) return cudaLaunchKernelEx(&cfg, decode_kernel<32, false, false, 1>, p);
     return cudaLaunchKernelEx(&cfg, decode_kernel<16, false, false, 1>, p);
+  }
+  if (p.row_fmt == 2) {   // per-token FP8 rows: results in device memory (the host checks)
+    if (h32) return cudaLaunchKernelEx(&cfg, decode_kernel<32, false, false, 2>, p);
+    return cudaLaunchKernelEx(&cfg, decode_kernel<16, false, false, 2>, p);
   }
   if (p.merge_poll) {
     if (h32) return cudaLaunchKernelEx(&cfg, decode_kernel<32, false, true>, p);

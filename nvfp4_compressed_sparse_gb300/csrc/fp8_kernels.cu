@@ -1,4 +1,5 @@
-// Kernels of the FP8 comparison paths: the 576-byte FP8 row pack and the staged NVFP4 -> FP8 copy.
+// Kernels of the FP8 comparison paths: the 576-byte FP8 row pack, the per-token FP8 row pack and
+// the staged NVFP4 -> FP8 copy.
 //
 // What they compute ("Prime Inference: serving GLM-5.3 to agents is a KV-cache problem", sections
 // "Four bits per latent value: where 352 comes from" and "A kernel that reads four bits directly";
@@ -53,6 +54,56 @@ __global__ void __launch_bounds__(kFp8Warps * 32) fp8_pack_kernel(
     uint8_t* dst = cache + slot * kFp8RowBytes;
     __stcs(reinterpret_cast<uint4*>(dst) + lane, make_uint4(o[0], o[1], o[2], o[3]));
     __stcs(reinterpret_cast<unsigned short*>(dst + kLatent) + lane, (unsigned short)ptx::bf16x2_to_e4m3x2(r));
+  }
+}
+
+// bf16 rows -> per-token FP8 rows (672 bytes: E4M3 latent / scale, bf16 rope / scale, fp32 scale,
+// zero padding), the arithmetic of TokenSpeed's per-token write path: amax over the 512 latent
+// values, scale = max(amax, 1e-26) / 448, both divisions in IEEE fp32 (round to nearest even),
+// E4M3 (nearest even, saturating) and bf16 (nearest even) rounding. Lane l holds latent values
+// 16l..16l+15 and rope values 2l, 2l+1. Finite inputs (a NaN or an infinity gives an unspecified
+// row).
+__global__ void __launch_bounds__(kFp8Warps * 32) token_pack_kernel(
+    const uint16_t* __restrict__ latent, int64_t lstride, const uint16_t* __restrict__ rope, int64_t rstride,
+    const int64_t* __restrict__ slots, int64_t n, uint8_t* __restrict__ cache, int64_t num_pages,
+    int32_t* __restrict__ status) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nslots = num_pages * kPageTokens;
+  for (int64_t row = (int64_t)blockIdx.x * kFp8Warps + (threadIdx.x >> 5); row < n;
+       row += (int64_t)gridDim.x * kFp8Warps) {
+    const int64_t slot = __ldcs(slots + row);
+    const uint4* lp = reinterpret_cast<const uint4*>(latent + row * lstride) + 2 * lane;
+    const uint4 a = __ldcs(lp), b = __ldcs(lp + 1);
+    const uint32_t r = __ldcs(reinterpret_cast<const unsigned int*>(rope + row * rstride) + lane);
+    if (slot < 0 || slot >= nslots) {
+      if (slot != -1 && lane == 0 && status != nullptr) atomicAdd(status + 3, 1);
+      continue;
+    }
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    float x[16];
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      x[2 * i] = __uint_as_float(w[i] << 16);
+      x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+      amax = fmaxf(amax, fmaxf(fabsf(x[2 * i]), fabsf(x[2 * i + 1])));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float scale = __fdiv_rn(fmaxf(amax, 1e-26f), 448.0f);
+    uint32_t o4[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      o4[i] = ptx::f32x2_to_e4m3x2(__fdiv_rn(x[4 * i], scale), __fdiv_rn(x[4 * i + 1], scale)) |
+              (ptx::f32x2_to_e4m3x2(__fdiv_rn(x[4 * i + 2], scale), __fdiv_rn(x[4 * i + 3], scale)) << 16);
+    const __nv_bfloat162 rb = __floats2bfloat162_rn(__fdiv_rn(__uint_as_float(r << 16), scale),
+                                                    __fdiv_rn(__uint_as_float(r & 0xFFFF0000u), scale));
+    uint8_t* dst = cache + slot * kTokRowBytes;
+    __stcs(reinterpret_cast<uint4*>(dst) + lane, make_uint4(o4[0], o4[1], o4[2], o4[3]));
+    __stcs(reinterpret_cast<unsigned int*>(dst + kTokRopeOff) + lane, *reinterpret_cast<const unsigned int*>(&rb));
+    if (lane < 2)
+      __stcs(reinterpret_cast<uint4*>(dst + kTokScaleOff) + lane,
+             make_uint4(lane == 0 ? __float_as_uint(scale) : 0u, 0u, 0u, 0u));
   }
 }
 
@@ -163,6 +214,15 @@ cudaError_t launch_fp8_pack(const uint16_t* latent, int64_t lstride, const uint1
   const int grid = blocks_for(n, (const void*)fp8_pack_kernel);
   fp8_pack_kernel<<<grid, kFp8Warps * 32, 0, stream>>>(latent, lstride, rope, rstride, slots, n, cache, num_pages,
                                                        status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_token_pack(const uint16_t* latent, int64_t lstride, const uint16_t* rope, int64_t rstride,
+                              const int64_t* slots, int64_t n, uint8_t* cache, int64_t num_pages, int32_t* status,
+                              cudaStream_t stream) {
+  const int grid = blocks_for(n, (const void*)token_pack_kernel);
+  token_pack_kernel<<<grid, kFp8Warps * 32, 0, stream>>>(latent, lstride, rope, rstride, slots, n, cache,
+                                                         num_pages, status);
   return cudaGetLastError();
 }
 

@@ -12,6 +12,9 @@ constexpr int kRope = 64;
 constexpr int kQK = 576;
 constexpr int kRowBytes = 352;
 constexpr int kFp8RowBytes = 576;   // FP8 comparison rows: 512 latent + 64 rope E4M3 bytes
+constexpr int kTokRowBytes = 672;   // per-token FP8 rows: 512 E4M3 latent / scale, 64 bf16 rope / scale, fp32 scale, pad
+constexpr int kTokRopeOff = 512;
+constexpr int kTokScaleOff = 640;
 constexpr int kPageTokens = 64;
 constexpr int kScaleOff = 256;
 constexpr int kRopeOff = 288;
@@ -67,7 +70,8 @@ struct DecodeParams {
   int tiles_per_unit, ctas;
   int cluster;                // 0 = stream-K split, else CTAs per unit (one cluster per unit)
   uint32_t withhold;          // testing aid: 1 = the producers never publish tile 1's row table
-  int row_fmt;                // 0 = 352-byte NVFP4 rows, 1 = 576-byte FP8 rows (split schedule only)
+  int row_fmt;                // 0 = 352-byte NVFP4 rows, 1 = 576-byte FP8 rows, 2 = 672-byte per-token FP8 rows
+                              // (1 and 2: split schedule only)
 };
 
 cudaError_t launch_pack(const uint16_t* latent, int64_t lstride, const uint16_t* rope, int64_t rstride,
@@ -76,6 +80,9 @@ cudaError_t launch_pack(const uint16_t* latent, int64_t lstride, const uint16_t*
 cudaError_t launch_fp8_pack(const uint16_t* latent, int64_t lstride, const uint16_t* rope, int64_t rstride,
                             const int64_t* slots, int64_t n, uint8_t* cache, int64_t num_pages, int32_t* status,
                             cudaStream_t stream);
+cudaError_t launch_token_pack(const uint16_t* latent, int64_t lstride, const uint16_t* rope, int64_t rstride,
+                              const int64_t* slots, int64_t n, uint8_t* cache, int64_t num_pages, int32_t* status,
+                              cudaStream_t stream);
 cudaError_t launch_stage(const uint8_t* cache, int64_t num_pages, const int32_t* page_table, int64_t max_pages,
                          const int32_t* idx, const int32_t* seq_lens, int B, int Q, int K, uint8_t* staged,
                          int32_t* staged_idx, int32_t* staged_pt, int32_t* staged_sl, int32_t* status,

@@ -39,7 +39,7 @@ def assert_close(out, lse, ref_out, ref_lse, what=""):
 def oracle_units_from_device_rows(case, units, lat_dev, rope_dev, fmt="nvfp4"):
     """Oracle outputs for (b, j) units, encoding the selected rows from their bf16
     inputs (gathered from the device input tensors by physical slot) in the cache format
-    fmt ("nvfp4", "fp8" or "staged"). The CPU work runs in a pool of spawned worker
+    fmt ("nvfp4", "fp8", "staged" or "token"). The CPU work runs in a pool of spawned worker
     processes."""
     from tests import oracle_pool
     keys, jobs = [], []

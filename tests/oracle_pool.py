@@ -14,13 +14,16 @@ from oracle import attention, codec, fp8rows, pack
 
 def _rows_values(lat_bits, rope_bits, fmt):
     """Dequantised selected rows of a unit in the cache format fmt: "nvfp4" (the 352-byte rows),
-    "fp8" (576-byte FP8 rows packed from bf16) or "staged" (FP8 copies of the NVFP4 rows)."""
+    "fp8" (576-byte FP8 rows packed from bf16), "staged" (FP8 copies of the NVFP4 rows) or "token"
+    (672-byte per-token FP8 rows)."""
     if fmt == "nvfp4":
         return attention.dequant_rows(pack.encode_rows(lat_bits, rope_bits))
     if fmt == "fp8":
         return fp8rows.dequant_rows_fp8(fp8rows.encode_rows_fp8(lat_bits, rope_bits))
     if fmt == "staged":
         return fp8rows.dequant_rows_fp8(fp8rows.stage_rows(pack.encode_rows(lat_bits, rope_bits)))
+    if fmt == "token":
+        return fp8rows.dequant_rows_token(fp8rows.encode_rows_token(lat_bits, rope_bits))
     raise ValueError(fmt)
 
 

@@ -1,6 +1,6 @@
-"""The FP8 comparison paths on the GPU against the oracle: the FP8 row pack and the staging
-kernel bit-exact, the FP8 decode and the staged path within the decode tolerance (the reference
-is fp64 attention over the same FP8 rows)."""
+"""The FP8 comparison paths on the GPU against the oracle: the FP8 and per-token FP8 row packs and
+the staging kernel bit-exact, the FP8 decodes and the staged path within the decode tolerance (the
+reference is fp64 attention over the same rows)."""
 import numpy as np
 import pytest
 import torch
@@ -115,7 +115,44 @@ def test_staged_path_matches_oracle(spec):
     assert_close(out, lse, ref_out.reshape(out.shape), ref_lse.reshape(lse.shape), f"staged {spec}")
 
 
-@pytest.mark.parametrize("path", ["fp8", "staged"])
+def test_token_pack_bit_exact_with_slot_rules():
+    lat, rope = _bf16_rows(700, 2)
+    lat[5] = 0                                          # an all-zero latent: the scale comes from the 1e-26 floor
+    pages = 12
+    slots = np.arange(700, dtype=np.int64)
+    slots[9] = -1
+    slots[10] = pages * 64 + 7
+    cache = torch.full((pages, 64, 672), 0xAB, dtype=torch.uint8, device="cuda")
+    status = torch.zeros(4, dtype=torch.int32, device="cuda")
+    m.fp8_token_kv_pack(bf16_dev(lat), bf16_dev(rope), torch.from_numpy(slots).cuda(), cache, dev_status=status)
+    torch.cuda.synchronize()
+    ref = np.full((pages, 64, 672), 0xAB, np.uint8)
+    fp8rows.write_cache_token(ref, lat, rope, slots)
+    np.testing.assert_array_equal(cache.cpu().numpy(), ref)
+    assert status.cpu().tolist() == [0, 0, 0, 1]
+
+
+@pytest.mark.parametrize("spec", SMALL, ids=lambda s: "B{B}Q{Q}H{H}K{topk}".format(**s))
+def test_token_decode_matches_oracle(spec):
+    case = workloads.small_case(seed=80 + len(str(spec)), **spec)
+    lat, rope = workloads.host_rows(case, np.arange(case.num_pages))
+    n = case.num_pages * 64
+    cache = torch.zeros((case.num_pages, 64, 672), dtype=torch.uint8, device="cuda")
+    m.fp8_token_kv_pack(bf16_dev(lat), bf16_dev(rope), torch.arange(n, device="cuda"), cache)
+    q, pt, tk, sl = decode_inputs(case)
+    status = torch.zeros(4, dtype=torch.int32, device="cuda")
+    out, lse = m.sparse_mla_decode_fp8_token(q, cache, pt, tk, sl, case.softmax_scale, dev_status=status)
+    torch.cuda.synchronize()
+    ref_cache = np.zeros((case.num_pages, 64, 672), np.uint8)
+    fp8rows.write_cache_token(ref_cache, lat, rope, np.arange(n))
+    np.testing.assert_array_equal(cache.cpu().numpy(), ref_cache)
+    ref_out, ref_lse = fp8rows.sparse_decode_token(case.q_bits, ref_cache, case.page_table, case.topk_indices,
+                                                   case.seq_lens, case.softmax_scale)
+    assert_close(out, lse, ref_out, ref_lse, f"per-token {spec}")
+    assert status.cpu().tolist()[2] == 0
+
+
+@pytest.mark.parametrize("path", ["fp8", "staged", "token"])
 def test_headline_size_sampled_units(path):
     """The 64-query headline workload through either comparison path, with the launch
     configuration the bench times; 8 query tokens checked against the oracle on their own rows."""
@@ -128,6 +165,10 @@ def test_headline_size_sampled_units(path):
         cache = torch.empty((case.num_pages, 64, 576), dtype=torch.uint8, device="cuda")
         m.fp8_kv_pack(lat, rope, torch.arange(n, device="cuda"), cache)
         out, lse = m.sparse_mla_decode_fp8(q, cache, pt, tk, sl, case.softmax_scale, dev_status=status)
+    elif path == "token":
+        cache = torch.empty((case.num_pages, 64, 672), dtype=torch.uint8, device="cuda")
+        m.fp8_token_kv_pack(lat, rope, torch.arange(n, device="cuda"), cache)
+        out, lse = m.sparse_mla_decode_fp8_token(q, cache, pt, tk, sl, case.softmax_scale, dev_status=status)
     else:
         cache = torch.empty((case.num_pages, 64, 352), dtype=torch.uint8, device="cuda")
         m.mla_kv_pack(lat, rope, torch.arange(n, device="cuda"), cache)

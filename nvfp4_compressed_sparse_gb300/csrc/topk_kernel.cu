@@ -31,6 +31,7 @@
 #include <mutex>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace nvfp4mla {
 namespace {
@@ -102,7 +103,9 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* w
 }
 
 struct TopkShared {
-  uint32_t hist[4096];
+  alignas(16) uint32_t hist[4096];
+  alignas(16) uint32_t mhist[4096];            // cluster: the first tier's sample histogram summed over the CTAs
+  uint32_t m_local;                // cluster: this CTA's sample size
   uint32_t warp_sums[32];
   uint32_t found_digit, found_rem, cand_count;
   uint32_t cand_key[kTkCandCap];
@@ -116,20 +119,20 @@ __device__ __forceinline__ uint32_t* eq_map(TopkShared& sh) { return sh.eq_map_;
 
 // The digit of the rem-th largest key from a filled histogram (bins scanned from the top):
 // updates prefix/pmask with the digit at `shift` and rem with the rank left inside its bin.
-__device__ __forceinline__ void take_digit(TopkShared& sh, int bins, int shift, uint32_t& prefix, uint32_t& pmask,
-                                           uint32_t& rem) {
+__device__ __forceinline__ void take_digit(TopkShared& sh, const uint32_t* hist, int bins, int shift,
+                                           uint32_t& prefix, uint32_t& pmask, uint32_t& rem) {
   const int t = threadIdx.x;
   const int per = bins / kTkThreads > 0 ? bins / kTkThreads : 1;
   const int hi = bins - per * t;          // this thread owns bins [hi - per, hi)
   uint32_t mine = 0;
   if (hi > 0)
-    for (int i = 1; i <= per; ++i) mine += sh.hist[hi - i];
+    for (int i = 1; i <= per; ++i) mine += hist[hi - i];
   uint32_t total;
   const uint32_t above = block_exclusive_scan(mine, sh.warp_sums, &total);   // counts in higher bins
   if (hi > 0 && above < rem && above + mine >= rem) {
     uint32_t cum = above;
     for (int i = 1; i <= per; ++i) {
-      const uint32_t h = sh.hist[hi - i];
+      const uint32_t h = hist[hi - i];
       if (cum + h >= rem) {
         sh.found_digit = (uint32_t)(hi - i);
         sh.found_rem = rem - cum;
@@ -270,6 +273,17 @@ __device__ __forceinline__ void candidate_sweep(TopkShared& sh, const float* row
   }
 }
 
+// Histogram add for a warp whose lanes may hit the same bin (candidate keys crowd into a few
+// bins): lanes with equal bins are grouped and one of them adds the group's count. Called by all
+// 32 lanes.
+__device__ __forceinline__ void hist_add_grouped(uint32_t* hist, uint32_t bin, bool active) {
+  const uint32_t act = __ballot_sync(0xffffffffu, active);
+  if (active) {
+    const uint32_t peers = __match_any_sync(act, bin);
+    if ((int)(__ffs(peers) - 1) == (int)(threadIdx.x & 31)) atomicAdd(&hist[bin], (uint32_t)__popc(peers));
+  }
+}
+
 // The rest of the select over the c candidates in shared memory, which hold every key of the
 // row that can still be selected: the digits from d_start on (0: bits 31..20, 1: 19..8, 2: 7..0)
 // of the threshold key T and the count R of ties taken, then the bitmaps and the list.
@@ -282,12 +296,13 @@ __device__ void finish_from_candidates(TopkShared& sh, uint32_t c, int d_start, 
     const int shift = d == 0 ? 20 : (d == 1 ? 8 : 0), bins = d < 2 ? 4096 : 256;
     for (int i = t; i < bins; i += kTkThreads) sh.hist[i] = 0;
     __syncthreads();
-    for (uint32_t i = t; i < c; i += kTkThreads) {
-      const uint32_t k = sh.cand_key[i];
-      if ((k & pmask) == prefix) atomicAdd(&sh.hist[(k >> shift) & (uint32_t)(bins - 1)], 1u);
+    for (uint32_t base = (uint32_t)(t & ~31); base < c; base += kTkThreads) {   // warp-uniform trip count
+      const uint32_t i = base + (uint32_t)(t & 31);
+      const uint32_t k = i < c ? sh.cand_key[i] : 0u;
+      hist_add_grouped(sh.hist, (k >> shift) & (uint32_t)(bins - 1), i < c && (k & pmask) == prefix);
     }
     __syncthreads();
-    take_digit(sh, bins, shift, prefix, pmask, rem);
+    take_digit(sh, sh.hist, bins, shift, prefix, pmask, rem);
   }
   const uint32_t T = prefix, R = rem;
   if (clear_maps) {
@@ -336,15 +351,31 @@ __device__ void finish_from_candidates(TopkShared& sh, uint32_t c, int d_start, 
 // in shared memory. The bound is chosen so that about 1.5 K keys of the row are expected above
 // it; it is checked exactly (at least K candidates, at most the store's capacity), and on a miss
 // the caller takes the next tier. Returns true when the list is written (block-uniform).
-__device__ bool sample_select(TopkShared& sh, const float* row, int64_t n, int K, int32_t* o) {
+//
+// kCluster: the C CTAs of a thread-block cluster share the row; CTA r samples and sweeps the r-th
+// slice (a multiple of 8 positions). The sample histograms and sizes are summed through distributed
+// shared memory (every CTA computes the same bound from the sum), each CTA keeps its slice's
+// candidates, and the CTAs then append theirs to CTA 0's store, which finishes the select. Every
+// decision is taken on cluster-wide values, so all CTAs return the same value; on a miss CTA 0
+// alone takes the next tiers.
+template <bool kCluster>
+__device__ bool sample_select(TopkShared& sh, const float* row, int64_t n, int K, int32_t* o, uint32_t rank,
+                              uint32_t csize) {
+  namespace px = nvfp4mla::ptx;
   const int t = threadIdx.x;
+  int64_t lo_r = 0, hi_r = n;
+  if constexpr (kCluster) {
+    const int64_t per = ((n + csize - 1) / csize + 7) & ~(int64_t)7;
+    lo_r = min(n, (int64_t)rank * per);
+    hi_r = min(n, lo_r + per);
+  }
   for (int i = t; i < 4096; i += kTkThreads) sh.hist[i] = 0;
   if (t == 0) sh.cand_count = 0;
   __syncthreads();
   uint32_t mine = 0;
-  for (int64_t p0 = (int64_t)t * 128; p0 < n; p0 += (int64_t)kTkThreads * 128) {
+  for (int64_t p0 = lo_r + (int64_t)t * 128; p0 < hi_r; p0 += (int64_t)kTkThreads * 128) {
     uint32_t k[kTkPer];
-    const uint32_t v = load_keys<false>(row, p0, n, k);
+    const uint32_t v = load_keys<false>(row, p0, hi_r, k);
 #pragma unroll
     for (int i = 0; i < kTkPer; ++i)
       if ((v >> i) & 1u) atomicAdd(&sh.hist[k[i] >> 20], 1u);
@@ -353,20 +384,43 @@ __device__ bool sample_select(TopkShared& sh, const float* row, int64_t n, int K
   __syncthreads();
   uint32_t m;
   block_exclusive_scan(mine, sh.warp_sums, &m);
+  const uint32_t* hist = sh.hist;
+  if constexpr (kCluster) {
+    if (t == 0) sh.m_local = m;
+    px::cluster_sync_all();                        // every CTA's sample histogram and size are final
+    // thread t sums bins 4t..4t+3 of every CTA (one 16-byte load per CTA, all issued before use)
+    static_assert(4096 == 4 * kTkThreads, "one group of four bins per thread");
+    const uint32_t hbase = px::smem_u32(sh.hist) + 16 * t, mbase = px::smem_u32(&sh.m_local);
+    uint4 part[8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+      part[r] = r < (int)csize ? px::ld_dsmem_u4(px::map_shared_rank(hbase, r)) : make_uint4(0u, 0u, 0u, 0u);
+    uint4 sum = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int r = 0; r < 8; ++r) sum.x += part[r].x, sum.y += part[r].y, sum.z += part[r].z, sum.w += part[r].w;
+    *reinterpret_cast<uint4*>(&sh.mhist[4 * t]) = sum;
+    m = 0;
+    for (uint32_t r = 0; r < csize; ++r) m += px::ld_dsmem_u32(px::map_shared_rank(mbase, r));
+    __syncthreads();
+    hist = sh.mhist;
+  }
   // rank (from the top) in the sample of the bound: ceil(1.5 K m / n) + 32
   const int64_t want = (3 * (int64_t)K * m + 2 * n - 1) / (2 * n) + 32;
-  if (want > (int64_t)m) return false;
-  uint32_t prefix = 0, pmask = 0, rem = (uint32_t)want;
-  take_digit(sh, 4096, 20, prefix, pmask, rem);
-  const uint32_t db = prefix >> 20;
-  if (db < 8 || db > 0xFF8) return false;   // the bound would not be a number
+  uint32_t db = 0;
+  if (want <= (int64_t)m) {
+    uint32_t prefix = 0, pmask = 0, rem = (uint32_t)want;
+    take_digit(sh, hist, 4096, 20, prefix, pmask, rem);
+    db = prefix >> 20;
+  }
+  if constexpr (kCluster) px::cluster_sync_all();   // no CTA reads another's histogram after this
+  if (db < 8 || db > 0xFF8) return false;   // no usable bound (it would not be a number)
   const uint32_t lo = db << 20;
   const float f_lo = __uint_as_float(lo >= 0x80000000u ? (lo & 0x7FFFFFFFu) : ~lo);
 
   // the sweep: every key >= lo becomes a candidate (f_lo passes a superset, see candidate_sweep)
-  int64_t base = 0;
+  int64_t base = lo_r;
 #pragma unroll 1
-  for (; base + 4 * kTkGroup <= n; base += 4 * kTkGroup) {
+  for (; base + 4 * kTkGroup <= hi_r; base += 4 * kTkGroup) {
     float4 a[4], c[4];
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
@@ -391,28 +445,58 @@ __device__ bool sample_select(TopkShared& sh, const float* row, int64_t n, int K
     }
   }
 #pragma unroll 1
-  for (; base < n; base += kTkGroup) {
+  for (; base < hi_r; base += kTkGroup) {
     uint32_t k[kTkPer], bits = 0;
     const int64_t p0 = base + (int64_t)t * kTkPer;
-    const uint32_t v = load_keys(row, p0, n, k);
+    const uint32_t v = load_keys(row, p0, hi_r, k);
 #pragma unroll
     for (int i = 0; i < kTkPer; ++i)
       if (((v >> i) & 1u) && k[i] >= lo) bits |= 1u << i;
     append_candidates(sh, bits, k, (int32_t)p0);
   }
   __syncthreads();
-  const uint32_t c = sh.cand_count;
+  uint32_t c = sh.cand_count;
+  if constexpr (kCluster) {
+    // cluster-wide count and this CTA's offset in CTA 0's store
+    px::cluster_sync_all();                        // every CTA's count is final
+    const uint32_t cbase = px::smem_u32(&sh.cand_count);
+    uint32_t total = 0, off = 0;
+    bool over = false;
+    for (uint32_t r = 0; r < csize; ++r) {
+      const uint32_t cr = px::ld_dsmem_u32(px::map_shared_rank(cbase, r));
+      over |= cr > (uint32_t)kTkCandCap;
+      if (r < rank) off += cr;
+      total += cr;
+    }
+    px::cluster_sync_all();                        // every count has been read
+    if (over || total < (uint32_t)K || total > (uint32_t)kTkCandCap) return false;
+    if (rank != 0) {
+      const uint32_t kb = px::map_shared_rank(px::smem_u32(sh.cand_key), 0);
+      const uint32_t pb = px::map_shared_rank(px::smem_u32(sh.cand_pos), 0);
+      for (uint32_t i = t; i < c; i += kTkThreads) {
+        px::st_dsmem_u32(kb + 4 * (off + i), sh.cand_key[i]);
+        px::st_dsmem_u32(pb + 4 * (off + i), (uint32_t)sh.cand_pos[i]);
+      }
+    }
+    px::cluster_sync_all();                        // CTA 0 holds every candidate
+    if (rank != 0) return true;
+    c = total;
+  }
   if (c < (uint32_t)K || c > (uint32_t)kTkCandCap) return false;
   finish_from_candidates(sh, c, 0, 0u, 0u, (uint32_t)K, (int)((n + 31) >> 5), true, o);
   return true;
 }
 
+// kCluster: launched with clusters of C CTAs, cluster c selecting row c (see sample_select); the
+// tiers after the first run in CTA 0 of the cluster alone.
+template <bool kCluster>
 __global__ void __launch_bounds__(kTkThreads, 1) topk_kernel(const float* __restrict__ logits, int64_t stride,
                                                              const int32_t* __restrict__ seq_lens, int Q, int K,
-                                                             int32_t* __restrict__ out) {
+                                                             int32_t* __restrict__ out, int csize) {
   extern __shared__ __align__(16) unsigned char topk_smem[];
   TopkShared& sh = *reinterpret_cast<TopkShared*>(topk_smem);
-  const int64_t rowi = blockIdx.x;
+  const uint32_t rank = kCluster ? nvfp4mla::ptx::cluster_ctarank() : 0u;
+  const int64_t rowi = kCluster ? (int64_t)blockIdx.x / csize : (int64_t)blockIdx.x;
   const int b = (int)(rowi / Q), j = (int)(rowi - (int64_t)b * Q);
   int64_t n = (int64_t)__ldg(seq_lens + b) - Q + j + 1;
   if (n < 0) n = 0;
@@ -420,20 +504,22 @@ __global__ void __launch_bounds__(kTkThreads, 1) topk_kernel(const float* __rest
   int32_t* o = out + rowi * K;
   const int t = threadIdx.x;
   if (n <= K) {   // the whole range is selected
-    for (int i = t; i < K; i += kTkThreads) o[i] = i < n ? i : -1;
+    if (rank == 0)
+      for (int i = t; i < K; i += kTkThreads) o[i] = i < n ? i : -1;
     return;
   }
   const float* row = logits + rowi * stride;
 
   const bool maps_fit = n <= 32 * (int64_t)kTkMapWords;
-  if (maps_fit && 2 * K <= kTkCandCap && sample_select(sh, row, n, K, o)) return;
+  if (maps_fit && 2 * K <= kTkCandCap && sample_select<kCluster>(sh, row, n, K, o, rank, (uint32_t)csize)) return;
+  if (rank != 0) return;
   __syncthreads();
 
   // ---- second tier: the top 12 bits of the K-th largest key, over the whole row
   uint32_t prefix = 0, pmask = 0;
   uint32_t rem = (uint32_t)K;   // rank (from the top) of the wanted key among those matching prefix
   global_histogram<false>(sh, row, n, 20, 4096, 0u, 0u);
-  take_digit(sh, 4096, 20, prefix, pmask, rem);
+  take_digit(sh, sh.hist, 4096, 20, prefix, pmask, rem);
 
   if (maps_fit) {
     // one more sweep marks the keys above that digit in a position bitmap and
@@ -462,7 +548,7 @@ __global__ void __launch_bounds__(kTkThreads, 1) topk_kernel(const float* __rest
   for (int d = 1; d < 3; ++d) {
     const int shift = d == 1 ? 8 : 0, bins = d == 1 ? 4096 : 256;
     global_histogram<true>(sh, row, n, shift, bins, prefix, pmask);
-    take_digit(sh, bins, shift, prefix, pmask, rem);
+    take_digit(sh, sh.hist, bins, shift, prefix, pmask, rem);
   }
   const uint32_t T = prefix;      // the K-th largest key
   const uint32_t R = rem;         // keys equal to T that are taken (the first R in position order)
@@ -515,14 +601,39 @@ cudaError_t launch_topk(const float* logits, int64_t stride, const int32_t* seq_
   {
     std::lock_guard<std::mutex> lock(mu);
     if (dev < 0 || dev >= kMaxDevices || !done[dev]) {
-      err = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(TopkShared));
+      err = cudaFuncSetAttribute(topk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)sizeof(TopkShared));
+      if (err == cudaSuccess)
+        err = cudaFuncSetAttribute(topk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)sizeof(TopkShared));
       if (err != cudaSuccess) return err;
       if (dev >= 0 && dev < kMaxDevices) done[dev] = true;
     }
   }
-  topk_kernel<<<(unsigned)((int64_t)B * Q), kTkThreads, sizeof(TopkShared), stream>>>(logits, stride, seq_lens, Q, K,
-                                                                                       out);
-  return cudaGetLastError();
+  // Rows that leave SMs idle are split over a cluster of C CTAs (C <= 8, the portable cluster size):
+  // C = the SMs per row, so one wave of clusters covers the batch.
+  const int64_t rows = (int64_t)B * Q;
+  const int sms = device_sm_count();
+  int64_t c = sms > 0 ? sms / rows : 1;
+  if (c > 8) c = 8;
+  if (c < 2) {
+    topk_kernel<false><<<(unsigned)rows, kTkThreads, sizeof(TopkShared), stream>>>(logits, stride, seq_lens, Q, K, out,
+                                                                                   1);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(rows * c), 1, 1);
+  cfg.blockDim = dim3(kTkThreads, 1, 1);
+  cfg.dynamicSmemBytes = sizeof(TopkShared);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)c;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, topk_kernel<true>, logits, stride, seq_lens, Q, K, out, (int)c);
 }
 
 }  // namespace nvfp4mla

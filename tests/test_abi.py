@@ -28,7 +28,9 @@ def lib():
 def test_exports_every_declared_symbol(lib):
     names = _declared_functions()
     assert set(names) >= {"mla_kv_pack", "sparse_mla_decode", "sparse_mla_decode_workspace_size",
-                          "nvfp4mla_status_string"}
+                          "sparse_mla_decode_plan", "sparse_mla_decode_noalloc", "indexer_topk", "fp8_kv_pack",
+                          "nvfp4_stage_fp8", "sparse_mla_decode_fp8", "fp8_token_kv_pack",
+                          "sparse_mla_decode_fp8_token", "nvfp4mla_status_string"}
     for n in names:
         assert hasattr(lib, n), n
 
@@ -111,3 +113,34 @@ def test_decode_host_checks(lib):
     for kw in [dict(q=A + 8), dict(cache=A + 4), dict(out=A + 2), dict(pt=A + 2), dict(idx=A + 1), dict(sl=A + 2),
                dict(lse=A + 2)]:
         assert _dec(lib, **kw) == 2, kw
+
+
+def test_comparison_path_host_checks(lib):
+    """The FP8 packs, the staging, the FP8 decodes and top-k reject bad sizes, NULLs, misalignment
+    and host memory before any launch (these calls never reach a kernel here)."""
+    import numpy as np
+    A = 1 << 20
+    for entry in (lib.fp8_kv_pack, lib.fp8_token_kv_pack):
+        assert entry(V(A), 512, V(A), 64, V(A), 4, V(A), 0, None, None) == 1          # no pages
+        assert entry(V(A), 511, V(A), 64, V(A), 4, V(A), 1, None, None) == 1          # row stride too small
+        assert entry(V(A + 8), 512, V(A), 64, V(A), 4, V(A), 1, None, None) == 2      # latent not 16-byte aligned
+        assert entry(None, 512, V(A), 64, V(A), 4, V(A), 1, None, None) == 1
+        lat, rope = np.zeros((4, 512), np.uint16), np.zeros((4, 64), np.uint16)
+        slots, cache = np.arange(4, dtype=np.int64), np.full((1, 64, 672), 0xAB, np.uint8)
+        Pn = lambda a: V(a.ctypes.data)
+        assert entry(Pn(lat), 512, Pn(rope), 64, Pn(slots), 4, Pn(cache), 1, None, None) == 1   # host memory
+        assert (cache == 0xAB).all()
+    st = lambda **kw: lib.nvfp4_stage_fp8(V(kw.get("cache", A)), 10, V(A), 4, V(A), V(A), kw.get("B", 1), 1,
+                                          kw.get("K", 128), V(kw.get("staged", A)), V(A), V(A), V(A), None, None)
+    assert st(K=100) == 1                                                              # not a multiple of 64
+    assert st(K=0) == 1 and st(B=0) == 1
+    assert st(staged=A + 4) == 2
+    for entry in (lib.sparse_mla_decode_fp8, lib.sparse_mla_decode_fp8_token):
+        assert entry(V(A), V(A), 10, V(A), 4, V(A), V(A), 1, 1, 32, 0, ctypes.c_float(0.07), V(A), V(A), V(A),
+                     1 << 30, None, None) == 1                                         # topk 0
+        assert entry(V(A), V(A), 10, V(A), 4, V(A), V(A), 1, 1, 48, 128, ctypes.c_float(0.07), V(A), V(A), V(A),
+                     1 << 30, None, None) == 1                                         # H not supported
+    tk = lambda **kw: lib.indexer_topk(V(kw.get("lg", A)), kw.get("S", 64), V(A), kw.get("B", 1), kw.get("Q", 1),
+                                       kw.get("K", 8), V(A), None)
+    assert tk(B=0) == 1 and tk(Q=17) == 1 and tk(K=0) == 1 and tk(K=9000) == 1 and tk(S=0) == 1
+    assert tk(S=62) == 2 and tk(lg=A + 4) == 2

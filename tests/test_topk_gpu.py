@@ -38,6 +38,19 @@ def test_random_rows_with_ties_nan_and_signed_zero(B, Q, S, K):
     np.testing.assert_array_equal(_run(logits, L, Q, K), topk.select(logits, L, Q, K))
 
 
+@pytest.mark.parametrize("B,Q", [(20, 1), (40, 1), (100, 2)], ids=["7-CTA clusters", "3-CTA clusters", "one CTA per row"])
+def test_row_counts_that_change_the_launch(B, Q):
+    """The launch splits a row over SMs // rows CTAs (2..8) when the batch leaves SMs idle and uses
+    one CTA per row otherwise: 20 and 40 rows give clusters of 7 and 3 CTAs on 152 SMs, 200 rows
+    one CTA each. Rows of uneven length and ties in one request."""
+    rng = np.random.default_rng(B * 7 + Q)
+    S, K = 9000, 700
+    logits = rng.standard_normal((B, Q, S)).astype(np.float32)
+    logits[1] = np.round(logits[1] * 2) / 2
+    L = rng.integers(500, S + Q, size=B).astype(np.int32)
+    np.testing.assert_array_equal(_run(logits, L, Q, K), topk.select(logits, L, Q, K))
+
+
 @pytest.mark.parametrize("S", [5000, 20000])      # 20,000 equal keys overflow the candidate store
 def test_degenerate_rows(S):
     K = 2048

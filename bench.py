@@ -438,6 +438,55 @@ def fp8_table(m, workloads, case, cache, dev, stream, flush, hbm, steps, native_
     }
 
 
+def fold_table(m, workloads, dev, stream, flush, steps):
+    """Query tokens folded over a shared index list (sparse_mla_decode_shared) against one pass per
+    query token (sparse_mla_decode) on the same inputs: the spec-verify requests (B=32, contexts
+    100K-156K) with 16 heads and Q = 2 or 4 draft tokens, each keeping 90 % of a shared set of 2,048
+    positions. Device µs per step, L2 flushed before each step."""
+    import torch
+    base = workloads.make_case(3)
+    cache, _, _ = fill_cache(m, workloads, base, dev)
+    pt, sl = torch.from_numpy(base.page_table).to(dev), torch.from_numpy(base.seq_lens).to(dev)
+    res = []
+    for Q in (2, 4):
+        rng = np.random.default_rng(4040 + Q)
+        H, K = 16, base.topk
+        qb = np.ascontiguousarray(base.q_bits[:, :Q, :H])
+        q = torch.from_numpy(qb.view(np.int16)).to(dev).view(torch.bfloat16)
+        lists = np.stack([workloads.subset_lists(rng, int(base.seq_lens[b]), Q, K, 0.9) for b in range(base.B)])
+        shared, member = workloads.fold_lists(lists)
+        tk = torch.from_numpy(lists.astype(np.int32)).to(dev)
+        sh, mem = torch.from_numpy(shared).to(dev), torch.from_numpy(member).to(dev)
+        out = torch.empty((base.B, Q, H, 512), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((base.B, Q, H), dtype=torch.float32, device=dev)
+        ws = torch.empty(max(m.sparse_mla_decode_workspace_size(base.B, Q, H, K),
+                             m.sparse_mla_decode_workspace_size(base.B, 1, Q * H, shared.shape[1])),
+                         dtype=torch.uint8, device=dev)
+        times = {}
+        for name, fn in (("per_token_us", lambda: m.sparse_mla_decode(q, cache, pt, tk, sl, base.softmax_scale,
+                                                                        out=out, lse=lse, workspace=ws, stream=stream)),
+                         ("folded_us", lambda: m.sparse_mla_decode_shared(q, cache, pt, sh, mem, sl,
+                                                                          base.softmax_scale, out=out, lse=lse,
+                                                                          workspace=ws, stream=stream))):
+            ev = []
+            for i in range(5 + steps):
+                flush.zero_()
+                e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+                e[0].record(stream)
+                fn()
+                e[1].record(stream)
+                if i >= 5:
+                    ev.append(e)
+            torch.cuda.synchronize(dev)
+            times[name] = statistics.fmean(a.elapsed_time(b) for a, b in ev) * 1e3
+        res.append({"B": base.B, "Q": Q, "H": H, "list_entries_per_token": int(round(0.9 * K)),
+                    "shared_list_len": int(shared.shape[1]), "heads_per_pass": min(32, Q * H), **times,
+                    "speedup": times["per_token_us"] / times["folded_us"]})
+    del cache
+    torch.cuda.empty_cache()
+    return res
+
+
 def topk_table(m, case, cache, dev, stream, flush, hbm, steps):
     """indexer_topk on the headline case's query tokens (seeded N(0,1) fp32 logits over each causal
     range), alone and followed by sparse_mla_decode on the same stream. Algorithmic bytes: every
@@ -637,6 +686,7 @@ def run_gpu(args, world, rank, local):
         del cache, hq, hpt, htk, hsl, hout, hlse, ws
         torch.cuda.empty_cache()
         result["configs"] = extra_configs(m, workloads, dev, stream, flush, hbm, min(K, 200))
+        result["fold"] = fold_table(m, workloads, dev, stream, flush, min(K, 200))
     if rank == 0 and world == 1 and not args.no_cpu_baseline and case_id == 2:
         result["cpu_baseline"] = cpu_baseline(case)
     return result

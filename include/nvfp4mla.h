@@ -291,6 +291,39 @@ int indexer_topk(const float* logits, int64_t logits_row_stride, const int32_t* 
                  int32_t* topk_indices, void* stream);
 
 /*
+ * sparse_mla_decode_shared: one decode step for the Q query tokens of each
+ * request (speculative verify: draft tokens) folded into one pass over a
+ * shared index list ("TokenSpeed" walkthrough, MLA decode section: fold_sq
+ * folds the query-token axis into the head axis). Each cached row the request
+ * selects is gathered and unpacked once and scored for the Q * H (query, head)
+ * columns together, instead of once per query token.
+ *   shared_indices    int32 [B, topk]: the request's positions (any order, -1
+ *                     unused), the union of its query tokens' lists
+ *   member_masks      uint8 [B, topk] device memory: bit j set when entry e
+ *                     belongs to query token j's list
+ *   Q, H              2 <= Q <= 4, H >= 16, Q * H in {32, 64, 128}: the
+ *                     kernel treats the step as one query of Q * H heads, in
+ *                     head groups of 32 (so 32 / H query tokens share a pass)
+ *   everything else   as sparse_mla_decode (q [B, Q, H, 576], out
+ *                     [B, Q, H, 512], lse [B, Q, H]; workspace
+ *                     sparse_mla_decode_workspace_size(B, 1, Q * H, topk, 0)),
+ *                     except that the call always takes the split schedule
+ *                     (cluster flags are ignored) and out and lse must be
+ *                     device memory (else NVFP4MLA_ERR_UNSUPPORTED)
+ * Query token j attends exactly to the entries with bit j set that are usable
+ * under sparse_mla_decode's rule for query j (0 <= idx < seq_len,
+ * idx <= seq_len - Q + j, a valid page): the result equals sparse_mla_decode
+ * on per-query lists that hold those entries. Entries invalid for every query
+ * are counted in dev_status as sparse_mla_decode counts them.
+ * Returns as sparse_mla_decode; NVFP4MLA_ERR_INVALID_ARG for unsupported Q, H.
+ */
+int sparse_mla_decode_shared(const void* q, const void* kv_cache, int64_t num_pages, const int32_t* page_table,
+                             int64_t max_pages_per_seq, const int32_t* shared_indices, const uint8_t* member_masks,
+                             const int32_t* seq_lens, int B, int Q, int H, int topk, float softmax_scale, void* out,
+                             float* lse, void* workspace, size_t workspace_bytes, int32_t* dev_status, uint32_t flags,
+                             void* stream);
+
+/*
  * FP8 comparison paths. The pages compare the native NVFP4 decode with (i) a
  * staged path, where a gather kernel unpacks each selected 352-byte NVFP4 row
  * into a 576-byte FP8 copy in GPU memory and an FP8 attention kernel reads the

@@ -9,7 +9,7 @@ C entry points (see include/nvfp4mla.h): mla_kv_pack,
 sparse_mla_decode_workspace_size, sparse_mla_decode, sparse_mla_decode_plan,
 sparse_mla_decode_noalloc, indexer_topk, fp8_kv_pack, nvfp4_stage_fp8,
 sparse_mla_decode_fp8, fp8_token_kv_pack, sparse_mla_decode_fp8_token,
-nvfp4mla_status_string.
+sparse_mla_decode_shared, nvfp4mla_status_string.
 """
 from __future__ import annotations
 
@@ -77,6 +77,9 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.sparse_mla_decode_fp8.argtypes = [vp, vp, i64, vp, i64, vp, vp, i32, i32, i32, i32, ctypes.c_float,
                                               vp, vp, vp, sz, vp, vp]
         lib.sparse_mla_decode_fp8.restype = i32
+        lib.sparse_mla_decode_shared.argtypes = [vp, vp, i64, vp, i64, vp, vp, vp, i32, i32, i32, i32,
+                                                 ctypes.c_float, vp, vp, vp, sz, vp, u32, vp]
+        lib.sparse_mla_decode_shared.restype = i32
         lib.fp8_token_kv_pack.argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, vp, vp]
         lib.fp8_token_kv_pack.restype = i32
         lib.sparse_mla_decode_fp8_token.argtypes = [vp, vp, i64, vp, i64, vp, vp, i32, i32, i32, i32, ctypes.c_float,
@@ -370,3 +373,42 @@ def staged_sparse_mla_decode(q, kv_cache, page_table, topk_indices, seq_lens, so
     o, s = sparse_mla_decode_fp8(q.reshape(B * Q, 1, H, QK_DIM), staged, spt, sidx, ssl, softmax_scale, o, s,
                                  workspace, dev_status, stream)
     return o.view(B, Q, H, LATENT_DIM), s.view(B, Q, H), staging
+
+
+def sparse_mla_decode_shared(q, kv_cache, page_table, shared_indices, member_masks, seq_lens, softmax_scale,
+                             out=None, lse=None, workspace=None, dev_status=None, stream=None, cluster=None):
+    """The Q query tokens of each request folded over one shared index list: q bf16 [B,Q,H,576],
+    shared_indices int32 [B,K], member_masks uint8 [B,K] (bit j: entry in query j's list).
+    Returns (out bf16 [B,Q,H,512], lse fp32 [B,Q,H]). Always the split schedule (cluster flags
+    are ignored); device tensors only."""
+    import torch
+    _check(kv_cache, "kv_cache", torch.uint8, ndim=3)
+    dev = kv_cache.device
+    _check(q, "q", torch.bfloat16, dev, 4)
+    _check(page_table, "page_table", torch.int32, dev, 2)
+    _check(shared_indices, "shared_indices", torch.int32, dev, 2)
+    _check(member_masks, "member_masks", torch.uint8, dev, 2)
+    _check(seq_lens, "seq_lens", torch.int32, dev, 1)
+    B, Q, H, D = q.shape
+    K = shared_indices.shape[1]
+    if (D != QK_DIM or shared_indices.shape[0] != B or tuple(member_masks.shape) != (B, K) or seq_lens.shape[0] != B
+            or page_table.shape[0] != B):
+        raise ValueError("shape mismatch")
+    if out is None:
+        out = torch.empty((B, Q, H, LATENT_DIM), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((B, Q, H), dtype=torch.float32, device=dev)
+    _check(out, "out", torch.bfloat16, dev, 4)
+    _check(lse, "lse", torch.float32, dev, 3)
+    if workspace is None:
+        workspace = torch.empty(max(sparse_mla_decode_workspace_size(B, 1, Q * H, K), 1), dtype=torch.uint8,
+                                device=dev)
+    if dev_status is not None:
+        _check(dev_status, "dev_status", torch.int32, dev, 1)
+    rc = load_library().sparse_mla_decode_shared(
+        _ptr(q), _ptr(kv_cache), kv_cache.shape[0], _ptr(page_table), page_table.shape[1], _ptr(shared_indices),
+        _ptr(member_masks), _ptr(seq_lens), B, Q, H, K, float(softmax_scale), _ptr(out), _ptr(lse), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(dev_status), _cluster_flags(cluster), _stream_ptr(stream))
+    if rc != 0:
+        raise NvFp4MlaError(rc, "sparse_mla_decode_shared")
+    return out, lse

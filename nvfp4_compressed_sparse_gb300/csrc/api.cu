@@ -274,12 +274,19 @@ size_t sparse_mla_decode_workspace_size(int B, int Q, int H, int topk, int num_s
 
 }  // extern "C"
 
-// sparse_mla_decode over either row format (row_fmt 0: 352-byte NVFP4 rows; 1: 576-byte FP8 rows,
-// split schedule and results in device memory only).
+// Folded query tokens of sparse_mla_decode_shared (nullptr: none).
+struct FoldArgs {
+  const uint8_t* member;
+  int q, h;
+};
+
+// sparse_mla_decode over either row format (row_fmt 0: 352-byte NVFP4 rows; 1, 2: FP8 rows, split
+// schedule and results in device memory only), optionally with folded query tokens.
 static int decode_impl(const void* q, const void* kv_cache, int64_t num_pages, const int32_t* page_table,
                        int64_t max_pages_per_seq, const int32_t* topk_indices, const int32_t* seq_lens, int B, int Q,
                        int H, int topk, float softmax_scale, void* out, float* lse, void* workspace,
-                       size_t workspace_bytes, int32_t* dev_status, uint32_t flags, void* stream, int row_fmt) {
+                       size_t workspace_bytes, int32_t* dev_status, uint32_t flags, void* stream, int row_fmt,
+                       const FoldArgs* fold = nullptr) {
   const int row_bytes = row_fmt == 1 ? kFp8RowBytes : (row_fmt == 2 ? kTokRowBytes : kRowBytes);
   if (!sizes_ok(B, Q, H, topk)) return NVFP4MLA_ERR_INVALID_ARG;
   if (q == nullptr || kv_cache == nullptr || page_table == nullptr || topk_indices == nullptr ||
@@ -298,7 +305,7 @@ static int decode_impl(const void* q, const void* kv_cache, int64_t num_pages, c
       k_lse == kPtrInvalid || pointer_kind(kv_cache) != kPtrDevice ||
       (dev_status != nullptr && pointer_kind(dev_status) != kPtrDevice))
     return NVFP4MLA_ERR_INVALID_ARG;
-  if (row_fmt != 0) {
+  if (row_fmt != 0 || fold != nullptr) {
     if (k_out != kPtrDevice || k_lse != kPtrDevice) return NVFP4MLA_ERR_UNSUPPORTED;
     flags = (flags & ~(NVFP4MLA_FLAG_CLUSTER | NVFP4MLA_FLAG_CLUSTER_ANY)) | NVFP4MLA_FLAG_SPLIT;
   }
@@ -346,6 +353,9 @@ static int decode_impl(const void* q, const void* kv_cache, int64_t num_pages, c
   p.ctas = s.ctas;
   p.cluster = s.cluster;
   p.withhold = (flags & NVFP4MLA_FLAG_TEST_TIMEOUT) ? 1u : 0u;
+  p.fold_member = fold ? fold->member : nullptr;
+  p.fold_q = fold ? fold->q : 1;
+  p.fold_h = fold ? fold->h : H;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (launch_decode(p, st) != cudaSuccess) return NVFP4MLA_ERR_CUDA;
   if (p.cluster == 0 && launch_merge(p, st) != cudaSuccess) return NVFP4MLA_ERR_CUDA;
@@ -368,6 +378,19 @@ int sparse_mla_decode_fp8(const void* q, const void* kv_cache_fp8, int64_t num_p
                           size_t workspace_bytes, int32_t* dev_status, void* stream) {
   return decode_impl(q, kv_cache_fp8, num_pages, page_table, max_pages_per_seq, topk_indices, seq_lens, B, Q, H,
                      topk, softmax_scale, out, lse, workspace, workspace_bytes, dev_status, 0u, stream, 1);
+}
+
+int sparse_mla_decode_shared(const void* q, const void* kv_cache, int64_t num_pages, const int32_t* page_table,
+                             int64_t max_pages_per_seq, const int32_t* shared_indices, const uint8_t* member_masks,
+                             const int32_t* seq_lens, int B, int Q, int H, int topk, float softmax_scale, void* out,
+                             float* lse, void* workspace, size_t workspace_bytes, int32_t* dev_status, uint32_t flags,
+                             void* stream) {
+  if (Q < 2 || Q > 4 || H < 16 || (int64_t)Q * H > 128) return NVFP4MLA_ERR_INVALID_ARG;
+  if (member_masks == nullptr) return NVFP4MLA_ERR_INVALID_ARG;
+  if (pointer_kind(member_masks) != kPtrDevice) return NVFP4MLA_ERR_INVALID_ARG;
+  FoldArgs fold{member_masks, Q, H};
+  return decode_impl(q, kv_cache, num_pages, page_table, max_pages_per_seq, shared_indices, seq_lens, B, 1, Q * H,
+                     topk, softmax_scale, out, lse, workspace, workspace_bytes, dev_status, flags, stream, 0, &fold);
 }
 
 int sparse_mla_decode_fp8_token(const void* q, const void* kv_cache_tok, int64_t num_pages, const int32_t* page_table,

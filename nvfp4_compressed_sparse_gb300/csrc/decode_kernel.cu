@@ -96,6 +96,8 @@ struct alignas(16) Smem {
   uint32_t maskbuf[2][kRingStages];  // producer -> dequant: usable rows of each 32-row stage, by tile parity
   uint32_t stage_cnt[kRingStages];   // dequant warps done with a ring stage (2 per tile)
   uint32_t vmask[2][4];              // dequant -> softmax: usable rows of the tile, by tile parity
+  uint32_t maskq[2][4][4];           // folded queries: producer -> dequant, rows of each query token, by tile parity
+  uint32_t vmaskq[2][4][4];          // folded queries: dequant -> softmax, rows of each query token
   alignas(16) float red[4][32];      // softmax group: per-warp partial reductions (float4 stores)
   int vote[4];                       // softmax group: does a warp see a score above max + kLazy
   int need_rescale;
@@ -234,10 +236,12 @@ __device__ __forceinline__ float q_image(const DecodeParams& p, int64_t unit, in
 // are already in flight.
 struct TileIdx {
   int idx[2];     // this lane's entries of the warp's two 32-row stages
+  uint32_t mem[2];  // folded queries: the entries' query-token bits
   int L, causal;  // sequence length, causal limit of the query
   int b;
 };
 
+template <bool kFold>
 __device__ __forceinline__ void load_tile_idx(const DecodeParams& p, int64_t g, int lane, int q0, TileIdx& t) {
   const int64_t unit = g / p.tiles_per_unit;
   const int local = (int)(g - unit * p.tiles_per_unit);
@@ -251,6 +255,7 @@ __device__ __forceinline__ void load_tile_idx(const DecodeParams& p, int64_t g, 
   for (int qq = 0; qq < 2; ++qq) {
     const int e = local * kTileTokens + (q0 + qq) * 32 + lane;
     t.idx[qq] = e < p.topk ? __ldg(row + e) : -1;
+    t.mem[qq] = (kFold && e < p.topk) ? (uint32_t)__ldg(p.fold_member + (int64_t)b * p.topk + e) : 0u;
   }
 }
 
@@ -273,20 +278,21 @@ __device__ __forceinline__ void gather4(void* dst, const CUtensorMap* map, int r
       : "memory");
 }
 
+template <bool kFold>
 __device__ void producer_loop(const DecodeParams& p, Smem* sm, int64_t t_begin, int64_t t_end, int pw) {
   const int lane = threadIdx.x & 31;
   const int q0 = 2 * pw;
   TileIdx A0, A1, A2;
   int pg0[2], pg1[2];
-  if (t_begin < t_end) load_tile_idx(p, t_begin, lane, q0, A0);
-  if (t_begin + 1 < t_end) load_tile_idx(p, t_begin + 1, lane, q0, A1);
+  if (t_begin < t_end) load_tile_idx<kFold>(p, t_begin, lane, q0, A0);
+  if (t_begin + 1 < t_end) load_tile_idx<kFold>(p, t_begin + 1, lane, q0, A1);
   if (t_begin < t_end) load_tile_pages(p, A0, pg0);
   for (int64_t g = t_begin; g < t_end && !sm->abort; ++g) {
     const int64_t k = g - t_begin;
     const int b = (int)(k & 1);
     const TileInfo ti = tile_info(p, g, t_begin, t_end);
     if (g + 1 < t_end) load_tile_pages(p, A1, pg1);
-    if (g + 2 < t_end) load_tile_idx(p, g + 2, lane, q0, A2);
+    if (g + 2 < t_end) load_tile_idx<kFold>(p, g + 2, lane, q0, A2);
     const int hg = (int)(ti.unit % p.head_groups);
     // The row table is free once every stage of tile k-1 has been requested; by then tile k-2's
     // masks (the other parity) have been read too.
@@ -311,6 +317,15 @@ __device__ void producer_loop(const DecodeParams& p, Smem* sm, int64_t t_begin, 
       const uint32_t mask = __ballot_sync(0xffffffffu, ok);
       sm->rowbuf[q * 32 + lane] = ok ? page * kPageTokens + (idx & 63) : -1;
       if (lane == 0) sm->maskbuf[b][q] = mask;
+      if constexpr (kFold) {
+        // query token jj of the fold may use the entry if it is listed for jj and within jj's causal range
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          const bool use = ok && jj < p.fold_q && ((A0.mem[qq] >> jj) & 1u) && idx <= A0.L - p.fold_q + jj;
+          const uint32_t mj = __ballot_sync(0xffffffffu, use);
+          if (lane == 0) sm->maskq[b][q][jj] = mj;
+        }
+      }
     }
     __syncwarp();
     // (testing aid: withholding tile 1's table makes the waits on it expire)
@@ -386,7 +401,7 @@ __device__ __forceinline__ void convert_fp8_64(const uint8_t* src, uint32_t (&r)
 // releases the ring stage. Pass B copies the latent part of those K rows from TMEM into the
 // V tile in shared memory (the A operand of PV, read MN-major) once PV of the previous tile is done
 // with those V rows, so the compressed rows are converted only once and leave the ring early.
-template <int kFmt>
+template <int kFmt, bool kFold>
 __device__ void dequant_loop(const DecodeParams& p, Smem* sm, uint8_t* ring, uint8_t* vtile, float* rowscale,
                              int64_t t_begin, int64_t t_end, int warp) {
   using F = RowFmt<kFmt>;
@@ -470,6 +485,10 @@ __device__ void dequant_loop(const DecodeParams& p, Smem* sm, uint8_t* ring, uin
     if constexpr (kFmt == 2) {
       // the row's scale, for the softmax (published with the row mask)
       if (half == 0) rowscale[(k & 1) * kTileTokens + row] = *reinterpret_cast<const float*>(rowp + kTokScaleOff);
+      __syncwarp();
+    }
+    if constexpr (kFold) {
+      if (half == 0 && lane < 4) sm->vmaskq[k & 1][q][lane] = sm->maskq[k & 1][q][lane];
       __syncwarp();
     }
     if (lane == 0) {
@@ -719,7 +738,7 @@ constexpr float kLazy = 15.f;
 // inside fp16's range exactly as P does for the other formats, and the row sums add P' / scale_t.
 // O and the sums share the reference, so the quotient and the LSE (m + log2 of the sum) are
 // unchanged.
-template <int NH, bool kCluster, int kFmt = 0>
+template <int NH, bool kCluster, int kFmt = 0, bool kFold = false>
 __device__ bool softmax_loop(const DecodeParams& p, Smem* sm, uint8_t* ps, uint8_t* vtile, ClusterScratch* cs,
                              const float* rowscale, int64_t t_begin, int64_t t_end, int64_t cta, float qscale) {
   constexpr uint32_t kPBytes = 128 * NH * 2;
@@ -768,6 +787,19 @@ __device__ bool softmax_loop(const DecodeParams& p, Smem* sm, uint8_t* ps, uint8
       }
     } else {
       load_scores<NH>(tmem_lane + s_col, valid, qscale, z);
+    }
+    if constexpr (kFold) {
+      // folded queries: column h of head group hg is head (hg * NH + h) % fold_h of query token
+      // (hg * NH + h) / fold_h, which uses this row only if the row is in its list and causal range
+      int fb, fj, hg;
+      split_unit(p, ti.unit, fb, fj, hg);
+      uint32_t qb = 0;
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) qb |= ((sm->vmaskq[k & 1][w][jj] >> lane) & 1u) << jj;
+      const int hshift = __ffs(p.fold_h) - 1;
+#pragma unroll
+      for (int h = 0; h < NH; ++h)
+        if (!((qb >> ((hg * NH + h) >> hshift)) & 1u)) z[h] = kNegInf;
     }
     // ---- lazy running max: vote whether any score exceeds max + kLazy (the first tile of a unit
     // always sets the max, so it skips the vote)
@@ -1022,9 +1054,11 @@ __device__ void cluster_merge(const DecodeParams& p, ClusterScratch* sm, uint8_t
 // kCluster: the cluster schedule (in-kernel q, DSMEM merge). kPublish: the split schedule with a
 // polling merge grid (results in host memory): each CTA tags its partial slots when done. The
 // tagging is a separate instance because its mere presence slowed the other split kernel by ~2 %.
-template <int NH, bool kCluster, bool kPublish, int kFmt = 0>
+template <int NH, bool kCluster, bool kPublish, int kFmt = 0, bool kFold = false>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ DecodeParams p) {
   static_assert(kFmt == 0 || !kCluster, "FP8 rows run on the split schedule only");
+  static_assert(!kFold || (!kCluster && !kPublish && kFmt == 0),
+                "folded queries run on the split schedule with results in device memory");
   static_assert(kFmt == 0 || !kPublish, "FP8 rows write their results to device memory only");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1098,14 +1132,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     }
   }
   if (warp == 0 || warp == 3) {
-    producer_loop(p, sm, t_begin, t_end, warp == 0 ? 0 : 1);
+    producer_loop<kFold>(p, sm, t_begin, t_end, warp == 0 ? 0 : 1);
   } else if (warp == 1 || warp == 2) {
     if ((threadIdx.x & 31) == 0) mma_loop<NH, kCluster>(p, sm, vtile, qs, ps, t_begin, t_end, warp - 1);
     __syncwarp();
   } else if (warp >= 4 && warp < 12) {
-    dequant_loop<kFmt>(p, sm, ring, vtile, rowscale, t_begin, t_end, warp);
+    dequant_loop<kFmt, kFold>(p, sm, ring, vtile, rowscale, t_begin, t_end, warp);
   } else if (warp >= 12) {
-    const bool ok = softmax_loop<NH, kCluster, kFmt>(p, sm, ps, vtile, reinterpret_cast<ClusterScratch*>(ring),
+    const bool ok = softmax_loop<NH, kCluster, kFmt, kFold>(p, sm, ps, vtile, reinterpret_cast<ClusterScratch*>(ring),
                                                      rowscale, t_begin, t_end, cta, qscale);
     if constexpr (kPublish) {
       // Polling merge (results in host memory): publish this CTA's partials. Every writer fences
@@ -1315,17 +1349,20 @@ static cudaError_t set_attributes() {
     const cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess && result == cudaSuccess) result = e;
   }
-  const void* big[10] = {(const void*)decode_kernel<32, false, false>,    (const void*)decode_kernel<32, false, true>,
+  const void* big[12] = {(const void*)decode_kernel<32, false, false>,    (const void*)decode_kernel<32, false, true>,
                          (const void*)decode_kernel<32, true, false>,     (const void*)decode_kernel<16, false, false>,
                          (const void*)decode_kernel<16, false, true>,     (const void*)decode_kernel<16, true, false>,
                          (const void*)decode_kernel<32, false, false, 1>, (const void*)decode_kernel<16, false, false, 1>,
-                         (const void*)decode_kernel<32, false, false, 2>, (const void*)decode_kernel<16, false, false, 2>};
-  const int bytes[10] = {(int)decode_smem_bytes<32>(),    (int)decode_smem_bytes<32>(), (int)decode_smem_bytes<32>(),
+                         (const void*)decode_kernel<32, false, false, 2>, (const void*)decode_kernel<16, false, false, 2>,
+                         (const void*)decode_kernel<32, false, false, 0, true>,
+                         (const void*)decode_kernel<16, false, false, 0, true>};
+  const int bytes[12] = {(int)decode_smem_bytes<32>(),    (int)decode_smem_bytes<32>(), (int)decode_smem_bytes<32>(),
                          (int)decode_smem_bytes<16>(),    (int)decode_smem_bytes<16>(), (int)decode_smem_bytes<16>(),
                          (int)decode_smem_bytes<32, 1>(), (int)decode_smem_bytes<16, 1>(),
-                         (int)decode_smem_bytes<32, 2>(), (int)decode_smem_bytes<16, 2>()};
+                         (int)decode_smem_bytes<32, 2>(), (int)decode_smem_bytes<16, 2>(),
+                         (int)decode_smem_bytes<32>(),    (int)decode_smem_bytes<16>()};
   static_assert(sizeof(big) / sizeof(big[0]) == sizeof(bytes) / sizeof(bytes[0]), "one size per decode instance");
-  for (int i = 0; i < 10; ++i) {
+  for (int i = 0; i < 12; ++i) {
     const cudaError_t e = cudaFuncSetAttribute(big[i], cudaFuncAttributeMaxDynamicSharedMemorySize, bytes[i]);
     if (e != cudaSuccess && result == cudaSuccess) result = e;
   }
@@ -1392,6 +1429,10 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream) {
   if (p.row_fmt == 1) {   // FP8 rows: results in device memory (the host checks)
     if (h32) return cudaLaunchKernelEx(&cfg, decode_kernel<32, false, false, 1>, p);
     return cudaLaunchKernelEx(&cfg, decode_kernel<16, false, false, 1>, p);
+  }
+  if (p.fold_q > 1) {     // folded queries: results in device memory (the host checks)
+    if (h32) return cudaLaunchKernelEx(&cfg, decode_kernel<32, false, false, 0, true>, p);
+    return cudaLaunchKernelEx(&cfg, decode_kernel<16, false, false, 0, true>, p);
   }
   if (p.row_fmt == 2) {   // per-token FP8 rows: results in device memory (the host checks)
     if (h32) return cudaLaunchKernelEx(&cfg, decode_kernel<32, false, false, 2>, p);

@@ -70,6 +70,11 @@ struct DecodeParams {
   int tiles_per_unit, ctas;
   int cluster;                // 0 = stream-K split, else CTAs per unit (one cluster per unit)
   uint32_t withhold;          // testing aid: 1 = the producers never publish tile 1's row table
+  // Folded queries (sparse_mla_decode_shared): the kernel runs Q = 1 with H = fold_q * fold_h heads, the
+  // fold_q query tokens of a request sharing one index list; fold_member[b * topk + e] bit j says whether
+  // entry e belongs to query token j. fold_q = 1: no fold.
+  const uint8_t* fold_member;
+  int fold_q, fold_h;
   int row_fmt;                // 0 = 352-byte NVFP4 rows, 1 = 576-byte FP8 rows, 2 = 672-byte per-token FP8 rows
                               // (1 and 2: split schedule only)
 };

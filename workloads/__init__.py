@@ -120,6 +120,35 @@ def _shared_lists(rng, L: int, Q: int, K: int, shared: float) -> np.ndarray:
     return out
 
 
+def subset_lists(rng, L: int, Q: int, K: int, keep: float) -> np.ndarray:
+    """Index lists [Q, K] of one request whose Q query tokens each keep round(keep * K) positions
+    of one set of K positions valid for all of them (before L - Q + 1), in increasing order and -1
+    padded: the tokens' lists fit in one shared list of K entries."""
+    base = np.sort(_draw_without_replacement(rng, 0, L - Q + 1, K))
+    n = int(round(keep * K))
+    out = np.full((Q, K), -1, dtype=np.int64)
+    for j in range(Q):
+        out[j, :n] = np.sort(base[rng.permutation(K)[:n]])
+    return out
+
+
+def fold_lists(topk_indices: np.ndarray):
+    """Per-query index lists int [B, Q, K] -> (shared int32 [B, U], member uint8 [B, U]): each
+    request's distinct entries (-1 dropped; invalid positions kept, the decode skips them) in
+    increasing order, -1 padded to the longest union U, and bit j of member set where the entry
+    is in query j's list."""
+    B, Q, _ = topk_indices.shape
+    unions = [np.unique(topk_indices[b][topk_indices[b] != -1]) for b in range(B)]
+    U = max(1, max(u.size for u in unions))
+    shared = np.full((B, U), -1, dtype=np.int32)
+    member = np.zeros((B, U), dtype=np.uint8)
+    for b, u in enumerate(unions):
+        shared[b, :u.size] = u
+        for j in range(Q):
+            member[b, :u.size] |= (np.isin(u, topk_indices[b, j]).astype(np.uint8) << j)
+    return shared, member
+
+
 def host_rows(case: DecodeCase, pages: np.ndarray):
     """Draw the bf16 latent and rope rows of the given physical pages on the host.
 

@@ -48,3 +48,27 @@ def test_bf16_rounding_is_nearest_even():
     x = np.array([1.0, 1.0 + 2**-8, 1.0 + 3 * 2**-8, -2.5, 0.0, -0.0], np.float32)
     bits = workloads.f32_to_bf16_bits(x)
     assert bits.tolist() == [0x3F80, 0x3F80, 0x3F82, 0xC020, 0x0000, 0x8000]
+
+
+def test_fold_lists_round_trip():
+    """The shared list and member bits give back each query's set of entries (duplicates merged)."""
+    rng = np.random.default_rng(0)
+    lists = rng.integers(-1, 50, size=(3, 4, 20))
+    shared, member = workloads.fold_lists(lists)
+    for b in range(3):
+        for j in range(4):
+            got = set(shared[b][((member[b] >> j) & 1).astype(bool)].tolist())
+            assert got == set(lists[b, j].tolist()) - {-1}
+        u = shared[b][shared[b] != -1]
+        assert (np.diff(u) > 0).all() and not member[b][shared[b] == -1].any()
+
+
+def test_subset_and_shared_lists_shapes():
+    rng = np.random.default_rng(1)
+    L, Q, K = 9000, 4, 512
+    sub = workloads.subset_lists(rng, L, Q, K, 0.9)
+    assert sub.shape == (Q, K) and all((sub[j] != -1).sum() == round(0.9 * K) for j in range(Q))
+    assert np.unique(sub[sub != -1]).size <= K and sub.max() <= L - Q
+    sh = workloads._shared_lists(rng, L, Q, K, 0.9)
+    for j in range(Q):
+        assert np.unique(sh[j]).size == K and sh[j].max() <= L - Q + j and (np.diff(sh[j]) > 0).all()

@@ -191,6 +191,7 @@ size_t sparse_mla_decode_workspace_size(int B, int Q, int H, int topk, int num_s
 #define NVFP4MLA_FLAG_CLUSTER (1u << 30)
 #define NVFP4MLA_FLAG_CLUSTER_ANY (1u << 29)
 #define NVFP4MLA_FLAG_SPLIT (1u << 28)
+#define NVFP4MLA_FLAG_PAIR (1u << 27)
 int sparse_mla_decode(const void* q, const void* kv_cache, int64_t num_pages, const int32_t* page_table,
                       int64_t max_pages_per_seq, const int32_t* topk_indices, const int32_t* seq_lens, int B,
                       int Q, int H, int topk, float softmax_scale, void* out, float* lse, void* workspace,

@@ -28,6 +28,7 @@ FLAG_TEST_TIMEOUT = 1 << 31   # NVFP4MLA_FLAG_TEST_TIMEOUT
 FLAG_CLUSTER = 1 << 30        # NVFP4MLA_FLAG_CLUSTER
 FLAG_CLUSTER_ANY = 1 << 29    # NVFP4MLA_FLAG_CLUSTER_ANY
 FLAG_SPLIT = 1 << 28          # NVFP4MLA_FLAG_SPLIT
+FLAG_PAIR = 1 << 27           # NVFP4MLA_FLAG_PAIR
 STATUS_WORDS = 4
 STAT_BAD_INDEX, STAT_BAD_PAGE, STAT_TIMEOUT, STAT_BAD_SLOT = 0, 1, 2, 3
 
@@ -172,17 +173,21 @@ def sparse_mla_decode_workspace_size(B: int, Q: int, H: int, topk: int, num_sms:
 def _cluster_flags(cluster) -> int:
     # cluster: None (the library's default schedule), False/"split" (always the split schedule),
     # True (also the cluster schedule wherever it is as balanced as the split one) or "any" (the
-    # cluster schedule whenever one wave of clusters fits; a tuning aid)
+    # cluster schedule whenever one wave of clusters fits; a tuning aid) or "pair" (the split run by
+    # 2-CTA clusters, one half of the contraction per CTA)
     if cluster is None:
         return 0
     if cluster is False or cluster == "split":
         return FLAG_SPLIT
+    if cluster == "pair":
+        return FLAG_PAIR
     return FLAG_CLUSTER | (FLAG_CLUSTER_ANY if cluster == "any" else 0)
 
 
 def sparse_mla_decode_plan(B: int, Q: int, H: int, topk: int, max_ctas: int = 0,
                            cluster=None) -> tuple[int, int]:
-    """(decode CTAs, cluster size G; 0 = split schedule) that sparse_mla_decode launches on the current device."""
+    """(decode CTAs, cluster size G; 0 = split schedule, -2 = pair schedule) that sparse_mla_decode
+    launches on the current device."""
     flags = (max_ctas & 0xFFFF) | _cluster_flags(cluster)
     ctas, g = ctypes.c_int(0), ctypes.c_int(0)
     rc = load_library().sparse_mla_decode_plan(B, Q, H, topk, flags, ctypes.byref(ctas), ctypes.byref(g))

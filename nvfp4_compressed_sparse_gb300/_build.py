@@ -17,7 +17,8 @@ CSRC = os.path.join(PKG_DIR, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_PATH = os.path.join(PKG_DIR, "libnvfp4mla.so")
-SOURCES = ["api.cu", "pack_kernel.cu", "decode_kernel.cu", "noalloc.cu", "topk_kernel.cu", "fp8_kernels.cu"]
+SOURCES = ["api.cu", "pack_kernel.cu", "decode_kernel.cu", "decode_pair.cu", "noalloc.cu", "topk_kernel.cu",
+           "fp8_kernels.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v", "-I", INCLUDE]
 

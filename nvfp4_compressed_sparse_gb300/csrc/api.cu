@@ -43,6 +43,17 @@ DecodeSchedule make_schedule(int B, int Q, int H, int topk, int num_sms, int max
   s.ctas = (int)g;
   s.partial_slots = s.ctas + s.units - 1;
   s.cluster = 0;
+  s.pair = 0;
+  if (policy == kPairSplit) {
+    // one stream-K range per pair of SMs
+    int64_t pairs = num_sms > 1 ? num_sms / 2 : 1;
+    if (max_ctas > 0 && max_ctas < pairs) pairs = max_ctas;
+    if (pairs > s.total_tiles) pairs = s.total_tiles;
+    s.ctas = (int)pairs;
+    s.partial_slots = s.ctas + s.units - 1;
+    s.pair = 1;
+    return s;
+  }
   // Cluster schedule: G = min(8, SMs / units, tiles per unit) CTAs per unit, one wave; it needs no
   // q-prep and no merge grid. kClusterBalanced takes it when no CTA then runs more tiles than under
   // the stream-K split, kClusterAny whenever G >= 1 (to measure the schedules against each other).
@@ -176,7 +187,10 @@ static bool plan_on_device(int B, int Q, int H, int topk, uint32_t flags, bool h
   ClusterPolicy policy = host_results ? kClusterNone : kClusterDefault;
   if (flags & NVFP4MLA_FLAG_CLUSTER) policy = (flags & NVFP4MLA_FLAG_CLUSTER_ANY) ? kClusterAny : kClusterBalanced;
   if (flags & NVFP4MLA_FLAG_SPLIT) policy = kClusterNone;
+  if ((flags & NVFP4MLA_FLAG_PAIR) && !host_results && !(flags & NVFP4MLA_FLAG_SPLIT)) policy = kPairSplit;
   DecodeSchedule s = make_schedule(B, Q, H, topk, sms, (int)(flags & 0xFFFFu), policy);
+  if (s.pair && max_active_pairs(H < kHeadsPerCta ? H : kHeadsPerCta) < s.ctas)
+    s = make_schedule(B, Q, H, topk, sms, (int)(flags & 0xFFFFu), kClusterNone);
   if (s.cluster > 1) {
     const int fit = max_active_clusters(H < kHeadsPerCta ? H : kHeadsPerCta, s.cluster);
     if (fit < s.units) s = make_schedule(B, Q, H, topk, sms, (int)(flags & 0xFFFFu), kClusterNone);
@@ -258,8 +272,8 @@ int sparse_mla_decode_plan(int B, int Q, int H, int topk, uint32_t flags, int* c
   if (!sizes_ok(B, Q, H, topk)) return NVFP4MLA_ERR_INVALID_ARG;
   DecodeSchedule s;
   if (!plan_on_device(B, Q, H, topk, flags, false, &s)) return NVFP4MLA_ERR_CUDA;
-  if (ctas != nullptr) *ctas = s.ctas;
-  if (cluster != nullptr) *cluster = s.cluster;
+  if (ctas != nullptr) *ctas = s.pair ? 2 * s.ctas : s.ctas;
+  if (cluster != nullptr) *cluster = s.pair ? -2 : s.cluster;
   return NVFP4MLA_OK;
 }
 
@@ -307,7 +321,7 @@ static int decode_impl(const void* q, const void* kv_cache, int64_t num_pages, c
     return NVFP4MLA_ERR_INVALID_ARG;
   if (row_fmt != 0 || fold != nullptr) {
     if (k_out != kPtrDevice || k_lse != kPtrDevice) return NVFP4MLA_ERR_UNSUPPORTED;
-    flags = (flags & ~(NVFP4MLA_FLAG_CLUSTER | NVFP4MLA_FLAG_CLUSTER_ANY)) | NVFP4MLA_FLAG_SPLIT;
+    flags = (flags & ~(NVFP4MLA_FLAG_CLUSTER | NVFP4MLA_FLAG_CLUSTER_ANY | NVFP4MLA_FLAG_PAIR)) | NVFP4MLA_FLAG_SPLIT;
   }
   DecodeSchedule s;
   if (!plan_on_device(B, Q, H, topk, flags, k_out == kPtrHost || k_lse == kPtrHost, &s)) return NVFP4MLA_ERR_CUDA;
@@ -352,6 +366,7 @@ static int decode_impl(const void* q, const void* kv_cache, int64_t num_pages, c
   p.tiles_per_unit = s.tiles_per_unit;
   p.ctas = s.ctas;
   p.cluster = s.cluster;
+  p.pair = s.pair;
   p.withhold = (flags & NVFP4MLA_FLAG_TEST_TIMEOUT) ? 1u : 0u;
   p.fold_member = fold ? fold->member : nullptr;
   p.fold_q = fold ? fold->q : 1;

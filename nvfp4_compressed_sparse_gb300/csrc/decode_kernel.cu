@@ -35,6 +35,7 @@
 
 #include <mutex>
 
+#include "decode_common.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -71,8 +72,8 @@ struct alignas(16) Smem {
   alignas(16) float m_used[32];      // running max per head (log2 units); read as float4
   alignas(16) float alpha[32];       // rescale factor of this tile per head; read as float4
   uint64_t ring_full[kRingStages];   // gathered rows of a 32-row stage have landed
-  uint64_t rows_full;                // row numbers + masks of a tile resolved (2 producer warps)
-  uint64_t rows_empty;               // every stage of that tile has been requested (4 issuing warps)
+  uint64_t rows_full[1];             // row numbers + masks of a tile resolved (2 producer warps)
+  uint64_t rows_empty[1];            // every stage of that tile has been requested (4 issuing warps)
   // Half h of a tile = latent dims 256h..256h+255 (half 1 also carries the rope dims). Each half has
   // its own dequant warps and MMA issuer, so the two halves pipeline independently and only meet
   // in the softmax.
@@ -92,7 +93,7 @@ struct alignas(16) Smem {
   uint64_t drain;                    // every UMMA of both issuers complete
   uint32_t tmem_base;
   volatile int abort;
-  alignas(16) int32_t rowbuf[kTileTokens];  // producer -> dequant: cache row of every tile entry (-1: unusable)
+  alignas(16) int32_t rowbuf[1][kTileTokens];  // producer -> dequant: cache row of every tile entry (-1: unusable)
   uint32_t maskbuf[2][kRingStages];  // producer -> dequant: usable rows of each 32-row stage, by tile parity
   uint32_t stage_cnt[kRingStages];   // dequant warps done with a ring stage (2 per tile)
   uint32_t vmask[2][4];              // dequant -> softmax: usable rows of the tile, by tile parity
@@ -111,58 +112,6 @@ struct ClusterScratch {
   float cw[8][32];                   // weight of each CTA's partial per head
   float cinv[32], clse[32];          // 1 / combined sum, LSE per head
 };
-
-struct TileInfo {
-  int64_t unit;     // virtual unit (query, head group)
-  int local;        // tile index within the unit
-  bool first, last; // first/last tile of this CTA's segment of the unit
-};
-
-// Tile numbers fit in 32 bits (the host rejects larger problems), so unsigned 32-bit division is used.
-__device__ __forceinline__ TileInfo tile_info(const DecodeParams& p, int64_t g, int64_t t_begin, int64_t t_end) {
-  TileInfo ti;
-  const uint32_t u = (uint32_t)g / (uint32_t)p.tiles_per_unit;
-  ti.unit = u;
-  ti.local = (int)((uint32_t)g - u * (uint32_t)p.tiles_per_unit);
-  ti.first = (g == t_begin) || (ti.local == 0);
-  ti.last = (g == t_end - 1) || (ti.local == p.tiles_per_unit - 1);
-  return ti;
-}
-
-__device__ __forceinline__ void fail(Smem* sm, int32_t* status) {
-  if (!sm->abort) {
-    sm->abort = 1;
-    if (status != nullptr) atomicAdd(status + 2, 1);
-  }
-}
-
-__device__ __forceinline__ bool wait(Smem* sm, uint64_t* bar, uint32_t parity, int32_t* status) {
-  if (mbar_wait(bar, parity, &sm->abort, kWaitTimeoutNs)) return true;
-  fail(sm, status);
-  return false;
-}
-
-__device__ __forceinline__ void named_sync_softmax() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
-// Softmax-group barrier that also ORs a flag over the group, so every thread gets the same answer
-// (the abort flag can be set by another warp at any time; reading it after a plain barrier could
-// let one warp leave while the others wait at the next barrier).
-__device__ __forceinline__ bool named_sync_softmax_any(bool v) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, 1, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"((uint32_t)v)
-      : "memory");
-  return r != 0;
-}
-
-// Unit decomposition: virtual unit -> (b, j, head group)
-__device__ __forceinline__ void split_unit(const DecodeParams& p, int64_t unit, int& b, int& j, int& hg) {
-  hg = (int)(unit % p.head_groups);
-  const int64_t u = unit / p.head_groups;
-  b = (int)(u / p.Q);
-  j = (int)(u - (int64_t)b * p.Q);
-}
 
 // ------------------------------------------------------------------ q image
 // q (bf16) of one (query, head group) -> FP16 scaled by 2^e so that max|q| * 2^e lies in
@@ -225,118 +174,6 @@ __device__ __forceinline__ float q_image(const DecodeParams& p, int64_t unit, in
   return p.scale_log2 * ldexpf(1.f, -e);
 }
 
-// ------------------------------------------------------------------ producer
-// Two producer warps; warp pw owns ring stages 2pw and 2pw+1 of every tile.
-// Rows are gathered by TMA tile::gather4 (four arbitrary cache rows per
-// instruction; lanes 0..7 each issue one per 32-row stage). Unusable entries
-// get row -1, which the TMA unit fills with zeros without reading memory, so
-// every stage always lands exactly 32 x 352 bytes.
-// Index resolution is software-pipelined two tiles ahead: while tile g's rows
-// are issued, the page-table words of tile g+1 and the index words of tile g+2
-// are already in flight.
-struct TileIdx {
-  int idx[2];     // this lane's entries of the warp's two 32-row stages
-  uint32_t mem[2];  // folded queries: the entries' query-token bits
-  int L, causal;  // sequence length, causal limit of the query
-  int b;
-};
-
-template <bool kFold>
-__device__ __forceinline__ void load_tile_idx(const DecodeParams& p, int64_t g, int lane, int q0, TileIdx& t) {
-  const int64_t unit = g / p.tiles_per_unit;
-  const int local = (int)(g - unit * p.tiles_per_unit);
-  int b, j, hg;
-  split_unit(p, unit, b, j, hg);
-  t.b = b;
-  t.L = __ldg(p.seq_lens + b);
-  t.causal = t.L - p.Q + j;
-  const int32_t* row = p.idx + ((int64_t)b * p.Q + j) * p.topk;
-#pragma unroll
-  for (int qq = 0; qq < 2; ++qq) {
-    const int e = local * kTileTokens + (q0 + qq) * 32 + lane;
-    t.idx[qq] = e < p.topk ? __ldg(row + e) : -1;
-    t.mem[qq] = (kFold && e < p.topk) ? (uint32_t)__ldg(p.fold_member + (int64_t)b * p.topk + e) : 0u;
-  }
-}
-
-__device__ __forceinline__ void load_tile_pages(const DecodeParams& p, const TileIdx& t, int (&pg)[2]) {
-  const int32_t* pt_row = p.page_table + (int64_t)t.b * p.max_pages;
-#pragma unroll
-  for (int qq = 0; qq < 2; ++qq) {
-    const int idx = t.idx[qq];
-    const bool in_range = idx >= 0 && idx < t.L && idx <= t.causal;
-    pg[qq] = (in_range && (idx >> 6) < p.max_pages) ? __ldg(pt_row + (idx >> 6)) : -1;
-  }
-}
-
-__device__ __forceinline__ void gather4(void* dst, const CUtensorMap* map, int r0, int r1, int r2, int r3,
-                                        uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
-      "l"(map), "r"(0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar))
-      : "memory");
-}
-
-template <bool kFold>
-__device__ void producer_loop(const DecodeParams& p, Smem* sm, int64_t t_begin, int64_t t_end, int pw) {
-  const int lane = threadIdx.x & 31;
-  const int q0 = 2 * pw;
-  TileIdx A0, A1, A2;
-  int pg0[2], pg1[2];
-  if (t_begin < t_end) load_tile_idx<kFold>(p, t_begin, lane, q0, A0);
-  if (t_begin + 1 < t_end) load_tile_idx<kFold>(p, t_begin + 1, lane, q0, A1);
-  if (t_begin < t_end) load_tile_pages(p, A0, pg0);
-  for (int64_t g = t_begin; g < t_end && !sm->abort; ++g) {
-    const int64_t k = g - t_begin;
-    const int b = (int)(k & 1);
-    const TileInfo ti = tile_info(p, g, t_begin, t_end);
-    if (g + 1 < t_end) load_tile_pages(p, A1, pg1);
-    if (g + 2 < t_end) load_tile_idx<kFold>(p, g + 2, lane, q0, A2);
-    const int hg = (int)(ti.unit % p.head_groups);
-    // The row table is free once every stage of tile k-1 has been requested; by then tile k-2's
-    // masks (the other parity) have been read too.
-    bool good = true;
-    if (lane == 0 && k >= 1) good = wait(sm, &sm->rows_empty, (uint32_t)((k - 1) & 1), p.status);
-    good = __shfl_sync(0xffffffffu, good, 0);
-    if (!good) break;
-#pragma unroll
-    for (int qq = 0; qq < 2; ++qq) {
-      const int q = q0 + qq;
-      const int idx = A0.idx[qq];
-      const int page = pg0[qq];
-      const bool in_range = idx >= 0 && idx < A0.L && idx <= A0.causal;
-      const bool ok = in_range && page >= 0 && page < p.num_pages;
-      if (hg == 0 && p.status != nullptr) {
-        const int e = ti.local * kTileTokens + q * 32 + lane;
-        const uint32_t nbi = __popc(__ballot_sync(0xffffffffu, idx != -1 && !in_range && e < p.topk));
-        const uint32_t nbp = __popc(__ballot_sync(0xffffffffu, in_range && !ok));
-        if (lane == 0 && nbi) atomicAdd(p.status + 0, (int)nbi);
-        if (lane == 0 && nbp) atomicAdd(p.status + 1, (int)nbp);
-      }
-      const uint32_t mask = __ballot_sync(0xffffffffu, ok);
-      sm->rowbuf[q * 32 + lane] = ok ? page * kPageTokens + (idx & 63) : -1;
-      if (lane == 0) sm->maskbuf[b][q] = mask;
-      if constexpr (kFold) {
-        // query token jj of the fold may use the entry if it is listed for jj and within jj's causal range
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          const bool use = ok && jj < p.fold_q && ((A0.mem[qq] >> jj) & 1u) && idx <= A0.L - p.fold_q + jj;
-          const uint32_t mj = __ballot_sync(0xffffffffu, use);
-          if (lane == 0) sm->maskq[b][q][jj] = mj;
-        }
-      }
-    }
-    __syncwarp();
-    // (testing aid: withholding tile 1's table makes the waits on it expire)
-    if (lane == 0 && !(p.withhold && k == 1)) mbar_arrive(&sm->rows_full);
-    A0 = A1;
-    A1 = A2;
-    pg0[0] = pg1[0];
-    pg0[1] = pg1[1];
-  }
-}
-
 // Refill the ring buffer of quarter q with the 32 rows of tile k (8 gather4 copies, lanes 0..7),
 // once the producer has resolved them. Returns false on timeout/abort.
 template <int kFmt>
@@ -344,43 +181,23 @@ __device__ __forceinline__ bool issue_stage(const DecodeParams& p, Smem* sm, uin
   using F = RowFmt<kFmt>;
   bool good = true;
   if (lane == 0) {
-    good = wait(sm, &sm->rows_full, (uint32_t)(k & 1), p.status);
+    good = wait(sm, &sm->rows_full[0], (uint32_t)(k & 1), p.status);
     if (good) mbar_arrive_expect_tx(&sm->ring_full[q], (uint32_t)F::kStageBytes);
   }
   good = __shfl_sync(0xffffffffu, good, 0);
   if (!good) return false;
   if (lane < 8) {
-    const int4 r = *reinterpret_cast<const int4*>(&sm->rowbuf[q * 32 + 4 * lane]);
+    const int4 r = *reinterpret_cast<const int4*>(&sm->rowbuf[0][q * 32 + 4 * lane]);
     gather4(ring + (q % F::kBufs) * F::kStageBytes + lane * 4 * F::kBytes, &p.cache_map, r.x, r.y, r.z, r.w,
             &sm->ring_full[q]);
   }
   __syncwarp();   // every lane has read its row numbers before the table is released
-  if (lane == 0) mbar_arrive(&sm->rows_empty);
+  if (lane == 0) mbar_arrive(&sm->rows_empty[0]);
   return true;
 }
 
 // ------------------------------------------------------------------ dequant
 // Thread = one tile row (token). half 0: latent dims 0..255; half 1: dims 256..511 + rope.
-// One group = 64 values (32 nibble bytes) sharing four block scales (sw). Ring rows are 352 B
-// apart, so the 16-byte loads see two-way bank conflicts; undoing a lane-dependent load order
-// would cost more ALU work than the conflicts cost (the pass is bound by its conversions).
-__device__ __forceinline__ void convert_group(const uint8_t* rowp, int g, uint32_t sw, uint32_t (&r)[32]) {
-  const uint4 n0 = *reinterpret_cast<const uint4*>(rowp + 32 * g);
-  const uint4 n1 = *reinterpret_cast<const uint4*>(rowp + 32 * g + 16);
-  const uint32_t w[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
-#pragma unroll
-  for (int bb = 0; bb < 4; ++bb) {
-    const uint32_t s2 = e4m3x2_to_f16x2(__byte_perm(sw, 0, bb * 0x11));   // (scale, scale)
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      uint32_t c[4];
-      e2m1x8_to_f16x2x4(w[2 * bb + h], c);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) r[8 * bb + 4 * h + i] = hmul2(c[i], s2);
-    }
-  }
-}
-
 // FP8 rows: 64 E4M3 bytes -> 32 fp16 pairs (exact). Rows are 576 B apart, so the 16-byte loads of a
 // quarter-warp meet four-way bank conflicts; the comparison path keeps the simple layout.
 __device__ __forceinline__ void convert_fp8_64(const uint8_t* src, uint32_t (&r)[32]) {
@@ -676,33 +493,6 @@ __device__ void mma_loop(const DecodeParams& p, Smem* sm, uint8_t* vtile, uint8_
 }
 
 // ------------------------------------------------------------------ softmax / epilogue
-// Maximum of v over the 32 lanes of the warp (every lane gets it).
-__device__ __forceinline__ float redux_max(float v) {
-  float r;
-  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
-  return r;
-}
-
-// Transpose-reduce 32 values across a warp: afterwards lane l holds the reduction
-// (over the 32 lanes) of element l. op: 0 = max, 1 = sum.
-template <int OP>
-__device__ __forceinline__ float warp_transpose_reduce(float (&v)[32]) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int s = 16; s >= 1; s >>= 1) {
-    const bool upper = (lane & s) != 0;
-#pragma unroll
-    for (int i = 0; i < s; ++i) {
-      // keep half [i] (lower) or [i+s] (upper); send the other half
-      const float send = upper ? v[i] : v[i + s];
-      const float keep = upper ? v[i + s] : v[i];
-      const float got = __shfl_xor_sync(0xffffffffu, send, s);
-      v[i] = OP == 0 ? fmaxf(keep, got) : keep + got;
-    }
-  }
-  return v[0];
-}
-
 // Scores of this thread's tile row: S = S_a + S_b (the two issuers' halves of the 576-wide
 // contraction), loaded one after the other into the same registers; unusable rows become -inf.
 template <int NH>
@@ -722,15 +512,6 @@ __device__ __forceinline__ void load_scores(uint32_t taddr, bool valid, float qs
   for (int h = 0; h < 32; ++h) z[h] = (h < NH && valid) ? (z[h] + __uint_as_float(ra[h])) * qscale : kNegInf;
 }
 
-// Softmax group: thread t owns tile row t (a token) and all heads. The reference m of each head
-// (the "running max") is kept lazily: it is raised only when a score exceeds it by more than
-// kLazy = 15 (log2 units), so most tiles need one group vote instead of a max reduction, and
-// P = 2^(z - m) stays <= 2^15, inside the fp16 range. When raised it is set to the tile's maximum
-// (no headroom), so P keeps fp16's whole range below it: weights down to 2^-24 of the maximum's
-// are represented, and the mass lost below that is at most topk * 2^-25 of the total. (A reference
-// set above the maximum would cut the raises but move the underflow threshold up with it: with 8
-// units of headroom, 2,047 tokens 17 units below a dominant one lost 1.5 % of the mass.)
-constexpr float kLazy = 15.f;
 // Returns false when the group gave up (abort); every thread of the group returns the same value.
 // kFmt 2 (per-token FP8 rows, k = scale_t * k'): the score of row t is scale_t times the UMMA's
 // q . k'_t, and PV must weight v'_t by p_t * scale_t. The softmax keeps its reference on the shifted
@@ -1091,8 +872,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       mbar_init(&sm->ring_full[i], 1);
       sm->stage_cnt[i] = 0;
     }
-    mbar_init(&sm->rows_full, 2);
-    mbar_init(&sm->rows_empty, 4);
+    mbar_init(&sm->rows_full[0], 2);
+    mbar_init(&sm->rows_empty[0], 4);
     for (int h = 0; h < 2; ++h) {
       for (int i = 0; i < 4; ++i) mbar_init(&sm->vfree[h][i], 1);
       mbar_init(&sm->kv_ready[h], 4);
@@ -1132,7 +913,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     }
   }
   if (warp == 0 || warp == 3) {
-    producer_loop<kFold>(p, sm, t_begin, t_end, warp == 0 ? 0 : 1);
+    producer_loop<kFold, 2, 1>(p, sm, t_begin, t_end, warp == 0 ? 0 : 1);
   } else if (warp == 1 || warp == 2) {
     if ((threadIdx.x & 31) == 0) mma_loop<NH, kCluster>(p, sm, vtile, qs, ps, t_begin, t_end, warp - 1);
     __syncwarp();
@@ -1394,7 +1175,8 @@ static cudaLaunchAttribute cluster_attr(int g) {
 }
 
 // Stream-K: q prep (ordinary launch) -> decode (PDL) -> merge (PDL): each dependent grid is
-// launched early and waits with griddepcontrol.wait before reading its inputs.
+// launched early and waits with griddepcontrol.wait before reading its inputs. The pair schedule
+// runs the same three grids with the pair decode grid in the middle.
 // Cluster mode: the decode grid alone (q converted in-kernel, partials merged on chip).
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream) {
   cudaError_t err = set_attributes_once();
@@ -1415,6 +1197,7 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream) {
   if (h32) q_prep_kernel<32><<<(unsigned)p.units, 256, 0, stream>>>(p);
   else q_prep_kernel<16><<<(unsigned)p.units, 256, 0, stream>>>(p);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  if (p.pair) return launch_decode_pair(p, stream);   // decode_pair.cu
   const size_t smem = p.row_fmt == 1   ? (h32 ? decode_smem_bytes<32, 1>() : decode_smem_bytes<16, 1>())
                      : p.row_fmt == 2 ? (h32 ? decode_smem_bytes<32, 2>() : decode_smem_bytes<16, 2>())
                                       : (h32 ? decode_smem_bytes<32>() : decode_smem_bytes<16>());

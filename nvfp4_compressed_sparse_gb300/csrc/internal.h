@@ -34,12 +34,14 @@ struct DecodeSchedule {
   int ctas;                // grid size
   int64_t partial_slots;   // stream-K: ctas + units - 1
   int cluster;             // 0 = stream-K, else CTAs per unit
+  int pair;                // 1 = stream-K over pairs: ctas ranges, each run by a 2-CTA cluster (one K half per CTA)
 };
 
 // kClusterNone: stream-K split only; kClusterDefault: the policy without flags (the split, measured
 // faster); kClusterBalanced: the cluster schedule wherever it is as balanced as the split;
-// kClusterAny: whenever one wave of clusters fits.
-enum ClusterPolicy { kClusterNone, kClusterDefault, kClusterBalanced, kClusterAny };
+// kClusterAny: whenever one wave of clusters fits. kPairSplit: stream-K over SMs / 2 ranges, each run
+// by a 2-CTA cluster whose CTAs hold one half of the 576-wide contraction each.
+enum ClusterPolicy { kClusterNone, kClusterDefault, kClusterBalanced, kClusterAny, kPairSplit };
 DecodeSchedule make_schedule(int B, int Q, int H, int topk, int num_sms, int max_ctas, ClusterPolicy policy);
 size_t workspace_bytes_for(const DecodeSchedule& s, int H);
 
@@ -69,6 +71,7 @@ struct DecodeParams {
   int64_t units, total_tiles;
   int tiles_per_unit, ctas;
   int cluster;                // 0 = stream-K split, else CTAs per unit (one cluster per unit)
+  int pair;                   // 1 = the split run by 2-CTA clusters: ctas = ranges (pairs), 2 * ctas CTAs
   uint32_t withhold;          // testing aid: 1 = the producers never publish tile 1's row table
   // Folded queries (sparse_mla_decode_shared): the kernel runs Q = 1 with H = fold_q * fold_h heads, the
   // fold_q query tokens of a request sharing one index list; fold_member[b * topk + e] bit j says whether
@@ -94,6 +97,8 @@ cudaError_t launch_stage(const uint8_t* cache, int64_t num_pages, const int32_t*
                          cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);
 int max_active_clusters(int heads_per_cta, int cluster);   // clusters of the decode grid that fit at once
+cudaError_t launch_decode_pair(const DecodeParams& p, cudaStream_t stream);   // the pair grid alone
+int max_active_pairs(int heads_per_cta);                    // pairs of the pair grid that fit at once
 cudaError_t launch_merge(const DecodeParams& p, cudaStream_t stream);
 
 cudaError_t launch_topk(const float* logits, int64_t stride, const int32_t* seq_lens, int B, int Q, int K,

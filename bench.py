@@ -20,7 +20,7 @@ events on the launching stream. The JSON line also carries:
                rows and index lists): one thread, and one process per host core
   configs      the decode-shard (B=16), spec-verify (192K-row pack + Q=4 decode in
                one step) and capacity (1.63M-token pool) cases, device-timed
-  schedules    split vs cluster schedule for B = 1, 4, 16, 64 (headline requests)
+  schedules    split vs cluster vs pair schedule for B = 1, 4, 16, 64 (headline requests)
   pack         mla_kv_pack of one 1M-row chunk of the cache fill (mean of 10 calls,
                L2 flushed before each), for context
 --impl reference times the CPU oracle as the reference arm: every step runs all 64
@@ -530,8 +530,8 @@ def topk_table(m, case, cache, dev, stream, flush, hbm, steps):
 
 
 def schedule_table(m, workloads, case, cache, dev, stream, flush, steps):
-    """Split vs cluster schedule (forced wherever one wave of clusters fits) for the first B requests
-    of the headline case; cluster_size 0 = no wave of clusters fits."""
+    """Split vs cluster schedule (forced wherever one wave of clusters fits) vs pair schedule for the
+    first B requests of the headline case; cluster_size 0 = no wave of clusters fits."""
     import copy
     res = []
     for B in (1, 4, 16, 64):
@@ -549,6 +549,11 @@ def schedule_table(m, workloads, case, cache, dev, stream, flush, steps):
             cl_ms, _ = time_decode(m, c, cache, inputs, stream, flush, steps, 5, cluster="any")
             row["cluster_us"] = cl_ms * 1e3
             row["cluster_ctas"] = ctas
+        pair_ctas, pair_g = m.sparse_mla_decode_plan(c.B, c.Q, c.H, c.topk, cluster="pair")
+        if pair_g == -2:
+            pair_ms, _ = time_decode(m, c, cache, inputs, stream, flush, steps, 5, cluster="pair")
+            row["pair_us"] = pair_ms * 1e3
+            row["pair_ctas"] = pair_ctas
         res.append(row)
     return res
 

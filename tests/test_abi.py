@@ -144,3 +144,12 @@ def test_comparison_path_host_checks(lib):
                                        kw.get("K", 8), V(A), None)
     assert tk(B=0) == 1 and tk(Q=17) == 1 and tk(K=0) == 1 and tk(K=9000) == 1 and tk(S=0) == 1
     assert tk(S=62) == 2 and tk(lg=A + 4) == 2
+
+
+def test_binding_flag_constants_match_the_header():
+    """The binding's schedule and testing flags are the header's bit values."""
+    text = open(os.path.join(ROOT, "include", "nvfp4mla.h")).read()
+    found = dict(re.findall(r"#define NVFP4MLA_FLAG_(\w+) \(1u << (\d+)\)", text))
+    assert set(found) == {"TEST_TIMEOUT", "CLUSTER", "CLUSTER_ANY", "SPLIT", "PAIR"}
+    for name, bit in found.items():
+        assert getattr(m, "FLAG_" + name) == 1 << int(bit), name

@@ -525,7 +525,7 @@ def topk_table(m, case, cache, dev, stream, flush, hbm, steps):
     res.update({"rows": case.B * case.Q, "topk": case.topk, "logits": "N(0,1) fp32, seeded",
                 "algorithmic_bytes": nbytes, "achieved_gbs": nbytes / t / 1e9,
                 "frac_of_measured_hbm": nbytes / t / 1e9 / hbm,
-                "launches": "one CTA per query row (64 of the SMs)"})
+                "launches": "one 2-CTA cluster per query row (128 of the SMs; min(8, SMs / rows) CTAs per row)"})
     return res
 
 
@@ -582,14 +582,16 @@ def run_gpu(args, world, rank, local):
                      dtype=torch.uint8, device=dev)
     status = torch.zeros(4, dtype=torch.int32, device=dev)
 
-    plan_ctas, plan_cluster = m.sparse_mla_decode_plan(case.B, case.Q, case.H, case.topk)
+    schedule = {"default": None, "split": False, "pair": "pair"}[args.schedule]
+    plan_ctas, plan_cluster = m.sparse_mla_decode_plan(case.B, case.Q, case.H, case.topk, cluster=schedule)
     launches_per_step = 1 if plan_cluster > 0 else 3
     timed_unit = ("sparse_mla_decode call (one cluster-mode decode kernel)" if plan_cluster > 0 else
+                  "sparse_mla_decode call (q prep + pair decode + merge kernels)" if plan_cluster == -2 else
                   "sparse_mla_decode call (q prep + decode + merge kernels)")
 
     def step():
         m.sparse_mla_decode(q, cache, pt, tk, sl, case.softmax_scale, out=out, lse=lse, workspace=ws,
-                            dev_status=status, stream=stream)
+                            dev_status=status, stream=stream, cluster=schedule)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -668,11 +670,13 @@ def run_gpu(args, world, rank, local):
         "throughput_query_tokens_per_s": world * case.B * case.Q / t_s,
         "median_us_per_step": statistics.median(times_ms) * 1000.0,
         "roofline": {"bound": "hbm" if roof_hbm_us >= roof_tc_us else "tensor", "achieved": achieved, "peak": hbm,
-                     "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic_from_profile(),
+                     "unit": "GB/s", "frac": achieved / hbm,
+                     "traffic": traffic_from_profile() if plan_cluster != -2 else None,
                      "peak_kind": peak_kind, "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
                      "algorithmic_bytes": nbytes, "algorithmic_flops": flops,
                      "roofline_us": max(roof_hbm_us, roof_tc_us), "tensor_roofline_us": roof_tc_us,
-                     "timed_unit": timed_unit, "decode_ctas": plan_ctas, "cluster": plan_cluster},
+                     "timed_unit": timed_unit, "decode_ctas": plan_ctas, "cluster": plan_cluster,
+                     "schedule": args.schedule},
         "e2e": {"value": e2e_ms * 1000.0, "unit": "us/step", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "transfer": "kernels read q / page table / index lists / lengths from pinned host memory and write "
                             "out + LSE to pinned host memory (NVLink-C2C), inside each timed step",
@@ -705,6 +709,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="skip the extra cases and the schedule table")
+    ap.add_argument("--schedule", default="default", choices=["default", "split", "pair"],
+                    help="decode schedule of the timed step (default: the library's; pair: NVFP4MLA_FLAG_PAIR). "
+                         "The end-to-end leg, with results in host memory, always runs the split schedule.")
     ap.add_argument("--case", default="2", choices=["0", "1", "2", "3", "3s", "4"],
                     help="workload of the timed line (default 2, the headline; the others for profiling, "
                          "without the extra tables)")

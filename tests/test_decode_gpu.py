@@ -323,3 +323,28 @@ def test_cluster_any_schedule_matches_oracle(spec):
                                                case.seq_lens, case.softmax_scale)
     out, lse = _decode(case, cache, cluster="any")
     assert_close(out, lse, ref_out, ref_lse, f"cluster any G={g} {spec}")
+
+
+@pytest.mark.parametrize("spec,kw", [
+    (dict(B=2, Q=1, H=32, topk=8192, L=(20000, 12000)), {}),                 # the largest index list: 64 tiles
+    (dict(B=2, Q=1, H=32, topk=8192, L=(20000, 12000)), dict(cluster="pair")),
+    (dict(B=1, Q=16, H=128, topk=300, L=(5000,)), {}),                       # the most query tokens, 4 head groups
+    (dict(B=2, Q=16, H=32, topk=2048, L=(9000, 3000)), dict(max_ctas=5)),   # 16 causal ranges per request
+], ids=["K8192", "K8192-pair", "Q16H128", "Q16-5ctas"])
+def test_maximum_sizes_match_oracle(spec, kw):
+    """The limits the C ABI accepts: top-k = NVFP4MLA_MAX_TOPK and Q = 16 query tokens per request."""
+    case = workloads.small_case(seed=900 + spec["Q"] + spec["topk"], **spec)
+    lat, rope, rows = _host_cache(case)
+    cache = _gpu_cache(lat, rope, case.num_pages)
+    status = torch.zeros(4, dtype=torch.int32, device="cuda")
+    out, lse = _decode(case, cache, dev_status=status, **kw)
+    ref_out, ref_lse = attention.sparse_decode(case.q_bits, rows, case.page_table, case.topk_indices,
+                                               case.seq_lens, case.softmax_scale)
+    assert_close(out, lse, ref_out, ref_lse, f"{spec} {kw}")
+    bad = 0
+    for b in range(case.B):
+        L = int(case.seq_lens[b])
+        for j in range(case.Q):
+            tk = case.topk_indices[b, j]
+            bad += int(np.sum((tk != -1) & ((tk < 0) | (tk >= L) | (tk > L - case.Q + j))))
+    assert status.cpu().tolist()[0] == bad and status.cpu().tolist()[1:] == [0, 0, 0]

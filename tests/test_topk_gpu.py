@@ -19,7 +19,7 @@ def _run(logits, L, Q, K):
 
 
 @pytest.mark.parametrize("B,Q,S,K", [(3, 1, 1000, 64), (2, 4, 20000, 2048), (4, 2, 9000, 100), (1, 1, 64, 2048),
-                                     (2, 3, 40000, 8192), (5, 1, 8, 3)])
+                                     (2, 3, 40000, 8192), (5, 1, 8, 3), (2, 16, 6000, 300), (1, 16, 30000, 8192)])
 def test_random_rows_with_ties_nan_and_signed_zero(B, Q, S, K):
     rng = np.random.default_rng(B * 1000 + S)
     logits = rng.standard_normal((B, Q, S)).astype(np.float32)

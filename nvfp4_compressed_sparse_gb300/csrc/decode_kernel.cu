@@ -16,8 +16,8 @@
 //    K tile in TMEM (pass A: the A operand of the QK UMMA) and later copy its
 //    latent part from TMEM into the V tile in shared memory (pass B: the A
 //    operand of PV, read MN-major).
-//  * The 576 K columns are split into two halves (latent 0..255; latent
-//    256..511 + rope), each with its own dequant warps, MMA issuer, and
+//  * The 576 K columns are split into two halves (latent 0..255 + rope 0..31;
+//    latent 256..511 + rope 32..63), each with its own dequant warps, MMA issuer, and
 //    barriers, so the halves pipeline independently and meet only in the
 //    softmax group (which adds the two partial score accumulators).
 //  * Four softmax warps keep a lazily raised running max per head, write P
@@ -74,7 +74,7 @@ struct alignas(16) Smem {
   uint64_t ring_full[kRingStages];   // gathered rows of a 32-row stage have landed
   uint64_t rows_full[1];             // row numbers + masks of a tile resolved (2 producer warps)
   uint64_t rows_empty[1];            // every stage of that tile has been requested (4 issuing warps)
-  // Half h of a tile = latent dims 256h..256h+255 (half 1 also carries the rope dims). Each half has
+  // Half h of a tile = latent dims 256h..256h+255 and rope dims 32h..32h+31. Each half has
   // its own dequant warps and MMA issuer, so the two halves pipeline independently and only meet
   // in the softmax.
   uint64_t vfree[2][4];              // PV of half h has finished reading V rows 32w..32w+31 (1 commit)
@@ -197,7 +197,7 @@ __device__ __forceinline__ bool issue_stage(const DecodeParams& p, Smem* sm, uin
 }
 
 // ------------------------------------------------------------------ dequant
-// Thread = one tile row (token). half 0: latent dims 0..255; half 1: dims 256..511 + rope.
+// Thread = one tile row (token). Half h: latent dims 256h..256h+255 and rope dims 32h..32h+31.
 // FP8 rows: 64 E4M3 bytes -> 32 fp16 pairs (exact). Rows are 576 B apart, so the 16-byte loads of a
 // quarter-warp meet four-way bank conflicts; the comparison path keeps the simple layout.
 __device__ __forceinline__ void convert_fp8_64(const uint8_t* src, uint32_t (&r)[32]) {
@@ -277,24 +277,38 @@ __device__ void dequant_loop(const DecodeParams& p, Smem* sm, uint8_t* ring, uin
         tmem_st32(tmem_row + kTmemK + 32 * grp, r);
       }
     }
-    if (half == 1) {
+    {
+      // rope dims 32 half .. 32 half + 31 -> K columns 256 + 16 half (each half converts 32 of the 64
+      // rope dims, so both halves convert 288 dims and issue 18 QK steps)
+      uint32_t rr[16];
       if constexpr (kFmt == 2) {
         // bf16 rope / scale -> fp16 (exact for values in fp16's normal range)
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint4 v = *reinterpret_cast<const uint4*>(rowp + kTokRopeOff + 16 * c);
+        for (int c = 0; c < 4; ++c) {
+          const uint4 v = *reinterpret_cast<const uint4*>(rowp + kTokRopeOff + 64 * half + 16 * c);
           const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const __half2 h2 = __floats2half2_rn(__uint_as_float(w4[i] << 16), __uint_as_float(w4[i] & 0xFFFF0000u));
-            r[4 * c + i] = *reinterpret_cast<const uint32_t*>(&h2);
+            rr[4 * c + i] = *reinterpret_cast<const uint32_t*>(&h2);
           }
         }
       } else {
-        convert_fp8_64(rowp + (kFmt == 0 ? kRopeOff : kLatent), r);   // the rope bytes are E4M3 in both formats
+        // the rope bytes are E4M3 in both formats
+        const uint8_t* src = rowp + (kFmt == 0 ? kRopeOff : kLatent) + 32 * half;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const uint4 v = *reinterpret_cast<const uint4*>(src + 16 * c);
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            rr[8 * c + 2 * i] = e4m3x2_to_f16x2(w[i] & 0xFFFFu);
+            rr[8 * c + 2 * i + 1] = e4m3x2_to_f16x2(w[i] >> 16);
+          }
+        }
       }
       __syncwarp();
-      tmem_st32(tmem_row + kTmemK + 256, r);
+      tmem_st16(tmem_row + kTmemK + 256 + 16 * half, rr);
     }
     tmem_wait_st();
     tc_fence_before();
@@ -379,7 +393,8 @@ struct MmaIssuer {
   uint8_t* q_smem;
 
   // Copy this half's part of the unit's pre-converted q image (atoms 0..3 for half 0, 4..8 for
-  // half 1: exactly the K-steps this issuer's QK reads) into the shared q buffer.
+  // half 1; issuer 0's QK also reads the rope atom 8, which issuer 1 copies) into the shared q
+  // buffer.
   __device__ __forceinline__ void request_q(int64_t unit) {
     const uint32_t atom_bytes = (uint32_t)NH * 128u;
     const uint32_t off = which == 0 ? 0u : 4u * atom_bytes;
@@ -406,13 +421,11 @@ struct MmaIssuer {
   }
   __device__ __forceinline__ void qk(int64_t k) {
     tc_fence_after();
-    if (which == 0) {
+    // half h: latent dims 256h..256h+255, then rope dims 32h..32h+31 (K-steps 32 + 2h, 33 + 2h)
 #pragma unroll
-      for (int x = 0; x < 16; ++x) qk_step(x, x > 0 ? 1u : 0u);          // latent dims 0..255
-    } else {
-#pragma unroll
-      for (int x = 0; x < 20; ++x) qk_step(16 + x, x > 0 ? 1u : 0u);     // latent 256..511, rope
-    }
+    for (int x = 0; x < 16; ++x) qk_step(16 * which + x, x > 0 ? 1u : 0u);
+    qk_step(32 + 2 * which, 1u);
+    qk_step(33 + 2 * which, 1u);
     umma_commit(&sm->kfree[which]);
     umma_commit(&sm->s_full);
   }
@@ -465,7 +478,9 @@ __device__ void mma_loop(const DecodeParams& p, Smem* sm, uint8_t* vtile, uint8_
     const TileInfo ti = tile_info(p, t_begin + k, t_begin, t_end);
     // ---- QK(k)
     bool ok = true;
+    // issuer 0 also reads the rope atom of the q image, which issuer 1 copies in
     if (ti.first) ok = wait(sm, &sm->q_full[which], (uint32_t)((q_copies - 1) & 1), p.status);
+    if (ok && ti.first && which == 0) ok = wait(sm, &sm->q_full[1], (uint32_t)((q_copies - 1) & 1), p.status);
     if (ok) ok = wait(sm, &sm->kv_ready[which], (uint32_t)(k & 1), p.status);
     if (ok && k > 0) ok = wait(sm, &sm->s_free, (uint32_t)((k - 1) & 1), p.status);
     if (!ok) break;
@@ -474,6 +489,8 @@ __device__ void mma_loop(const DecodeParams& p, Smem* sm, uint8_t* vtile, uint8_
       const TileInfo tn = tile_info(p, t_begin + k + 1, t_begin, t_end);
       if (tn.first) {
         if (!wait(sm, &sm->kfree[which], (uint32_t)(k & 1), p.status)) break;
+        // the rope atom that issuer 1 rewrites is read by issuer 0's QK(k) too
+        if (which == 1 && !wait(sm, &sm->kfree[0], (uint32_t)(k & 1), p.status)) break;
         m.request_q(tn.unit);
         ++q_copies;
       }

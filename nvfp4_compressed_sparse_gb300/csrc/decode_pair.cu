@@ -12,7 +12,7 @@
 // Why two CTAs: in one CTA the fp16 K tile (288 TMEM columns), the V tile (128 KB of shared memory)
 // and the one-tile ring of gathered rows fill TMEM and shared memory, so every buffer is single and
 // the stages of consecutive tiles wait on each other. CTA h of a pair holds only half h (latent dims
-// 256h..256h+255; half 1 also the rope dims): half the K tile, half the V tile, half the q image and
+// 256h..256h+255 and rope dims 32h..32h+31): half the K tile, half the V tile, half the q image and
 // half of the O accumulator. The room this frees double-buffers K and S in TMEM and deepens the ring
 // to two tiles, and leaves the TMEM for a PV of N = 2 NH. The price is one exchange per tile: the
 // two partial score tiles (QK over each half) are added in both CTAs, each sending its 128 x NH fp32
@@ -42,8 +42,8 @@ constexpr int kPairStages = 8;                          // ring: two tiles x fou
 constexpr int kPairStageBytes = 32 * kRowBytes;         // 11264 (88 x 128 B)
 constexpr int kPairRingBytes = kPairStages * kPairStageBytes;
 constexpr int kPairVBytes = 4 * 128 * 128;              // the half's 256 latent dims: 4 SW128 atoms x 128 rows
-constexpr int kPairQAtoms = 5;                          // q image atoms of a half (half 1: latent 256..511 + rope)
-constexpr int kPairKCols = 160;                         // one K buffer: 128 latent + 32 rope columns
+constexpr int kPairQAtoms = 5;                          // q image atoms of a half: its 4 latent atoms + the rope atom
+constexpr int kPairKCols = 160;                         // one K buffer: 128 latent + 16 rope columns (+ 16 spare)
 constexpr int kPairTmemS = 2 * kPairKCols;              // two S buffers (NH columns each), then O^T: 2 M-blocks
                                                         // of [O_hi | O_lo] (2 NH columns each)
 constexpr uint32_t kPairTmemCols = 512;
@@ -135,7 +135,7 @@ __device__ __forceinline__ bool pair_issue_stage(const DecodeParams& p, PairSmem
 
 // ---------------------------------------------------------------- dequant
 // Warp (q, s): tile rows 32q..32q+31 (TMEM lane quarter q), the half's 64-dim groups 2s and 2s+1
-// and (half 1) rope dims 32s..32s+31. Pass A converts the rows into K buffer k % 2 of TMEM; pass B
+// and rope dims 32 half + 16s .. + 15. Pass A converts the rows into K buffer k % 2 of TMEM; pass B
 // copies the latent part of K into the V tile once PV of the previous tile is done with those rows.
 // Pass A runs one tile ahead of pass B (A(k+1) before B(k)): K is double-buffered, so converting the
 // next tile does not wait for the softmax and PV of the current one.
@@ -177,21 +177,19 @@ __device__ void pair_dequant(const DecodeParams& p, PairSmem* sm, uint8_t* ring,
       __syncwarp();
       tmem_st32(tmem_row + kcol + 32 * l, r);
     }
-    if (half == 1) {
-      // rope dims 32s..32s+31: 32 E4M3 bytes -> 16 fp16 pairs
-      uint32_t rr[16];
+    {
+      // rope dims 32 half + 16 s .. + 15 (the half's 32 rope dims, 16 per sub-half): 16 E4M3 bytes
+      // -> 8 fp16 pairs, K columns 128 + 8 s
+      const uint4 v = *reinterpret_cast<const uint4*>(rowp + kRopeOff + 32 * half + 16 * s);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      uint32_t rr[8];
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const uint4 v = *reinterpret_cast<const uint4*>(rowp + kRopeOff + 32 * s + 16 * c);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          rr[8 * c + 2 * i] = e4m3x2_to_f16x2(w[i] & 0xFFFFu);
-          rr[8 * c + 2 * i + 1] = e4m3x2_to_f16x2(w[i] >> 16);
-        }
+      for (int i = 0; i < 4; ++i) {
+        rr[2 * i] = e4m3x2_to_f16x2(w[i] & 0xFFFFu);
+        rr[2 * i + 1] = e4m3x2_to_f16x2(w[i] >> 16);
       }
       __syncwarp();
-      tmem_st16(tmem_row + kcol + 128 + 16 * s, rr);
+      tmem_st8(tmem_row + kcol + 128 + 8 * s, rr);
     }
     tmem_wait_st();
     tc_fence_before();
@@ -245,8 +243,8 @@ __device__ void pair_dequant(const DecodeParams& p, PairSmem* sm, uint8_t* ring,
 
 // ---------------------------------------------------------------- MMA issue
 // Two issuing threads per CTA (a single thread issuing every UMMA of a tile was the step that set
-// the pace): warp 1 issues QK(k) = K half x q half into S buffer k % 2 (16 UMMAs of K = 16 for
-// half 0, 20 for half 1), warp 2 issues PV(k): for each of the half's two 128-dim M-blocks, the V
+// the pace): warp 1 issues QK(k) = K half x q half into S buffer k % 2 (18 UMMAs of K = 16),
+// warp 2 issues PV(k): for each of the half's two 128-dim M-blocks, the V
 // rows times [P_hi | P_lo] (N = 2 NH) into [O_hi | O_lo], which the epilogue adds. One UMMA thus
 // reads each V block once for both parts of P (the split kernel, with no TMEM left for a second
 // O, reads it twice), halving the PV UMMAs and their shared-memory reads. When a tile starts a new
@@ -258,13 +256,14 @@ __device__ void pair_qk_issuer(const DecodeParams& p, PairSmem* sm, uint8_t* qs,
   constexpr uint32_t kAtom = (uint32_t)NH * 128u;
   const uint32_t tmem = sm->tmem_base;
   const uint64_t qd = sdesc(smem_u32(qs), 16, 1024, SW_128B);
-  const int nks = half ? 20 : 16;
   const int64_t n = t_end - t_begin;
   int64_t q_copies = 0;
+  // this half's q atoms: latent atoms 4 half .. 4 half + 3, then the rope atom 8
   auto request_q = [&](int64_t unit) {
-    const uint32_t bytes = (half ? 5u : 4u) * kAtom;
-    mbar_arrive_expect_tx(&sm->q_full, bytes);
-    bulk_g2s(qs, p.q16 + unit * (int64_t)(9u * kAtom) + 4u * half * kAtom, bytes, &sm->q_full);
+    const uint8_t* src = p.q16 + unit * (int64_t)(9u * kAtom);
+    mbar_arrive_expect_tx(&sm->q_full, 5u * kAtom);
+    bulk_g2s(qs, src + 4u * half * kAtom, 4u * kAtom, &sm->q_full);
+    bulk_g2s(qs + 4u * kAtom, src + 8u * kAtom, kAtom, &sm->q_full);
     ++q_copies;
   };
   if (n > 0) asm volatile("griddepcontrol.wait;" ::: "memory");   // q16 comes from the prep grid
@@ -285,11 +284,12 @@ __device__ void pair_qk_issuer(const DecodeParams& p, PairSmem* sm, uint8_t* qs,
     tc_fence_after();
     const uint32_t s_col = tmem + kPairTmemS + (uint32_t)(k & 1) * NH;
     const uint32_t kcol = tmem + (uint32_t)((k & 1) * kPairKCols);
+    // latent dims 256 half .. + 255 (K-steps 16 half + x), then rope dims 32 half .. + 31 (K-steps
+    // 32 + 2 half, 33 + 2 half): the split kernel's steps of this half, in its order
 #pragma unroll
-    for (int x = 0; x < 20; ++x) {
-      if (x >= nks) break;
-      const int ks = 16 * half + x;                        // K-step of the full contraction
-      const int atom = (ks >> 2) - 4 * half;               // atom within this half's q image
+    for (int x = 0; x < 18; ++x) {
+      const int ks = x < 16 ? 16 * half + x : 32 + 2 * half + (x - 16);   // K-step of the full contraction
+      const int atom = x < 16 ? (x >> 2) : 4;                              // atom within this half's q image
       const uint64_t bq = qd + (uint64_t)(((uint32_t)atom * kAtom + (ks & 3) * 32) >> 4);
       umma_ts(s_col, kcol + 8 * x, bq, kIdQK, x > 0 ? 1u : 0u);
     }

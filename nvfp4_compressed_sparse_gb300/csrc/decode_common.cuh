@@ -59,6 +59,20 @@ __device__ __forceinline__ bool named_sync_softmax_any(bool v) {
   return r != 0;
 }
 
+// Stream-K ranges: the tiles of all units, cut into p.ctas contiguous ranges (CTAs, or pairs of
+// CTAs), the first total_tiles % ctas of them one tile longer. The ranges launched last are the
+// ones that can start late (on SMs the q-prep grid still holds), so they get the shorter shares.
+__device__ __forceinline__ int64_t range_begin(const DecodeParams& p, int64_t r) {
+  const int64_t base = p.total_tiles / p.ctas, extra = p.total_tiles % p.ctas;
+  return r * base + (r < extra ? r : extra);
+}
+// The range that holds tile g.
+__device__ __forceinline__ int64_t range_of_tile(const DecodeParams& p, int64_t g) {
+  const int64_t base = p.total_tiles / p.ctas, extra = p.total_tiles % p.ctas;
+  const int64_t split = extra * (base + 1);
+  return g < split ? g / (base + 1) : extra + (g - split) / base;
+}
+
 // Unit decomposition: virtual unit -> (b, j, head group)
 __device__ __forceinline__ void split_unit(const DecodeParams& p, int64_t unit, int& b, int& j, int& hg) {
   hg = (int)(unit % p.head_groups);

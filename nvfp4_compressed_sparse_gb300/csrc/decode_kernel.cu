@@ -117,11 +117,12 @@ struct ClusterScratch {
 // q (bf16) of one (query, head group) -> FP16 scaled by 2^e so that max|q| * 2^e lies in
 // [2^14, 2^15), written as the exact shared-memory image the decode CTA uses as the UMMA B operand
 // (K-major, 128-byte swizzle: 9 atoms of NH rows x 128 B) at dst (global or shared memory).
-// Threads tid = 0..kNT-1 take part; the maximum goes through wmax[kNT / 32] and barrier kBar
-// (0: __syncthreads, else named barrier kBar over kNT threads). Every thread returns the unit's
+// Threads tid = 0..kNT-1 take part; the maximum goes through wmax[kNT / 32] and barrier bar
+// (0: __syncthreads, else named barrier bar over kNT threads). Every thread returns the unit's
 // qscale = softmax_scale * log2(e) * 2^-e. All loads are issued before any is used.
-template <int NH, int kNT, int kBar>
-__device__ __forceinline__ float q_image(const DecodeParams& p, int64_t unit, int tid, uint8_t* dst, float* wmax) {
+template <int NH, int kNT>
+__device__ __forceinline__ float q_image(const DecodeParams& p, int64_t unit, int tid, uint8_t* dst, float* wmax,
+                                         int bar) {
   int b, j, hg;
   split_unit(p, unit, b, j, hg);
   const uint16_t* src = p.q + (((int64_t)b * p.Q + j) * p.H + (int64_t)hg * NH) * kQK;
@@ -144,8 +145,8 @@ __device__ __forceinline__ float q_image(const DecodeParams& p, int64_t unit, in
 #pragma unroll
   for (int s = 16; s >= 1; s >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, s));
   if ((tid & 31) == 0) wmax[tid >> 5] = mx;
-  if constexpr (kBar == 0) __syncthreads();
-  else asm volatile("bar.sync %0, %1;" ::"n"(kBar), "n"(kNT) : "memory");
+  if (bar == 0) __syncthreads();
+  else asm volatile("bar.sync %0, %1;" ::"r"(bar), "n"(kNT) : "memory");
   mx = wmax[0];
 #pragma unroll
   for (int i = 1; i < kNT / 32; ++i) mx = fmaxf(mx, wmax[i]);
@@ -880,8 +881,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     // Every decode CTA is resident once all of them reach this point, so letting the
     // merge grid be scheduled now cannot take resources a decode CTA still needs.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    t_begin = cta * p.total_tiles / p.ctas;
-    t_end = (cta + 1) * p.total_tiles / p.ctas;
+    t_begin = range_begin(p, cta);
+    t_end = range_begin(p, cta + 1);
   }
 
   if (threadIdx.x == 0) {
@@ -923,7 +924,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     // straight into the q buffer; the UMMAs read it through the async proxy once every writer
     // has arrived on q_full.
     if (warp >= 4) {
-      qscale = q_image<NH, 384, 2>(p, cta / p.cluster, threadIdx.x - 128, qs, sm->wmax);
+      qscale = q_image<NH, 384>(p, cta / p.cluster, threadIdx.x - 128, qs, sm->wmax, 2);
       fence_proxy_async_smem();
       mbar_arrive(&sm->q_full[0]);
       mbar_arrive(&sm->q_full[1]);
@@ -965,13 +966,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
 }
 
 // ------------------------------------------------------------------ q prep
-// Stream-K mode: one block per (query, head group) writes the unit's FP16 q image (see q_image)
-// and its qscale to the workspace, for the decode CTAs to copy.
+// Stream-K mode: each 256-thread group of a block writes one (query, head group) unit's FP16 q
+// image (see q_image) and its qscale to the workspace, for the decode CTAs to copy. Two units per
+// block: a decode CTA cannot share an SM with a prep block, so the fewer SMs the prep grid holds,
+// the fewer decode CTAs start late (those get the shorter stream-K shares).
+constexpr int kPrepUnitsPerBlock = 2;
 template <int NH>
-__global__ void __launch_bounds__(256) q_prep_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(256 * kPrepUnitsPerBlock) q_prep_kernel(const DecodeParams p) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  __shared__ float wmax[8];
-  const int64_t unit = blockIdx.x;
+  __shared__ float wmax[kPrepUnitsPerBlock][8];
+  const int grp = threadIdx.x >> 8, tid = threadIdx.x & 255;
+  const int64_t unit = (int64_t)blockIdx.x * kPrepUnitsPerBlock + grp;
+  if (unit >= p.units) return;   // a whole group (its named barrier is its own)
   int b, j, hg;
   split_unit(p, unit, b, j, hg);
   if (hg == 0) {
@@ -979,15 +985,15 @@ __global__ void __launch_bounds__(256) q_prep_kernel(const DecodeParams p) {
     // the decode grid resolves its first tiles from them while this grid runs.
     const char* tk = reinterpret_cast<const char*>(p.idx + ((int64_t)b * p.Q + j) * p.topk);
     const int64_t tk_bytes = (int64_t)p.topk * 4;
-    for (int64_t o = (int64_t)threadIdx.x * 128; o < tk_bytes; o += 256 * 128) prefetch_l2(tk + o);
+    for (int64_t o = (int64_t)tid * 128; o < tk_bytes; o += 256 * 128) prefetch_l2(tk + o);
     if (j == 0) {
       const char* pt = reinterpret_cast<const char*>(p.page_table + (int64_t)b * p.max_pages);
       const int64_t pt_bytes = p.max_pages * 4;
-      for (int64_t o = (int64_t)threadIdx.x * 128; o < pt_bytes; o += 256 * 128) prefetch_l2(pt + o);
+      for (int64_t o = (int64_t)tid * 128; o < pt_bytes; o += 256 * 128) prefetch_l2(pt + o);
     }
   }
-  const float qscale = q_image<NH, 256, 0>(p, unit, threadIdx.x, p.q16 + unit * (int64_t)(9 * NH * 128), wmax);
-  if (threadIdx.x == 0) p.qscale[unit] = qscale;
+  const float qscale = q_image<NH, 256>(p, unit, tid, p.q16 + unit * (int64_t)(9 * NH * 128), wmax[grp], 1 + grp);
+  if (tid == 0) p.qscale[unit] = qscale;
 }
 
 // ------------------------------------------------------------------ merge
@@ -1059,8 +1065,8 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeParams
   const int h = blockIdx.y * (kMergeThreads / 64) + (threadIdx.x >> 6);
   const int d8 = threadIdx.x & 63;                 // dims 8*d8 .. 8*d8+7
   const int64_t g0 = unit * p.tiles_per_unit, g1 = g0 + p.tiles_per_unit - 1;
-  const int64_t c_lo = ((g0 + 1) * p.ctas - 1) / p.total_tiles;
-  const int64_t c_hi = ((g1 + 1) * p.ctas - 1) / p.total_tiles;
+  const int64_t c_lo = range_of_tile(p, g0);
+  const int64_t c_hi = range_of_tile(p, g1);
   const int n = (int)(c_hi - c_lo + 1);   // CTAs (partial slots) that covered the unit
   const float kNegInf = __int_as_float(0xff800000);
   if constexpr (kPoll) {
@@ -1211,8 +1217,9 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream) {
     if (h32) return cudaLaunchKernelEx(&cfg, decode_kernel<32, true, false>, p);
     return cudaLaunchKernelEx(&cfg, decode_kernel<16, true, false>, p);
   }
-  if (h32) q_prep_kernel<32><<<(unsigned)p.units, 256, 0, stream>>>(p);
-  else q_prep_kernel<16><<<(unsigned)p.units, 256, 0, stream>>>(p);
+  const unsigned prep_blocks = (unsigned)((p.units + kPrepUnitsPerBlock - 1) / kPrepUnitsPerBlock);
+  if (h32) q_prep_kernel<32><<<prep_blocks, 256 * kPrepUnitsPerBlock, 0, stream>>>(p);
+  else q_prep_kernel<16><<<prep_blocks, 256 * kPrepUnitsPerBlock, 0, stream>>>(p);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   if (p.pair) return launch_decode_pair(p, stream);   // decode_pair.cu
   const size_t smem = p.row_fmt == 1   ? (h32 ? decode_smem_bytes<32, 1>() : decode_smem_bytes<16, 1>())

@@ -624,8 +624,8 @@ __global__ void __launch_bounds__(kPairThreads, 1) decode_pair_kernel(const __gr
   // Every decode CTA is resident once all of them reach this point, so letting the merge grid be
   // scheduled now cannot take resources a decode CTA still needs.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int64_t t_begin = pair * p.total_tiles / p.ctas;
-  const int64_t t_end = (pair + 1) * p.total_tiles / p.ctas;
+  const int64_t t_begin = range_begin(p, pair);
+  const int64_t t_end = range_begin(p, pair + 1);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kPairStages; ++i) {

@@ -416,17 +416,20 @@ struct MmaIssuer {
     pd0 = sdesc(smem_u32(ps), 4096, kPSbo, kPSw);
   }
 
-  __device__ __forceinline__ void qk_step(int ks, uint32_t acc) {
-    const uint64_t b = qd + (uint64_t)((((ks >> 2) * NH * 128) + (ks & 3) * 32) >> 4);
-    umma_ts(s_col, tmem + kTmemK + 8 * ks, b, kIdQK, acc);
+  template <int kAcc>
+  __device__ __forceinline__ void qk_step(int ks) {
+    umma_ts_w<kAcc>(s_col, tmem + kTmemK + 8 * ks,
+                    (uint32_t)qd + (uint32_t)((((ks >> 2) * NH * 128) + (ks & 3) * 32) >> 4), (uint32_t)(qd >> 32),
+                    kIdQK);
   }
   __device__ __forceinline__ void qk(int64_t k) {
     tc_fence_after();
     // half h: latent dims 256h..256h+255, then rope dims 32h..32h+31 (K-steps 32 + 2h, 33 + 2h)
+    qk_step<0>(16 * which);
 #pragma unroll
-    for (int x = 0; x < 16; ++x) qk_step(16 * which + x, x > 0 ? 1u : 0u);
-    qk_step(32 + 2 * which, 1u);
-    qk_step(33 + 2 * which, 1u);
+    for (int x = 1; x < 16; ++x) qk_step<1>(16 * which + x);
+    qk_step<1>(32 + 2 * which);
+    qk_step<1>(33 + 2 * which);
     umma_commit(&sm->kfree[which]);
     umma_commit(&sm->s_full);
   }
@@ -444,10 +447,15 @@ struct MmaIssuer {
 #pragma unroll
         for (int kk = 0; kk < 2; ++kk) {
           const int ks = 2 * w + kk;
-          const uint64_t a = vd + (uint64_t)((mb * 32768 + ks * 2048) >> 4);
-          const uint64_t bdesc = pd0 + (uint64_t)((ks * 2 * kPSbo) >> 4);
-          umma_ss(o_col + mb * NH, a, bdesc, kIdPV, (ti.first && ks == 0) ? 0u : 1u);
-          umma_ss(o_col + mb * NH, a, bdesc + (uint64_t)(kPBytes >> 4), kIdPV, 1u);
+          const uint32_t a_lo = (uint32_t)vd + (uint32_t)((mb * 32768 + ks * 2048) >> 4);
+          const uint32_t b_lo = (uint32_t)pd0 + (uint32_t)((ks * 2 * kPSbo) >> 4);
+          if (ks == 0)
+            umma_ss_w<-1>(o_col + mb * NH, a_lo, (uint32_t)(vd >> 32), b_lo, (uint32_t)(pd0 >> 32), kIdPV,
+                          ti.first ? 0u : 1u);
+          else
+            umma_ss_w<1>(o_col + mb * NH, a_lo, (uint32_t)(vd >> 32), b_lo, (uint32_t)(pd0 >> 32), kIdPV);
+          umma_ss_w<1>(o_col + mb * NH, a_lo, (uint32_t)(vd >> 32), b_lo + (kPBytes >> 4), (uint32_t)(pd0 >> 32),
+                       kIdPV);
         }
       }
       umma_commit(&sm->vfree[which][w]);

@@ -483,8 +483,8 @@ __device__ void mma_loop(const DecodeParams& p, Smem* sm, uint8_t* vtile, uint8_
     m.request_q(tile_info(p, t_begin, t_begin, t_end).unit);
     q_copies = 1;
   }
+  TileInfo ti = tile_info(p, t_begin, t_begin, t_end);
   for (int64_t k = 0; k < n; ++k) {
-    const TileInfo ti = tile_info(p, t_begin + k, t_begin, t_end);
     // ---- QK(k)
     bool ok = true;
     // issuer 0 also reads the rope atom of the q image, which issuer 1 copies in
@@ -494,8 +494,9 @@ __device__ void mma_loop(const DecodeParams& p, Smem* sm, uint8_t* vtile, uint8_
     if (ok && k > 0) ok = wait(sm, &sm->s_free, (uint32_t)((k - 1) & 1), p.status);
     if (!ok) break;
     m.qk(k);
+    TileInfo tn = ti;   // the next tile's info, computed here (off the PV -> QK path)
     if (k + 1 < n) {
-      const TileInfo tn = tile_info(p, t_begin + k + 1, t_begin, t_end);
+      tn = tile_info(p, t_begin + k + 1, t_begin, t_end);
       if (tn.first) {
         if (!wait(sm, &sm->kfree[which], (uint32_t)(k & 1), p.status)) break;
         // the rope atom that issuer 1 rewrites is read by issuer 0's QK(k) too
@@ -505,11 +506,13 @@ __device__ void mma_loop(const DecodeParams& p, Smem* sm, uint8_t* vtile, uint8_
       }
     }
     // ---- PV(k)
-    ok = wait(sm, &sm->p_full, (uint32_t)(k & 1), p.status);
-    if (ok) ok = wait(sm, &sm->v_ready[which], (uint32_t)(k & 1), p.status);
+    // the V half is normally in place well before P: test it first, off the P -> PV path
+    ok = wait(sm, &sm->v_ready[which], (uint32_t)(k & 1), p.status);
+    if (ok) ok = wait(sm, &sm->p_full, (uint32_t)(k & 1), p.status);
     if (ok && ti.first && k > 0) ok = wait(sm, &sm->o_free, (uint32_t)(m.ofree_waits & 1), p.status);
     if (!ok) break;
     m.pv(k, ti);
+    ti = tn;
   }
   // never leave with a q copy in flight (abort path)
   if (q_copies > (kCluster ? 1 : 0)) mbar_wait(&sm->q_full[which], (uint32_t)((q_copies - 1) & 1), nullptr, kWaitTimeoutNs);

@@ -201,7 +201,7 @@ __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64
 // descriptor's start-address field (bits 0..13, in 16-byte units) is added to the low half alone,
 // which no shared-memory address carries out of. kAcc: 1 = accumulate into D, 0 = overwrite D (both
 // written into the instruction), -1 = `accumulate` decides at run time. Every instruction saved
-// here counts: one thread issues a tile's UMMAs, and under load it issues them at ~140 cycles each.
+// here counts: one thread issues a half's UMMAs, one every ~60-85 cycles under load.
 template <int kAcc>
 __device__ __forceinline__ void umma_ss_w(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi, uint32_t b_lo,
                                           uint32_t b_hi, uint32_t idesc, uint32_t accumulate = 0) {

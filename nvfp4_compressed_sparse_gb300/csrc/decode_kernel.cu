@@ -77,10 +77,12 @@ struct alignas(16) Smem {
   // Half h of a tile = latent dims 256h..256h+255 and rope dims 32h..32h+31. Each half has
   // its own dequant warps and MMA issuer, so the two halves pipeline independently and only meet
   // in the softmax.
-  uint64_t vfree[2][4];              // PV of half h has finished reading V rows 32w..32w+31 (1 commit)
+  // Each issuer commits only where a waiter needs it (a commit costs the issuing thread time):
+  // once after its QK, once after its PV.
+  uint64_t vfree[2];                 // PV of half h complete: its V rows may be rewritten (1 commit)
   uint64_t kv_ready[2];              // half h of the K tile is in TMEM (4 dequant warps)
-  uint64_t kfree[2];                 // QK of half h complete: that half of the K tile may be rewritten
-  uint64_t s_full;                   // QK of both halves complete (2 commits)
+  uint64_t s_full;                   // QK of both halves complete (2 commits): S may be read, the K
+                                     // tile and the q image rewritten
   uint64_t s_free;                   // softmax has read S of a tile (4 warps): S may be overwritten
   uint64_t v_ready[2];               // half h of the V rows of a tile is in shared memory (4 warps)
   uint64_t mask_full[2];             // vmask of a tile written (4 warps), by tile parity
@@ -247,8 +249,8 @@ __device__ void dequant_loop(const DecodeParams& p, Smem* sm, uint8_t* ring, uin
     bool good = true;
     if (lane == 0) {
       good = wait(sm, &sm->ring_full[q], (uint32_t)(k & 1), p.status);
-      // this half of the K tile may be rewritten once the previous tile's QK of the half is done
-      if (good && k > 0) good = wait(sm, &sm->kfree[half], (uint32_t)((k - 1) & 1), p.status);
+      // the K tile may be rewritten once the previous tile's QK (both halves) is done
+      if (good && k > 0) good = wait(sm, &sm->s_full, (uint32_t)((k - 1) & 1), p.status);
     }
     good = __shfl_sync(0xffffffffu, good, 0);
     if (!good) break;
@@ -345,7 +347,7 @@ __device__ void dequant_loop(const DecodeParams& p, Smem* sm, uint8_t* ring, uin
       }
     }
     // ---- pass B: latent K rows (TMEM) -> V rows (shared memory, SW128 K-major atoms)
-    if (lane == 0) good = wait(sm, &sm->vfree[half][q], (uint32_t)((k & 1) ^ 1), p.status);
+    if (lane == 0) good = wait(sm, &sm->vfree[half], (uint32_t)((k & 1) ^ 1), p.status);
     good = __shfl_sync(0xffffffffu, good, 0);
     if (!good) break;
     __syncwarp();
@@ -430,15 +432,15 @@ struct MmaIssuer {
     for (int x = 1; x < 16; ++x) qk_step<1>(16 * which + x);
     qk_step<1>(32 + 2 * which);
     qk_step<1>(33 + 2 * which);
-    umma_commit(&sm->kfree[which]);
     umma_commit(&sm->s_full);
   }
 
   __device__ __forceinline__ void pv(int64_t k, const TileInfo& ti) {
     if (ti.first && k > 0) ++ofree_waits;
     tc_fence_after();
-    // P_hi and P_lo planes: the same V rows times each, into the same fp32 accumulator.
-    // Row chunk w (tokens 32w..) of this half is released as soon as its UMMAs complete.
+    // P_hi and P_lo planes: the same V rows times each, into the same fp32 accumulator. The half's
+    // V rows are released when all of its UMMAs complete (releasing each 32-row chunk as soon as
+    // its own UMMAs completed took three more commits per tile and measured slower).
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
 #pragma unroll
@@ -458,8 +460,8 @@ struct MmaIssuer {
                        kIdPV);
         }
       }
-      umma_commit(&sm->vfree[which][w]);
     }
+    umma_commit(&sm->vfree[which]);
     if (ti.last) umma_commit(&sm->o_done);
   }
 };
@@ -498,9 +500,8 @@ __device__ void mma_loop(const DecodeParams& p, Smem* sm, uint8_t* vtile, uint8_
     if (k + 1 < n) {
       tn = tile_info(p, t_begin + k + 1, t_begin, t_end);
       if (tn.first) {
-        if (!wait(sm, &sm->kfree[which], (uint32_t)(k & 1), p.status)) break;
-        // the rope atom that issuer 1 rewrites is read by issuer 0's QK(k) too
-        if (which == 1 && !wait(sm, &sm->kfree[0], (uint32_t)(k & 1), p.status)) break;
+        // both halves' QK(k) have finished reading the q buffer
+        if (!wait(sm, &sm->s_full, (uint32_t)(k & 1), p.status)) break;
         m.request_q(tn.unit);
         ++q_copies;
       }
@@ -696,8 +697,8 @@ __device__ bool softmax_loop(const DecodeParams& p, Smem* sm, uint8_t* ps, uint8
     // ---- a raised reference: O^T[dim, h] *= alpha[h] before PV(k) adds to it, once PV(k-1) has
     // finished accumulating (P above did not have to wait for this)
     if (raise && sm->need_rescale && !ti.first) {
-      if (lane == 0 && wait(sm, &sm->vfree[0][3], (uint32_t)((k - 1) & 1), p.status))
-        wait(sm, &sm->vfree[1][3], (uint32_t)((k - 1) & 1), p.status);
+      if (lane == 0 && wait(sm, &sm->vfree[0], (uint32_t)((k - 1) & 1), p.status))
+        wait(sm, &sm->vfree[1], (uint32_t)((k - 1) & 1), p.status);
       __syncwarp();
       tc_fence_after();
 #pragma unroll 1
@@ -904,9 +905,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     mbar_init(&sm->rows_full[0], 2);
     mbar_init(&sm->rows_empty[0], 4);
     for (int h = 0; h < 2; ++h) {
-      for (int i = 0; i < 4; ++i) mbar_init(&sm->vfree[h][i], 1);
+      mbar_init(&sm->vfree[h], 1);
       mbar_init(&sm->kv_ready[h], 4);
-      mbar_init(&sm->kfree[h], 1);
       mbar_init(&sm->v_ready[h], 4);
       mbar_init(&sm->mask_full[h], 4);
     }

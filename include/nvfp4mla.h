@@ -227,8 +227,8 @@ int sparse_mla_decode(const void* q, const void* kv_cache, int64_t num_pages, co
  * half 1 also the rope dims), the two exchange their partial scores every
  * 128-row tile through distributed shared memory, and the freed on-chip
  * memory double-buffers K and S and lets PV read V once for both parts of P.
- * Measured on GB300 (headline rows, L2 flushed): 66.9 vs 50.1 us for 64
- * queries, 33.7 vs 29.5 us for 16, 23.5 vs 21.4 us for 4, 21.4 vs 21.1 for 1; each
+ * Measured on GB300 (headline rows, L2 flushed): 67.7 vs 50.0 us for 64
+ * queries, 33.6 vs 29.6 us for 16, 23.4 vs 21.5 us for 4, 21.7 vs 21.0 for 1; each
  * SM then runs the softmax of twice as many tile visits, and the exchange
  * adds a dependency between the CTAs every tile.
  *   B, Q, H, topk     as for sparse_mla_decode

@@ -83,13 +83,11 @@ struct alignas(16) Smem {
   uint64_t kv_ready[2];              // half h of the K tile is in TMEM (4 dequant warps)
   uint64_t s_full;                   // QK of both halves complete (2 commits): S may be read, the K
                                      // tile and the q image rewritten
-  uint64_t s_free;                   // softmax has read S of a tile (4 warps): S may be overwritten
   uint64_t v_ready[2];               // half h of the V rows of a tile is in shared memory (4 warps)
   uint64_t mask_full[2];             // vmask of a tile written (4 warps), by tile parity
   // P of a tile written and O rescaled (128 threads). One P buffer serves every tile: P(k+1) is
   // written after QK(k+1) completes, which each issuer queued behind its PV(k).
   uint64_t p_full;
-  uint64_t o_done;                   // last PV of a unit segment complete (2 issuers)
   uint64_t o_free;                   // epilogue has read O (128 threads)
   uint64_t q_full[2];                // half h of the unit's q image copied in (issuer h's copy)
   uint64_t drain;                    // every UMMA of both issuers complete
@@ -462,7 +460,6 @@ struct MmaIssuer {
       }
     }
     umma_commit(&sm->vfree[which]);
-    if (ti.last) umma_commit(&sm->o_done);
   }
 };
 
@@ -493,7 +490,8 @@ __device__ void mma_loop(const DecodeParams& p, Smem* sm, uint8_t* vtile, uint8_
     if (ti.first) ok = wait(sm, &sm->q_full[which], (uint32_t)((q_copies - 1) & 1), p.status);
     if (ok && ti.first && which == 0) ok = wait(sm, &sm->q_full[1], (uint32_t)((q_copies - 1) & 1), p.status);
     if (ok) ok = wait(sm, &sm->kv_ready[which], (uint32_t)(k & 1), p.status);
-    if (ok && k > 0) ok = wait(sm, &sm->s_free, (uint32_t)((k - 1) & 1), p.status);
+    // (S of tile k-1 has been read: the softmax writes P(k-1) after reading it, and this thread
+    // waited for P(k-1) before issuing PV(k-1))
     if (!ok) break;
     m.qk(k);
     TileInfo tn = ti;   // the next tile's info, computed here (off the PV -> QK path)
@@ -559,7 +557,6 @@ __device__ bool softmax_loop(const DecodeParams& p, Smem* sm, uint8_t* ps, uint8
   const uint32_t s_col = kTmemS, o_col = kTmemS + 2 * NH;
   const float kNegInf = __int_as_float(0xff800000);
   float l_part[32];
-  int64_t seg = 0;
   bool ok = true;
   if constexpr (!kCluster) asm volatile("griddepcontrol.wait;" ::: "memory");   // qscale comes from the prep kernel
   for (int64_t g = t_begin; g < t_end && ok; ++g) {
@@ -659,9 +656,7 @@ __device__ bool softmax_loop(const DecodeParams& p, Smem* sm, uint8_t* ps, uint8
         l_part[h] *= av.x; l_part[h + 1] *= av.y; l_part[h + 2] *= av.z; l_part[h + 3] *= av.w;
       }
     }
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sm->s_free);      // S read: the next QK and K tile may proceed
+    tc_fence_before();   // S read (its reuse by the next QK is ordered by the P barrier below)
     // ---- P = 2^(z - m) as two fp16 parts, P_hi = fp16(p) and P_lo = fp16(p - P_hi), rows of the two
     // P planes (MN-major: heads contiguous); PV multiplies V by both and accumulates them in fp32,
     // so the weights carry ~22 bits instead of fp16's 11. (With P_hi alone, the rounding of a few
@@ -722,7 +717,9 @@ __device__ bool softmax_loop(const DecodeParams& p, Smem* sm, uint8_t* ps, uint8
 
     if (ti.last) {
       // ---- epilogue: write this segment's unnormalised partial
-      if (lane == 0) wait(sm, &sm->o_done, (uint32_t)(seg & 1), p.status);
+      // O is final once both halves' PV of this tile has completed
+      if (lane == 0 && wait(sm, &sm->vfree[0], (uint32_t)(k & 1), p.status))
+        wait(sm, &sm->vfree[1], (uint32_t)(k & 1), p.status);
       if (named_sync_softmax_any(sm->abort != 0)) {
         ok = false;
         break;
@@ -767,7 +764,6 @@ __device__ bool softmax_loop(const DecodeParams& p, Smem* sm, uint8_t* ps, uint8
       tc_fence_before();
       mbar_arrive(&sm->o_free);
       named_sync_softmax();
-      ++seg;
     }
   }
   return ok;
@@ -911,9 +907,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       mbar_init(&sm->mask_full[h], 4);
     }
     mbar_init(&sm->s_full, 2);
-    mbar_init(&sm->s_free, 4);
     mbar_init(&sm->p_full, 128);
-    mbar_init(&sm->o_done, 2);
     mbar_init(&sm->o_free, 128);
     mbar_init(&sm->q_full[0], kCluster ? 384 : 1);   // cluster mode: the converting threads
     mbar_init(&sm->q_full[1], kCluster ? 384 : 1);

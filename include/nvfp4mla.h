@@ -216,15 +216,15 @@ int sparse_mla_decode(const void* q, const void* kv_cache, int64_t num_pages, co
  *     sequence cut into *ctas contiguous ranges (one CTA per SM); a q-prep
  *     grid runs before it and a merge grid combines the partials.
  * Without flags the split schedule is used: on GB300 it measured faster at
- * every size tried (64 queries: 54.2 vs 55.6 us with 2-CTA clusters; 128
- * queries: 93.9 vs 96.9 us with 1-CTA clusters; 1 and 4 queries: ~8 us faster
- * than 8-CTA clusters). NVFP4MLA_FLAG_CLUSTER takes the cluster schedule when
+ * every size tried (64 queries: 50.0 vs 52.8 us with 2-CTA clusters; 128
+ * queries, an earlier build: 93.9 vs 96.9 us with 1-CTA clusters; 1 and 4
+ * queries: ~6 us faster than 8-CTA clusters). NVFP4MLA_FLAG_CLUSTER takes the cluster schedule when
  * one wave of clusters fits and no CTA runs more 128-row tiles than under the
  * split schedule; NVFP4MLA_FLAG_CLUSTER_ANY whenever one wave fits.
  * A third, opt-in schedule (NVFP4MLA_FLAG_PAIR, *cluster = -2) runs the
  * split schedule's ranges on 2-CTA clusters (*ctas = 2 x SMs / 2): CTA h of a
- * pair holds half h of the 576-wide contraction (latent dims 256h..256h+255,
- * half 1 also the rope dims), the two exchange their partial scores every
+ * pair holds half h of the 576-wide contraction (latent dims 256h..256h+255
+ * and rope dims 32h..32h+31), the two exchange their partial scores every
  * 128-row tile through distributed shared memory, and the freed on-chip
  * memory double-buffers K and S and lets PV read V once for both parts of P.
  * Measured on GB300 (headline rows, L2 flushed): 67.7 vs 50.0 us for 64
